@@ -1,0 +1,205 @@
+"""Python binding of the NWC C ABI (``include/nwc.h``, ``_build/libnwc.so``).
+
+Argument marshalling only: every step of encode, decode, gather and the fused
+decode-GEMV runs in the library (host encoder in C++, sm_103a kernels). PyTorch
+supplies device memory and streams. There is no fallback: if the library is
+missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "BF16", "FP8", "NwcError", "lib", "encode", "encode_fp8", "quantize_fp8", "validate",
+    "Matrix", "check", "sm_count", "status_str",
+]
+
+BF16, FP8 = 0, 1
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libnwc.so")
+
+
+class NwcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_str(status) if _lib else status} ({status})")
+        self.status = status
+
+
+class NwcMatrix(ctypes.Structure):
+    """Mirror of struct nwc_matrix."""
+    _fields_ = [
+        ("elem", ctypes.c_int32), ("n_ranked", ctypes.c_int32),
+        ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+        ("row_blocks", ctypes.c_int64), ("col_blocks", ctypes.c_int64),
+        ("rank_exp", ctypes.c_uint8 * 16),
+        ("block_tab", ctypes.c_void_p), ("data", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+        ("blob_bytes", ctypes.c_uint64), ("max_block_bytes", ctypes.c_uint64),
+        ("data_bytes", ctypes.c_uint64),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libnwc.so (built by ``__graft_entry__.build()`` / ``build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libnwc.so not built ({LIB_PATH}); run decode_gemv_nwc_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    p, i64, u64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+    L.nwc_status_str.argtypes = [i32]
+    L.nwc_status_str.restype = ctypes.c_char_p
+    L.nwc_version.restype = ctypes.c_char_p
+    L.nwc_encode.argtypes = [p, i64, i64, i64, i32, i32, p, ctypes.POINTER(sz)]
+    L.nwc_encode_fp8.argtypes = [p, p, i64, i64, i64, i32, p, ctypes.POINTER(sz)]
+    L.nwc_quantize_fp8.argtypes = [p, i64, i64, i64, p, i64, p]
+    L.nwc_validate.argtypes = [p, sz]
+    L.nwc_bind.argtypes = [p, sz, p, ctypes.POINTER(NwcMatrix)]
+    L.nwc_decode.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, p]
+    L.nwc_gemv_workspace_bytes.argtypes = [ctypes.POINTER(NwcMatrix)]
+    L.nwc_gemv_workspace_bytes.restype = sz
+    L.nwc_gemv.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, p]
+    L.nwc_gather.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, i64, p]
+    L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+    L.nwc_sm_count.restype = i32
+    for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
+                 "nwc_decode", "nwc_gemv", "nwc_gather", "nwc_check"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def status_str(status: int) -> str:
+    return lib().nwc_status_str(int(status)).decode()
+
+
+def _ok(status: int, what: str):
+    if status != 0:
+        raise NwcError(status, what)
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def encode(w_bits: np.ndarray, elem: int = BF16, threads: int = 0) -> bytes:
+    """Host encoder: (N, K) BF16 bit patterns (uint16, any row stride) -> blob."""
+    w = np.asarray(w_bits)
+    if w.dtype != np.uint16 or w.ndim != 2 or w.strides[1] != 2:
+        w = np.ascontiguousarray(w, dtype=np.uint16)
+    n, k = w.shape
+    ld = w.strides[0] // 2
+    size = ctypes.c_size_t(0)
+    _ok(lib().nwc_encode(_np_ptr(w), n, k, ld, elem, threads, None, ctypes.byref(size)), "nwc_encode")
+    out = np.empty(size.value, np.uint8)
+    _ok(lib().nwc_encode(_np_ptr(w), n, k, ld, elem, threads, _np_ptr(out), ctypes.byref(size)), "nwc_encode")
+    return out.tobytes()
+
+
+def encode_fp8(q: np.ndarray, scales: np.ndarray, threads: int = 0) -> bytes:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.float32)
+    n, k = q.shape
+    size = ctypes.c_size_t(0)
+    _ok(lib().nwc_encode_fp8(_np_ptr(q), _np_ptr(s), n, k, k, threads, None, ctypes.byref(size)), "nwc_encode_fp8")
+    out = np.empty(size.value, np.uint8)
+    _ok(lib().nwc_encode_fp8(_np_ptr(q), _np_ptr(s), n, k, k, threads, _np_ptr(out), ctypes.byref(size)),
+        "nwc_encode_fp8")
+    return out.tobytes()
+
+
+def quantize_fp8(w_bits: np.ndarray):
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    n, k = w.shape
+    q = np.empty((n, k), np.uint8)
+    s = np.empty(n, np.float32)
+    _ok(lib().nwc_quantize_fp8(_np_ptr(w), n, k, k, _np_ptr(q), k, _np_ptr(s)), "nwc_quantize_fp8")
+    return q, s
+
+
+def validate(blob: bytes) -> int:
+    b = np.frombuffer(blob, np.uint8)
+    return int(lib().nwc_validate(_np_ptr(b), len(blob)))
+
+
+def sm_count() -> int:
+    return int(lib().nwc_sm_count())
+
+
+def check(stream=None):
+    """(status, flags) of the device error word; synchronizes the stream."""
+    flags = ctypes.c_uint32(0)
+    st = lib().nwc_check(_stream_ptr(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)
+
+
+class Matrix:
+    """A blob resident in device memory and bound through nwc_bind.
+
+    ``device_blob`` is a torch uint8 CUDA tensor holding the blob (caller-visible so that
+    benchmarks can keep several copies); the GEMV workspace is allocated once, zeroed, and
+    reused by every call.
+    """
+
+    def __init__(self, blob: bytes, device="cuda", device_blob=None):
+        import torch
+        host = np.frombuffer(blob, np.uint8)
+        if device_blob is None:
+            device_blob = torch.from_numpy(host.copy()).to(device)
+        self.device_blob = device_blob
+        self.m = NwcMatrix()
+        _ok(lib().nwc_bind(_np_ptr(host), len(blob), ctypes.c_void_p(device_blob.data_ptr()), ctypes.byref(self.m)),
+            "nwc_bind")
+        self.elem, self.n, self.k = self.m.elem, self.m.n, self.m.k
+        self.blob_bytes = len(blob)
+        ws = int(lib().nwc_gemv_workspace_bytes(ctypes.byref(self.m)))
+        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device_blob.device)
+        self.ws_bytes = ws
+
+    def gemv(self, x, y=None, stream=None):
+        """y (float32[N]) = W x for x a BF16 vector given as an int16/bfloat16 CUDA tensor."""
+        import torch
+        assert x.numel() == self.k and x.is_cuda and x.is_contiguous()
+        if y is None:
+            y = torch.empty(self.n, dtype=torch.float32, device=x.device)
+        _ok(lib().nwc_gemv(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+                           ctypes.c_void_p(self.workspace.data_ptr()) if self.ws_bytes else None, self.ws_bytes,
+                           _stream_ptr(stream)), "nwc_gemv")
+        return y
+
+    def decode(self, out=None, stream=None):
+        """Stored elements: int16 (BF16 bits) [N, K], or (uint8 e4m3 [N, K], float32 scales [N])."""
+        import torch
+        dev = self.device_blob.device
+        if self.elem == BF16:
+            out = out if out is not None else torch.empty((self.n, self.k), dtype=torch.int16, device=dev)
+            _ok(lib().nwc_decode(ctypes.byref(self.m), ctypes.c_void_p(out.data_ptr()), out.stride(0), None,
+                                 _stream_ptr(stream)), "nwc_decode")
+            return out
+        out = out if out is not None else torch.empty((self.n, self.k), dtype=torch.uint8, device=dev)
+        scales = torch.empty(self.n, dtype=torch.float32, device=dev)
+        _ok(lib().nwc_decode(ctypes.byref(self.m), ctypes.c_void_p(out.data_ptr()), out.stride(0),
+                             ctypes.c_void_p(scales.data_ptr()), _stream_ptr(stream)), "nwc_decode")
+        return out, scales
+
+    def gather(self, ids, out=None, stream=None):
+        """Rows ids (int32 CUDA tensor) of the stored matrix, bit-exact."""
+        import torch
+        assert ids.dtype == torch.int32 and ids.is_cuda and ids.is_contiguous()
+        dt = torch.int16 if self.elem == BF16 else torch.uint8
+        out = out if out is not None else torch.empty((ids.numel(), self.k), dtype=dt, device=ids.device)
+        _ok(lib().nwc_gather(ctypes.byref(self.m), ctypes.c_void_p(ids.data_ptr()), ids.numel(),
+                             ctypes.c_void_p(out.data_ptr()), out.stride(0), _stream_ptr(stream)), "nwc_gather")
+        return out

@@ -1,0 +1,747 @@
+// kernels.cu -- sm_103a kernels and C-ABI launchers: decode to BF16/e4m3, embedding gather,
+// and the fused decode-GEMV.
+//
+// "NWC -- Neural Weight Compression", section "How it works":
+//   * each lane decodes its own bit stream for a block of 8 rows x 512 columns (16 columns
+//     x 8 rows per lane), keeps the 16 matching activations in registers and accumulates
+//     eight row sums; a transposed shuffle reduction produces partial sums per (row, column
+//     block);
+//   * a 12-bit peek into a 16 KB shared-memory lookup table yields two complete codes per
+//     step; the bit window is shifted and refilled from the lane's words;
+//   * dequantization and embedding lookup run on the same decoder.
+// "Qwen3-4B-NWC-fp8": the per-channel scale is applied at the end of the matvec.
+//
+// GB300 choices: the GEMV is a persistent grid sized from the queried SM count; each warp
+// streams whole block regions (counts, code streams, mantissas) from HBM into its own
+// double-buffered shared-memory stage with one TMA bulk copy (cp.async.bulk, completion on an
+// mbarrier, bounded waits); the LUT entry carries both codes as BF16 high halves so that one
+// LOP3 merges a row pair's two raw mantissas (stored 16 bits apart) into a BF16x2; products
+// accumulate with packed FP32 FMA (FFMA2). Cross-column-block sums are done by the last warp
+// to finish a row block (one counter per row block, reset by that warp), in a fixed order.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "nwc.h"
+#include "nwc_format.h"
+
+using namespace nwcf;
+
+// Device error word: bit 0 = malformed stream (a lane read past its words), bit 1 = gather
+// id out of range, bit 2 = a bounded wait ran out. Read and cleared by nwc_check.
+__device__ uint32_t g_nwc_error;
+
+namespace {
+
+constexpr uint32_t kErrFormat = 1u, kErrId = 2u, kErrTimeout = 4u;
+constexpr uint32_t kFlagGen = 1u << 6;  // LUT entry: decode this pair with the generic path
+
+struct Mat {
+    int elem, nr;
+    uint64_t n, k, rbs, cbs, nb;
+    const uint32_t *tab;
+    const uint8_t *data;
+    const float *scales;
+    uint8_t rank_exp[16];
+};
+
+Mat to_mat(const nwc_matrix &m) {
+    Mat t;
+    t.elem = m.elem;
+    t.nr = m.n_ranked;
+    t.n = (uint64_t)m.n;
+    t.k = (uint64_t)m.k;
+    t.rbs = (uint64_t)m.row_blocks;
+    t.cbs = (uint64_t)m.col_blocks;
+    t.nb = t.rbs * t.cbs;
+    t.tab = m.block_tab;
+    t.data = m.data;
+    t.scales = m.scales;
+    for (int i = 0; i < 16; i++) t.rank_exp[i] = m.rank_exp[i];
+    return t;
+}
+
+__device__ __forceinline__ void raise_error(uint32_t bits) { atomicOr(&g_nwc_error, bits); }
+
+// Copies the rank table into shared memory without indexing the kernel parameter
+// dynamically (which would spill the whole parameter struct to local memory).
+__device__ __forceinline__ void load_rank_table(const Mat &m, uint8_t *rexp) {
+    if (threadIdx.x < 16) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            if ((int)threadIdx.x == i) v = m.rank_exp[i];
+        rexp[threadIdx.x] = (uint8_t)v;
+    }
+}
+
+// ------------------------------------------------------------------ lane bit stream
+// 64-bit window, most significant bit = next stream bit; nb valid bits at the top.
+struct LaneStream {
+    const uint32_t *p;
+    uint32_t left, nwords, inserted;
+    int nb;
+    uint64_t win;
+
+    __device__ __forceinline__ void init(const uint32_t *ptr, uint32_t n) {
+        p = ptr;
+        left = n;
+        nwords = n;
+        inserted = 0;
+        nb = 0;
+        win = 0;
+        refill();
+        refill();
+    }
+    // Ensures at least 33 valid bits. Past the lane's last word, zero words are inserted
+    // without reading memory; overrun() reports whether such bits were consumed.
+    __device__ __forceinline__ void refill() {
+        if (nb <= 32) {
+            uint32_t w = 0;
+            if (left) {
+                w = *p;
+                p++;
+                left--;
+            }
+            win |= (uint64_t)w << (32 - nb);
+            nb += 32;
+            inserted++;
+        }
+    }
+    __device__ __forceinline__ void consume(int L) {
+        win <<= L;
+        nb -= L;
+    }
+    __device__ __forceinline__ bool overrun() const {
+        return (uint64_t)inserted * 32u - (uint64_t)nb > (uint64_t)nwords * 32u;
+    }
+};
+
+// One code: rank p < nr is p ones, a zero, the sign; an escape is nr ones, the raw exponent
+// (EB bits, most significant first), the sign.
+template <int ELEM>
+__device__ __forceinline__ void decode_one(LaneStream &ls, int nr, const uint8_t *rexp, uint32_t &s,
+                                           uint32_t &v) {
+    constexpr int EB = ELEM == 0 ? 8 : 4;
+    ls.refill();
+    const uint32_t top = (uint32_t)(ls.win >> 32);
+    const int ones = __clz(~top);
+    int L;
+    if (ones < nr) {
+        v = rexp[ones];
+        s = (top >> (30 - ones)) & 1u;
+        L = ones + 2;
+    } else {
+        v = (top << nr) >> (32 - EB);
+        s = (top >> (31 - nr - EB)) & 1u;
+        L = nr + EB + 1;
+    }
+    ls.consume(L);
+}
+
+// Field j of the even (odd = 0) or odd (odd = 1) mantissa half-stream of a lane region.
+template <int F>
+__device__ __forceinline__ uint32_t half_field(const uint32_t *man, int odd, uint32_t j) {
+    const uint32_t bit = (uint32_t)F * j, k = bit >> 4, o = bit & 15u;
+    uint32_t w = man[k];
+    uint32_t h = odd ? (w >> 16) : (w & 0xFFFFu);
+    if (o + F > 16) {
+        uint32_t w1 = man[k + 1];
+        h |= (odd ? (w1 >> 16) : (w1 & 0xFFFFu)) << 16;
+    }
+    return (h >> o) & ((1u << F) - 1u);
+}
+
+// Element value as FP32 from its fields.
+template <int ELEM>
+__device__ __forceinline__ float elem_value(uint32_t s, uint32_t v, uint32_t m) {
+    if (ELEM == 0) return __uint_as_float(((s << 15) | (v << 7) | m) << 16);
+    // e4m3: bias 7, subnormals at v == 0, S.1111.111 is NaN
+    if (v == 0) {
+        float f = (float)m * 0.001953125f;  // m * 2^-9, exact
+        return s ? -f : f;
+    }
+    if (v == 15 && m == 7) return __uint_as_float(0x7FC00000u);
+    return __uint_as_float((s << 31) | ((v + 120u) << 23) | (m << 20));
+}
+
+template <int ELEM>
+__device__ __forceinline__ uint32_t elem_bits(uint32_t s, uint32_t v, uint32_t m) {
+    return ELEM == 0 ? ((s << 15) | (v << 7) | m) : ((s << 7) | (v << 3) | m);
+}
+
+// Generic decode of one lane of one block: calls fn(t, s, v, m) for each real element t
+// (t = 8c + r, both static after unrolling). rows/cols are the lane's real extent.
+template <int ELEM, class Fn>
+__device__ __forceinline__ void lane_generic(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
+                                             const uint8_t *rexp, Fn &&fn) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    uint32_t je = 0, jo = 0;
+#pragma unroll
+    for (int t = 0; t < kSyms; t++) {
+        const int c = t >> 3, r = t & 7;
+        uint32_t s, v;
+        decode_one<ELEM>(ls, nr, rexp, s, v);
+        if (r < rows && c < cols) {
+            uint32_t m;
+            if (r & 1) m = half_field<F>(man, 1, jo++);
+            else m = half_field<F>(man, 0, je++);
+            fn(t, s, v, m);
+        }
+    }
+}
+
+// Layout facts of one block region at `reg` for this lane.
+struct LaneRegion {
+    const uint32_t *code, *man;
+    uint32_t nwords;
+};
+
+__device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, int lane, int rows, uint64_t k,
+                                                  uint64_t cb, int F) {
+    const uint32_t lw = reg[lane];
+    uint32_t incl = lw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    LaneRegion lr;
+    lr.code = reinterpret_cast<const uint32_t *>(reg + 32) + (incl - lw);
+    lr.nwords = lw;
+    // mantissa regions in lane order; sizes from the real extents of lanes before this one
+    uint32_t mw = man_words(rows, real_cols(k, cb, lane), F);
+    uint32_t mincl = mw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, mincl, d);
+        if (lane >= d) mincl += o;
+    }
+    lr.man = reinterpret_cast<const uint32_t *>(reg + up16(32 + 4 * (uint64_t)total)) + (mincl - mw);
+    return lr;
+}
+
+// =================================================================== decode kernel
+template <int ELEM>
+__global__ void __launch_bounds__(256) decode_kernel(Mat m, void *out, int64_t ld_out) {
+    __shared__ uint8_t rexp[16];
+    load_rank_table(m, rexp);
+    __syncthreads();
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    const int lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    for (uint64_t b = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < m.nb; b += warps) {
+        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
+        const int rows = real_rows(m.n, rb), cols = real_cols(m.k, cb, lane);
+        const uint8_t *reg = m.data + 16 * (uint64_t)m.tab[b];
+        LaneRegion lr = lane_region(reg, lane, rows, m.k, cb, F);
+        LaneStream ls;
+        ls.init(lr.code, lr.nwords);
+        uint32_t o[8][8];  // [row][column pair] two elements per word (BF16) / [row][4 bytes]
+#pragma unroll
+        for (int r = 0; r < 8; r++)
+#pragma unroll
+            for (int i = 0; i < 8; i++) o[r][i] = 0;
+        lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
+            const int c = t >> 3, r = t & 7;
+            const uint32_t e = elem_bits<ELEM>(s, v, mm);
+            if (ELEM == 0) o[r][c >> 1] |= e << (16 * (c & 1));
+            else o[r][c >> 2] |= e << (8 * (c & 3));
+        });
+        if (ls.overrun()) raise_error(kErrFormat);
+        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
+#pragma unroll
+        for (int r = 0; r < 8; r++) {
+            if (r >= rows) break;
+            const uint64_t row = rb * kRows + (uint64_t)r;
+            if (ELEM == 0) {
+                uint16_t *dst = static_cast<uint16_t *>(out) + row * (uint64_t)ld_out + col0;
+                if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[r][0], o[r][1], o[r][2], o[r][3]);
+                    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[r][4], o[r][5], o[r][6], o[r][7]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; c++)
+                        if (c < cols) dst[c] = (uint16_t)(o[r][c >> 1] >> (16 * (c & 1)));
+                }
+            } else {
+                uint8_t *dst = static_cast<uint8_t *>(out) + row * (uint64_t)ld_out + col0;
+                if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[r][0], o[r][1], o[r][2], o[r][3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 16; c++)
+                        if (c < cols) dst[c] = (uint8_t)(o[r][c >> 2] >> (8 * (c & 3)));
+                }
+            }
+        }
+    }
+}
+
+// =================================================================== gather kernel
+template <int ELEM>
+__global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, int64_t n_ids, void *out,
+                                                     int64_t ld_out) {
+    __shared__ uint8_t rexp[16];
+    load_rank_table(m, rexp);
+    __syncthreads();
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    const int lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    const uint64_t items = (uint64_t)n_ids * m.cbs;
+    for (uint64_t it = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+        const uint64_t i = it / m.cbs, cb = it % m.cbs;
+        const int64_t id = ids[i];
+        const int cols = real_cols(m.k, cb, lane);
+        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
+        uint32_t o[8];
+#pragma unroll
+        for (int c = 0; c < 8; c++) o[c] = 0;
+        if (id < 0 || (uint64_t)id >= m.n) {
+            if (lane == 0 && cb == 0) raise_error(kErrId);
+        } else {
+            const uint64_t rb = (uint64_t)id >> 3;
+            const int want = (int)(id & 7);
+            const int rows = real_rows(m.n, rb);
+            const uint8_t *reg = m.data + 16 * (uint64_t)m.tab[rb * m.cbs + cb];
+            LaneRegion lr = lane_region(reg, lane, rows, m.k, cb, F);
+            LaneStream ls;
+            ls.init(lr.code, lr.nwords);
+            lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
+                const int c = t >> 3, r = t & 7;
+                if (r == want) {
+                    const uint32_t e = elem_bits<ELEM>(s, v, mm);
+                    if (ELEM == 0) o[c >> 1] |= e << (16 * (c & 1));
+                    else o[c >> 2] |= e << (8 * (c & 3));
+                }
+            });
+            if (ls.overrun()) raise_error(kErrFormat);
+        }
+        if (ELEM == 0) {
+            uint16_t *dst = static_cast<uint16_t *>(out) + i * (uint64_t)ld_out + col0;
+            if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+                for (int c = 0; c < cols; c++) dst[c] = (uint16_t)(o[c >> 1] >> (16 * (c & 1)));
+            }
+        } else {
+            uint8_t *dst = static_cast<uint8_t *>(out) + i * (uint64_t)ld_out + col0;
+            if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                for (int c = 0; c < cols; c++) dst[c] = (uint8_t)(o[c >> 2] >> (8 * (c & 3)));
+            }
+        }
+    }
+}
+
+// =================================================================== GEMV kernel
+constexpr int kGemvWarps = 16;
+constexpr int kStageBytes = 6144;
+constexpr int kLutBytes = 4096 * 4;
+constexpr int kRexpOff = kLutBytes;
+constexpr int kBarOff = kRexpOff + 16;
+constexpr int kStageOff = 16768;  // 128-aligned, after LUT, rank table and 2 barriers/warp
+constexpr int kGemvSmem = kStageOff + kGemvWarps * 2 * kStageBytes;
+static_assert(kBarOff + kGemvWarps * 2 * 8 <= kStageOff, "smem layout");
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after about 2^32 SM clocks (1-3 s) and reports failure.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try(bar, phase)) return true;
+        if (clock64() - t0 > (1ll << 32)) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// LUT entry for a 12-bit peek P (first stream bit = bit 11): both codes complete give
+// hi1 | hi2 << 16 | (L1 + L2), where hi = BF16 high part (s << 15 | exponent << 7); anything
+// else (escape, second code cut off, fp8 subnormal/NaN-capable exponents) is kFlagGen.
+template <int ELEM>
+__device__ uint32_t lut_entry(uint32_t P, int nr, const uint8_t *rexp) {
+    const uint32_t bits = P << 20;
+    const int ones1 = __clz(~bits);
+    if (ones1 >= nr) return kFlagGen;
+    const int L1 = ones1 + 2;
+    const uint32_t s1 = (bits >> (30 - ones1)) & 1u, v1 = rexp[ones1];
+    const uint32_t rest = bits << L1;
+    const int avail = 12 - L1;
+    const int ones2 = __clz(~rest);
+    if (ones2 >= nr || ones2 + 2 > avail) return kFlagGen;
+    const uint32_t s2 = (rest >> (30 - ones2)) & 1u, v2 = rexp[ones2];
+    const int L = L1 + ones2 + 2;
+    if (ELEM == 0) return (s1 << 15) | (v1 << 7) | (((s2 << 15) | (v2 << 7)) << 16) | (uint32_t)L;
+    if (v1 == 0 || v1 == 15 || v2 == 0 || v2 == 15) return kFlagGen;
+    return (s1 << 15) | ((v1 + 120u) << 7) | (((s2 << 15) | ((v2 + 120u) << 7)) << 16) | (uint32_t)L;
+}
+
+// Pair p's two mantissas (even t at bits 0.., odd t at bits 16..) from a full lane's words.
+template <int F>
+__device__ __forceinline__ uint32_t xpair(const uint32_t *mw, int p) {
+    const int bit = F * p, k = bit >> 4, o = bit & 15;
+    if (o + F <= 16) return mw[k] >> o;
+    const uint32_t M = (0xFFFFu >> o) * 0x10001u;
+    return ((mw[k] >> o) & M) | ((mw[k + 1] << (16 - o)) & ~M);
+}
+
+// Transposed reduction of acc[8] over the 32 lanes: afterwards lanes with (lane & 3) == 0
+// hold the sum of row rowsel(lane) = bit4<<2 | bit3<<1 | bit2 of the lane id.
+__device__ __forceinline__ float transpose_reduce(float (&acc)[8], int lane) {
+    float a4[4];
+    const bool up16 = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        float send = up16 ? acc[i] : acc[i + 4];
+        float keep = up16 ? acc[i + 4] : acc[i];
+        a4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float a2[2];
+    const bool up8 = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        float send = up8 ? a4[i] : a4[i + 2];
+        float keep = up8 ? a4[i + 2] : a4[i];
+        a2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    const bool up4 = lane & 4;
+    float send = up4 ? a2[0] : a2[1];
+    float keep = up4 ? a2[1] : a2[0];
+    float a1 = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 2);
+    a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, 1);
+    return a1;
+}
+
+template <int ELEM>
+__device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const uint32_t *lut, const uint8_t *rexp,
+                                           int nr, const float (&x)[16], float (&acc)[8], bool &bad) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
+    const uint32_t lw = reg[lane];
+    uint32_t incl = lw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t *code = reinterpret_cast<const uint32_t *>(reg + 32) + (incl - lw);
+    const uint4 *man4 = reinterpret_cast<const uint4 *>(reg + up16(32 + 4 * (uint64_t)total) + (uint64_t)lane * MW * 4);
+    uint32_t mw[MW + 1];
+#pragma unroll
+    for (int i = 0; i < MW / 4; i++) {
+        uint4 q = man4[i];
+        mw[4 * i] = q.x;
+        mw[4 * i + 1] = q.y;
+        mw[4 * i + 2] = q.z;
+        mw[4 * i + 3] = q.w;
+    }
+    mw[MW] = 0;
+    LaneStream ls;
+    ls.init(code, lw);
+#pragma unroll
+    for (int p = 0; p < 64; p++) {
+        const int c = p >> 2, pp = p & 3;
+        const uint32_t X = xpair<F>(mw, p);
+        ls.refill();
+        const uint32_t e = lut[(uint32_t)(ls.win >> 52)];
+        float w0, w1;
+        if (e & kFlagGen) {
+            uint32_t s0, v0, s1, v1;
+            decode_one<ELEM>(ls, nr, rexp, s0, v0);
+            decode_one<ELEM>(ls, nr, rexp, s1, v1);
+            constexpr uint32_t FM = (1u << F) - 1u;
+            w0 = elem_value<ELEM>(s0, v0, X & FM);
+            w1 = elem_value<ELEM>(s1, v1, (X >> 16) & FM);
+        } else {
+            ls.consume((int)(e & 31u));
+            uint32_t bf;
+            if (ELEM == 0) bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
+            else bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
+            w0 = __uint_as_float(bf << 16);
+            w1 = __uint_as_float(bf & 0xFFFF0000u);
+        }
+        const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(x[c], x[c]),
+                                    make_float2(acc[2 * pp], acc[2 * pp + 1]));
+        acc[2 * pp] = r.x;
+        acc[2 * pp + 1] = r.y;
+    }
+    bad |= ls.overrun();
+}
+
+template <int ELEM>
+__device__ __forceinline__ void block_generic(const uint8_t *reg, int lane, const uint8_t *rexp, int nr, int rows,
+                                              uint64_t k, uint64_t cb, const float (&x)[16], float (&acc)[8],
+                                              bool &bad) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    const int cols = real_cols(k, cb, lane);
+    LaneRegion lr = lane_region(reg, lane, rows, k, cb, F);
+    LaneStream ls;
+    ls.init(lr.code, lr.nwords);
+    lane_generic<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
+        acc[t & 7] = fmaf(elem_value<ELEM>(s, v, mm), x[t >> 3], acc[t & 7]);
+    });
+    bad |= ls.overrun();
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kGemvWarps * 32, 1)
+    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, float *partial, uint32_t *counters,
+                uint64_t n_pad) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint8_t *rexp = smem + kRexpOff;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    load_rank_table(m, rexp);
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < 4096; i += blockDim.x) lut[i] = lut_entry<ELEM>(i, m.nr, rexp);
+    const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16), bar1 = bar0 + 8;
+    uint8_t *stage0 = smem + kStageOff + warp * 2 * kStageBytes, *stage1 = stage0 + kStageBytes;
+    if (lane == 0) {
+        mbar_init(bar0);
+        mbar_init(bar1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
+    uint64_t b = (uint64_t)blockIdx.x * kGemvWarps + warp;
+    uint32_t phase = 0;  // bit i: parity of the next completion of stage i
+    bool bad = false, timed_out = false;
+
+    // Region bounds of block bb, read by lane 0 and broadcast.
+    auto region = [&](uint64_t bb, const uint8_t *&ptr, uint32_t &bytes) {
+        uint32_t s = 0, e = 0;
+        if (lane == 0) {
+            s = m.tab[bb];
+            e = m.tab[bb + 1];
+        }
+        s = __shfl_sync(0xFFFFFFFFu, s, 0);
+        e = __shfl_sync(0xFFFFFFFFu, e, 0);
+        ptr = m.data + 16 * (uint64_t)s;
+        bytes = 16 * (e - s);
+    };
+    auto issue = [&](uint64_t bb, int which) {
+        const uint8_t *src;
+        uint32_t bytes;
+        region(bb, src, bytes);
+        if (bytes <= (uint32_t)kStageBytes && lane == 0) {
+            const uint32_t bar = which ? bar1 : bar0;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar, bytes);
+            tma_load_1d(smem_u32(which ? stage1 : stage0), src, bytes, bar);
+        }
+    };
+
+    if (b < m.nb) issue(b, 0);
+    for (int it = 0; b < m.nb; it++) {
+        const int cur = it & 1;
+        const uint64_t nxt = b + total_warps;
+        __syncwarp();
+        if (nxt < m.nb) issue(nxt, cur ^ 1);
+        const uint8_t *src;
+        uint32_t bytes;
+        region(b, src, bytes);
+        const uint8_t *reg = src;
+        if (bytes <= (uint32_t)kStageBytes) {
+            const uint32_t bar = cur ? bar1 : bar0;
+            if (!mbar_wait(bar, (phase >> cur) & 1u)) {
+                timed_out = true;
+                break;
+            }
+            phase ^= 1u << cur;
+            reg = cur ? stage1 : stage0;
+        }
+        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
+        const int rows = real_rows(m.n, rb);
+        // activations of this lane's 16 columns, zero past K
+        float xv[16];
+        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
+        const int cols = real_cols(m.k, cb, lane);
+        if (cols == 16 && (reinterpret_cast<uintptr_t>(x + col0) & 15) == 0) {
+            const uint4 *xp = reinterpret_cast<const uint4 *>(x + col0);
+            uint4 q0 = __ldg(xp), q1 = __ldg(xp + 1);
+            const uint32_t u[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                xv[2 * i] = __uint_as_float(u[i] << 16);
+                xv[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; c++) xv[c] = c < cols ? __uint_as_float((uint32_t)x[col0 + c] << 16) : 0.0f;
+        }
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; r++) acc[r] = 0.0f;
+        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
+        if (interior) block_fast<ELEM>(reg, lane, lut, rexp, m.nr, xv, acc, bad);
+        else block_generic<ELEM>(reg, lane, rexp, m.nr, rows, m.k, cb, xv, acc, bad);
+        const float sum = transpose_reduce(acc, lane);
+        const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
+        const uint64_t row = rb * kRows + (uint64_t)row_in;
+        const bool writer = (lane & 3) == 0 && row < m.n;
+        if (m.cbs == 1) {
+            if (writer) y[row] = ELEM == 0 ? sum : sum * m.scales[row];
+        } else {
+            if (writer) partial[cb * n_pad + row] = sum;
+            __threadfence();
+            __syncwarp();
+            uint32_t ticket = 0;
+            if (lane == 0) ticket = atomicAdd(&counters[rb], 1u);
+            ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+            if (ticket == (uint32_t)m.cbs - 1) {
+                __threadfence();
+                if (lane < kRows && rb * kRows + (uint64_t)lane < m.n) {
+                    const uint64_t r2 = rb * kRows + (uint64_t)lane;
+                    float s = 0.0f;
+                    for (uint64_t c2 = 0; c2 < m.cbs; c2++) s += __ldcg(partial + c2 * n_pad + r2);
+                    y[r2] = ELEM == 0 ? s : s * m.scales[r2];
+                }
+                if (lane == 0) counters[rb] = 0;
+            }
+        }
+        b = nxt;
+    }
+    if (timed_out) {
+        raise_error(kErrTimeout);
+        // let this warp's own copies land before the CTA's shared memory goes away
+        mbar_wait(bar0, phase & 1u);
+        mbar_wait(bar1, (phase >> 1) & 1u);
+    }
+    if (bad) raise_error(kErrFormat);
+}
+
+// =================================================================== host side
+int g_sm_count = -1;
+std::mutex g_mu;
+
+int sm_count() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count < 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        g_sm_count = n;
+    }
+    return g_sm_count;
+}
+
+template <class K>
+bool set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+nwc_status launched() { return cudaGetLastError() == cudaSuccess ? NWC_OK : NWC_ERR_CUDA; }
+
+uint64_t pad_rows(const nwc_matrix &m) { return (uint64_t)m.row_blocks * kRows; }
+
+}  // namespace
+
+extern "C" int nwc_sm_count(void) { return sm_count(); }
+
+extern "C" nwc_status nwc_decode(const nwc_matrix *mp, void *out, int64_t ld_out, float *scales_out, nwc_stream stream) {
+    if (!mp || !out || ld_out < mp->k) return NWC_ERR_INVALID_ARG;
+    const Mat m = to_mat(*mp);
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    const uint64_t want = (m.nb + 7) / 8;
+    const int grid = (int)(want < (uint64_t)sms * 8 ? (want ? want : 1) : (uint64_t)sms * 8);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (m.elem == NWC_ELEM_BF16) decode_kernel<0><<<grid, 256, 0, s>>>(m, out, ld_out);
+    else decode_kernel<1><<<grid, 256, 0, s>>>(m, out, ld_out);
+    if (launched() != NWC_OK) return NWC_ERR_CUDA;
+    if (m.elem == NWC_ELEM_FP8_E4M3 && scales_out) {
+        if (cudaMemcpyAsync(scales_out, m.scales, 4 * m.n, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return NWC_ERR_CUDA;
+    }
+    return NWC_OK;
+}
+
+extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64_t n_ids, void *out, int64_t ld_out,
+                                 nwc_stream stream) {
+    if (!mp || n_ids < 0 || ld_out < mp->k) return NWC_ERR_INVALID_ARG;
+    if (n_ids == 0) return NWC_OK;
+    if (!ids || !out) return NWC_ERR_INVALID_ARG;
+    const Mat m = to_mat(*mp);
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    const uint64_t items = (uint64_t)n_ids * m.cbs, want = (items + 7) / 8;
+    const int grid = (int)(want < (uint64_t)sms * 8 ? want : (uint64_t)sms * 8);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (m.elem == NWC_ELEM_BF16) gather_kernel<0><<<grid, 256, 0, s>>>(m, ids, n_ids, out, ld_out);
+    else gather_kernel<1><<<grid, 256, 0, s>>>(m, ids, n_ids, out, ld_out);
+    return launched();
+}
+
+extern "C" size_t nwc_gemv_workspace_bytes(const nwc_matrix *mp) {
+    if (!mp || mp->col_blocks <= 1) return 0;
+    return (size_t)(4 * (uint64_t)mp->col_blocks * pad_rows(*mp) + 4 * (uint64_t)mp->row_blocks);
+}
+
+extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                               nwc_stream stream) {
+    if (!mp || !x || !y) return NWC_ERR_INVALID_ARG;
+    const size_t need = nwc_gemv_workspace_bytes(mp);
+    if (need && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15))) return NWC_ERR_INVALID_ARG;
+    const Mat m = to_mat(*mp);
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    static bool smem_ok[2] = {false, false};
+    static std::once_flag once[2];
+    std::call_once(once[0], [] { smem_ok[0] = set_smem(gemv_kernel<0>, kGemvSmem); });
+    std::call_once(once[1], [] { smem_ok[1] = set_smem(gemv_kernel<1>, kGemvSmem); });
+    if (!smem_ok[m.elem]) return NWC_ERR_CUDA;
+    const uint64_t n_pad = pad_rows(*mp);
+    float *partial = static_cast<float *>(ws);
+    uint32_t *counters = need ? reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + 4 * m.cbs * n_pad) : nullptr;
+    const uint64_t want = (m.nb + kGemvWarps - 1) / kGemvWarps;
+    const int grid = (int)(want < (uint64_t)sms ? want : (uint64_t)sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (m.elem == NWC_ELEM_BF16)
+        gemv_kernel<0><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, partial, counters, n_pad);
+    else
+        gemv_kernel<1><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, partial, counters, n_pad);
+    return launched();
+}
+
+extern "C" nwc_status nwc_check(nwc_stream stream, uint32_t *flags) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return NWC_ERR_CUDA;
+    uint32_t f = 0;
+    if (cudaMemcpyFromSymbol(&f, g_nwc_error, 4) != cudaSuccess) return NWC_ERR_CUDA;
+    if (f) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_nwc_error, &zero, 4) != cudaSuccess) return NWC_ERR_CUDA;
+    }
+    if (flags) *flags = f;
+    if (f & kErrTimeout) return NWC_ERR_TIMEOUT;
+    return f ? NWC_ERR_DEVICE_FLAG : NWC_OK;
+}

@@ -1,0 +1,176 @@
+/*
+ * nwc.h -- C ABI of the GB300 (sm_103a) library for batch-1 matrix-vector products over
+ * losslessly entropy-coded BF16 (and fp8 e4m3) weight matrices.
+ *
+ * What the calls compute is defined by two pages:
+ *   "NWC -- Neural Weight Compression" (PyPI project page, v0.9.0), section "How it works":
+ *     a BF16 weight splits into a raw mantissa plane and an entropy-coded exponent/sign part;
+ *     the exponent is ranked by frequency and written as a unary rank code plus a raw sign
+ *     bit, with an escape for rare values; lanes decode their own bit streams over blocks of
+ *     8 rows x 512 columns inside the matrix-vector kernel; dequantization and the embedding
+ *     lookup run on the same decoder; any shape works (2 bits per filler, no mantissa).
+ *   "Qwen3-4B-NWC-fp8" (model card): weight-only e4m3 with a symmetric per-output-channel
+ *     scale, fp8 bytes coded losslessly, the scale applied at the end of the matvec.
+ *
+ * Conventions
+ *   - Every call returns nwc_status; no exception or abort crosses this boundary.
+ *   - Host pointers are read (or written) only during the call. Device pointers stay owned
+ *     by the caller; the library allocates no device or pinned memory, ever.
+ *   - GPU calls are asynchronous on the given stream (NULL = the legacy default stream).
+ *     A launch failure returns NWC_ERR_CUDA. Data errors found on the device (a lane
+ *     stream that runs past its words, a gather id out of range) do not fault: the kernel
+ *     skips the bad access, writes zeros and raises the device error word, which
+ *     nwc_check() reads and clears.
+ *   - Matrices are row-major: element (n, k) of an N x K matrix is at index n*ld + k.
+ *     N = output features (rows), K = input features (columns), ld >= K.
+ *   - BF16 values are passed as their 16-bit patterns (uint16_t); x is BF16, y is FP32.
+ */
+#ifndef NWC_H
+#define NWC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers; pass a cudaStream_t (or torch's raw stream). */
+typedef struct CUstream_st *nwc_stream;
+
+typedef enum nwc_status {
+    NWC_OK = 0,
+    NWC_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad enum, misaligned buffer      */
+    NWC_ERR_FORMAT = 2,      /* blob fails validation (header, tables, region sizes)     */
+    NWC_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed              */
+    NWC_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (reported by nwc_check)    */
+    NWC_ERR_DEVICE_FLAG = 5, /* a kernel raised the device error word (see nwc_check)    */
+    NWC_ERR_UNSUPPORTED = 6  /* valid request this build does not implement              */
+} nwc_status;
+
+enum { NWC_ELEM_BF16 = 0, NWC_ELEM_FP8_E4M3 = 1 };
+
+/* Geometry of the format (fixed by the pages: blocks of 8 rows x 512 columns, 32 lanes of
+ * 16 columns x 8 rows). */
+enum { NWC_BLOCK_ROWS = 8, NWC_BLOCK_COLS = 512, NWC_LANES = 32, NWC_MAX_RANKED = 11 };
+
+/*
+ * A bound, validated matrix: plain data, safe to copy by value. Built by nwc_bind from the
+ * blob's host copy (parsed once) and the address of its device copy. All pointers are device
+ * pointers into that device copy; the caller keeps it alive while the struct is used.
+ */
+typedef struct nwc_matrix {
+    int32_t elem;            /* NWC_ELEM_BF16 or NWC_ELEM_FP8_E4M3                          */
+    int32_t n_ranked;        /* exponents with a unary code (1..11)                         */
+    int64_t n, k;            /* rows (output features), columns (input features)           */
+    int64_t row_blocks;      /* ceil(n / 8)                                                 */
+    int64_t col_blocks;      /* ceil(k / 512)                                               */
+    uint8_t rank_exp[16];    /* exponent value of rank 0..n_ranked-1                        */
+    const uint32_t *block_tab; /* u32[row_blocks*col_blocks + 1], 16-byte units from data  */
+    const uint8_t *data;     /* start of the block regions                                  */
+    const float *scales;     /* fp32[n] per-row scales (fp8), NULL for BF16                 */
+    uint64_t blob_bytes;     /* size of the whole blob                                      */
+    uint64_t max_block_bytes;/* largest block region                                        */
+    uint64_t data_bytes;     /* bytes of all block regions                                  */
+} nwc_matrix;
+
+/* Human-readable name of a status code (static string). */
+const char *nwc_status_str(nwc_status s);
+
+/* Library version string, e.g. "nwc 1 (format 1, sm_103a)". */
+const char *nwc_version(void);
+
+/*
+ * nwc_encode -- host encoder ("How it works": byte planes, prefix code, per-lane bit streams).
+ *   w       host, N x K BF16 bit patterns, row stride ld (elements).
+ *   elem    NWC_ELEM_BF16 codes w as is. NWC_ELEM_FP8_E4M3 first quantizes each row n to
+ *           e4m3 with scale s_n = absmax_n / 448 (FP32, s_n = 1 for an all-zero row), q =
+ *           nearest e4m3 to fp32(w)/s_n (ties to even, saturating), then codes the bytes
+ *           ("Qwen3-4B-NWC-fp8": symmetric per-output-channel scale). Non-finite weights
+ *           are rejected for fp8 (NWC_ERR_INVALID_ARG).
+ *   threads host worker threads (<= 0: all hardware threads). Output bytes do not depend on it.
+ *   blob    host output buffer or NULL. Two-call pattern: with blob == NULL only *blob_bytes
+ *           is set (the exact size); otherwise *blob_bytes holds the capacity on entry and
+ *           the written size on return (NWC_ERR_INVALID_ARG if too small).
+ */
+nwc_status nwc_encode(const uint16_t *w, int64_t n, int64_t k, int64_t ld, int elem, int threads,
+                      void *blob, size_t *blob_bytes);
+
+/*
+ * nwc_encode_fp8 -- codes already-quantized e4m3 bytes q (N x K, stride ld) with their row
+ * scales (fp32[N], stored as given). Same two-call pattern and threads as nwc_encode.
+ */
+nwc_status nwc_encode_fp8(const uint8_t *q, const float *scales, int64_t n, int64_t k, int64_t ld,
+                          int threads, void *blob, size_t *blob_bytes);
+
+/*
+ * nwc_quantize_fp8 -- the quantization step of nwc_encode(elem = FP8) alone, on the host:
+ * q (N x K, stride ldq) and scales (fp32[N]) as defined there.
+ */
+nwc_status nwc_quantize_fp8(const uint16_t *w, int64_t n, int64_t k, int64_t ld, uint8_t *q,
+                            int64_t ldq, float *scales);
+
+/*
+ * nwc_validate -- host check of a blob: header, rank table, block table, and every block
+ * region's size against its lane word counts and real-element counts. NWC_ERR_FORMAT if any
+ * check fails. Stream contents are checked by the kernels while decoding.
+ */
+nwc_status nwc_validate(const void *blob_host, size_t bytes);
+
+/*
+ * nwc_bind -- validates the host copy of a blob (as nwc_validate) and fills *out with its
+ * geometry and the device pointers of the same blob copied to blob_dev (16-byte aligned,
+ * caller-owned). No device call is made.
+ */
+nwc_status nwc_bind(const void *blob_host, size_t bytes, const void *blob_dev, nwc_matrix *out);
+
+/*
+ * nwc_decode -- dequantization to the stored elements, bit-exact ("decompressed weights are
+ * bit-exact"): BF16 blobs write uint16 out[n*ld_out + k]; fp8 blobs write the e4m3 bytes
+ * (uint8) to out and the row scales to scales_out (fp32[N], may be NULL). ld_out >= K.
+ */
+nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *scales_out,
+                      nwc_stream stream);
+
+/*
+ * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (0 when K <= 512): FP32
+ * partial sums per (row, 512-column block) and one counter per 8-row block. The caller zeroes
+ * it once after allocating; every nwc_gemv call leaves the counters at zero again, so the
+ * same workspace serves repeated calls and CUDA-graph replays. Calls sharing one workspace
+ * must not overlap on the GPU.
+ */
+size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
+
+/*
+ * nwc_gemv -- batch-1 y = W x with W decoded in registers ("Fused kernel"): x is BF16[K],
+ * y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
+ * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes as returned
+ * by nwc_gemv_workspace_bytes (16-byte aligned; may be NULL when that size is 0).
+ */
+nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                    nwc_stream stream);
+
+/*
+ * nwc_gather -- embedding lookup on the same decoder ("Dequantization and embedding lookup
+ * (tied lm_head) run on the same decoder"): out row i = row ids[i] of the stored matrix,
+ * bit-exact (uint16 BF16 or uint8 e4m3), out[i*ld_out + k]. An id outside [0, N) writes a
+ * zero row and raises the device error word.
+ */
+nwc_status nwc_gather(const nwc_matrix *m, const int32_t *ids, int64_t n_ids, void *out,
+                      int64_t ld_out, nwc_stream stream);
+
+/*
+ * nwc_check -- synchronizes the stream, then reads and clears the device error word of the
+ * current device. NWC_OK if clear; NWC_ERR_DEVICE_FLAG (format/bounds) or NWC_ERR_TIMEOUT
+ * (a bounded wait ran out) otherwise; *flags (if not NULL) receives the raw bits.
+ */
+nwc_status nwc_check(nwc_stream stream, uint32_t *flags);
+
+/* Streaming multiprocessors of the current device (queried, never assumed). */
+int nwc_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NWC_H */

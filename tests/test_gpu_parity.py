@@ -1,0 +1,207 @@
+"""GPU parity against the CPU oracle, through the C ABI (needs a CUDA GPU).
+
+Decode and gather must be bit-exact. The matrix-vector product must satisfy, per row,
+|y - y_ref| <= 2^-10 * sum_k |w x| + 1e-6 (FP32 output against the oracle's FP64 sum).
+"""
+import numpy as np
+import pytest
+import torch
+
+import decode_gemv_nwc_gb300 as nwc
+import oracle
+from decode_gemv_nwc_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+TOL_REL, TOL_ABS = 2.0 ** -10, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_gemv_nwc_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def dev_bits(a: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def assert_clean():
+    st, flags = nwc.check()
+    assert st == 0, f"device error word {flags:#x}"
+
+
+def gemv_check(blob, x_bits, rows=None, mat=None):
+    mat = mat or nwc.Matrix(blob)
+    y = mat.gemv(dev_bits(x_bits)).cpu().numpy().astype(np.float64)
+    assert_clean()
+    if rows is None:
+        rows = np.arange(mat.n)
+    ref = oracle.gemv(blob, x_bits, rows)
+    scale = oracle.abs_dot(blob, x_bits, rows)
+    err = np.abs(y[rows] - ref)
+    bound = TOL_REL * scale + TOL_ABS
+    worst = int(np.argmax(err - bound))
+    assert (err <= bound).all(), f"row {rows[worst]}: |{y[rows][worst]} - {ref[worst]}| > {bound[worst]}"
+    return y
+
+
+# --------------------------------------------------------------------- decode
+@pytest.mark.parametrize("shape", [(1, 1), (7, 9), (9, 513), (17, 1100), (64, 512), (130, 2049)])
+def test_decode_bit_exact_shapes(shape):
+    w = synth.normal_bf16(shape, 0.02, seed=sum(shape))
+    blob = nwc.encode(w)
+    out = nwc.Matrix(blob).decode().cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, oracle.decode(blob)[0])
+    assert np.array_equal(out, w)
+
+
+def test_decode_all_bf16_patterns():
+    rng = np.random.default_rng(3)
+    w = rng.permutation(np.arange(65536, dtype=np.uint32)).astype(np.uint16).reshape(128, 512)
+    blob = nwc.encode(w)
+    out = nwc.Matrix(blob).decode().cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w)
+
+
+def test_decode_outlier_matrix_then_gemv():
+    w = synth.small_matrix_with_outliers(0)
+    x = synth.activations_bf16(512, 1000)
+    blob = nwc.encode(w)
+    assert blob == oracle.encode(w)
+    mat = nwc.Matrix(blob)
+    out = mat.decode().cpu().numpy().view(np.uint16)
+    assert np.array_equal(out, w)
+    gemv_check(blob, x, mat=mat)
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096), (4095, 4100)])
+def test_square_and_odd_decode_and_gemv(shape):
+    w = synth.normal_bf16(shape, 0.02, seed=0 if shape[0] == 4096 else 1)
+    x = synth.activations_bf16(shape[1], 1001)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    out = mat.decode().cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w)
+    gemv_check(blob, x, mat=mat)
+
+
+# ----------------------------------------------------------------------- gemv
+@pytest.mark.parametrize("shape", [(1, 1), (8, 512), (9, 513), (17, 1100), (33, 4000), (1000, 512), (40, 9728)])
+def test_gemv_shapes(shape):
+    w = synth.normal_bf16(shape, 0.02, seed=shape[0] + 3 * shape[1])
+    x = synth.activations_bf16(shape[1], 7)
+    gemv_check(nwc.encode(w), x)
+
+
+def test_gemv_special_values():
+    """Zeros, subnormals, large finite values and +-0 in one matrix (finite only)."""
+    rng = np.random.default_rng(17)
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = pats[((pats >> 7) & 0xFF) != 0xFF]
+    # keep magnitudes below 2^40 so the FP32 sum stays finite
+    finite = finite[((finite >> 7) & 0xFF) < 127 + 40]
+    w = rng.choice(finite, size=(24, 2048)).astype(np.uint16)
+    x = synth.activations_bf16(2048, 5)
+    gemv_check(nwc.encode(w), x)
+
+
+def test_gemv_repeat_graph_and_stream():
+    w = synth.normal_bf16((520, 2600), 0.03, seed=31)
+    x = synth.activations_bf16(2600, 32)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    xd = dev_bits(x)
+    y0 = mat.gemv(xd).clone()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y1 = mat.gemv(xd, stream=s)
+    s.synchronize()
+    assert torch.equal(y0, y1)  # fixed reduction order: bitwise reproducible
+    yg = torch.empty_like(y0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mat.gemv(xd, y=yg)
+    for _ in range(3):
+        yg.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(yg, y0)
+    assert_clean()
+    gemv_check(blob, x, mat=mat)
+
+
+# ------------------------------------------------------------------------ fp8
+@pytest.mark.parametrize("shape", [(9728, 2560), (2560, 9728), (9, 700)])
+def test_fp8_decode_and_gemv(shape):
+    w = synth.normal_bf16(shape, 0.02, seed=50 + shape[0])
+    q, s = oracle.quantize_fp8(w)
+    blob = nwc.encode(w, elem=nwc.FP8)
+    assert blob == oracle.encode(q, oracle.FP8, s)
+    mat = nwc.Matrix(blob)
+    qd, sd = mat.decode()
+    assert_clean()
+    assert np.array_equal(qd.cpu().numpy(), q) and np.array_equal(sd.cpu().numpy(), s)
+    x = synth.activations_bf16(shape[1], 77)
+    rows = None if shape[0] * shape[1] < 10 ** 6 else np.sort(np.random.default_rng(0).choice(shape[0], 512, False))
+    gemv_check(blob, x, rows=rows, mat=mat)
+
+
+def test_fp8_subnormal_and_zero_codes():
+    rng = np.random.default_rng(8)
+    q = rng.integers(0, 256, size=(16, 1024)).astype(np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x01  # no NaN codes in a GEMV test
+    s = rng.uniform(0.5, 2.0, 16).astype(np.float32)
+    blob = nwc.encode_fp8(q, s)
+    mat = nwc.Matrix(blob)
+    qd, _ = mat.decode()
+    assert np.array_equal(qd.cpu().numpy(), q)
+    gemv_check(blob, synth.activations_bf16(1024, 3), mat=mat)
+
+
+# --------------------------------------------------------------------- gather
+def test_gather_bit_exact_and_bad_id():
+    w = synth.normal_bf16((1000, 2560), 0.02, seed=7)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    ids = synth.token_ids(300, 1000, seed=8)
+    out = mat.gather(torch.from_numpy(ids).cuda()).cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w[ids])
+    bad = torch.tensor([3, 1000, -1, 999], dtype=torch.int32, device="cuda")
+    out = mat.gather(bad).cpu().numpy().view(np.uint16)
+    st, flags = nwc.check()
+    assert st == 5 and flags & 2
+    assert np.array_equal(out[0], w[3]) and np.array_equal(out[3], w[999])
+    assert (out[1] == 0).all() and (out[2] == 0).all()
+    assert_clean()  # cleared by the previous check
+
+
+def test_gather_ragged_width_fp8():
+    w = synth.normal_bf16((77, 1300), 0.02, seed=70)
+    q, s = oracle.quantize_fp8(w)
+    blob = nwc.encode_fp8(q, s)
+    mat = nwc.Matrix(blob)
+    ids = np.array([0, 76, 8, 8, 15, 64], np.int32)
+    out = mat.gather(torch.from_numpy(ids).cuda()).cpu().numpy()
+    assert_clean()
+    assert np.array_equal(out, q[ids])
+
+
+@pytest.mark.slow
+def test_embedding_table_gather_and_lm_head_sampled():
+    """151936 x 2560 tied table: 4096 random ids bit-exact, then the lm_head GEMV on
+    sampled rows (full size, the launch configuration the benchmark times)."""
+    w = synth.normal_bf16((synth.VOCAB, synth.HIDDEN), 0.02, seed=7)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    ids = synth.token_ids(4096, synth.VOCAB, seed=8)
+    out = mat.gather(torch.from_numpy(ids).cuda()).cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w[ids])
+    x = synth.activations_bf16(synth.HIDDEN, 9)
+    rows = np.sort(np.random.default_rng(1).choice(synth.VOCAB, 2048, False))
+    gemv_check(blob, x, rows=rows, mat=mat)
