@@ -64,12 +64,13 @@ def lib():
     L.nwc_decode.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, p]
     L.nwc_gemv_workspace_bytes.argtypes = [ctypes.POINTER(NwcMatrix)]
     L.nwc_gemv_workspace_bytes.restype = sz
+    L.nwc_gemv_prepare.argtypes = [ctypes.POINTER(NwcMatrix), p, sz, p]
     L.nwc_gemv.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, p]
     L.nwc_gather.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, i64, p]
     L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
     L.nwc_sm_count.restype = i32
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
-                 "nwc_decode", "nwc_gemv", "nwc_gather", "nwc_check"):
+                 "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gather", "nwc_check"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -150,7 +151,7 @@ class Matrix:
 
     ``device_blob`` is a torch uint8 CUDA tensor holding the blob (caller-visible so that
     benchmarks can keep several copies); the GEMV workspace is allocated once, zeroed, and
-    reused by every call.
+    reused by every call (prepared once here: decode table built, counters zeroed).
     """
 
     def __init__(self, blob: bytes, device="cuda", device_blob=None):
@@ -165,8 +166,10 @@ class Matrix:
         self.elem, self.n, self.k = self.m.elem, self.m.n, self.m.k
         self.blob_bytes = len(blob)
         ws = int(lib().nwc_gemv_workspace_bytes(ctypes.byref(self.m)))
-        self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device_blob.device)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device_blob.device)
         self.ws_bytes = ws
+        _ok(lib().nwc_gemv_prepare(ctypes.byref(self.m), ctypes.c_void_p(self.workspace.data_ptr()), ws,
+                                   _stream_ptr(None)), "nwc_gemv_prepare")
 
     def gemv(self, x, y=None, stream=None):
         """y (float32[N]) = W x for x a BF16 vector given as an int16/bfloat16 CUDA tensor."""
@@ -175,7 +178,7 @@ class Matrix:
         if y is None:
             y = torch.empty(self.n, dtype=torch.float32, device=x.device)
         _ok(lib().nwc_gemv(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
-                           ctypes.c_void_p(self.workspace.data_ptr()) if self.ws_bytes else None, self.ws_bytes,
+                           ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes,
                            _stream_ptr(stream)), "nwc_gemv")
         return y
 

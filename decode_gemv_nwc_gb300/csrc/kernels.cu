@@ -35,7 +35,9 @@ __device__ uint32_t g_nwc_error;
 namespace {
 
 constexpr uint32_t kErrFormat = 1u, kErrId = 2u, kErrTimeout = 4u;
-constexpr uint32_t kFlagGen = 1u << 6;  // LUT entry: decode this pair with the generic path
+// LUT entry flag: the code at the peek is the escape prefix (n_ranked ones); the raw exponent
+// and the sign follow it in the stream.
+constexpr uint32_t kEsc = 1u << 16;
 
 struct Mat {
     int elem, nr;
@@ -77,18 +79,17 @@ __device__ __forceinline__ void load_rank_table(const Mat &m, uint8_t *rexp) {
 }
 
 // ------------------------------------------------------------------ lane bit stream
-// 64-bit window, most significant bit = next stream bit; nb valid bits at the top.
+// 64-bit window, most significant bit = next stream bit; nb valid bits at the top. The word
+// pointer may point into shared memory (a staged block) or global memory; after inlining the
+// compiler emits shared or global loads accordingly.
 struct LaneStream {
-    const uint32_t *p;
-    uint32_t left, nwords, inserted;
+    const uint32_t *p, *start, *end;
     int nb;
     uint64_t win;
 
     __device__ __forceinline__ void init(const uint32_t *ptr, uint32_t n) {
-        p = ptr;
-        left = n;
-        nwords = n;
-        inserted = 0;
+        p = start = ptr;
+        end = ptr + n;
         nb = 0;
         win = 0;
         refill();
@@ -98,34 +99,29 @@ struct LaneStream {
     // without reading memory; overrun() reports whether such bits were consumed.
     __device__ __forceinline__ void refill() {
         if (nb <= 32) {
-            uint32_t w = 0;
-            if (left) {
-                w = *p;
-                p++;
-                left--;
-            }
+            const uint32_t w = p < end ? *p : 0u;
+            p++;
             win |= (uint64_t)w << (32 - nb);
             nb += 32;
-            inserted++;
         }
     }
-    __device__ __forceinline__ void consume(int L) {
+    __device__ __forceinline__ void consume(uint32_t L) {
         win <<= L;
-        nb -= L;
+        nb -= (int)L;
     }
+    __device__ __forceinline__ uint32_t top() const { return (uint32_t)(win >> 32); }
     __device__ __forceinline__ bool overrun() const {
-        return (uint64_t)inserted * 32u - (uint64_t)nb > (uint64_t)nwords * 32u;
+        return (uint64_t)(p - start) * 32u - (uint64_t)nb > (uint64_t)(end - start) * 32u;
     }
 };
 
 // One code: rank p < nr is p ones, a zero, the sign; an escape is nr ones, the raw exponent
 // (EB bits, most significant first), the sign.
-template <int ELEM>
-__device__ __forceinline__ void decode_one(LaneStream &ls, int nr, const uint8_t *rexp, uint32_t &s,
-                                           uint32_t &v) {
+template <int ELEM, class S>
+__device__ __forceinline__ void decode_one(S &ls, int nr, const uint8_t *rexp, uint32_t &s, uint32_t &v) {
     constexpr int EB = ELEM == 0 ? 8 : 4;
     ls.refill();
-    const uint32_t top = (uint32_t)(ls.win >> 32);
+    const uint32_t top = ls.top();
     const int ones = __clz(~top);
     int L;
     if (ones < nr) {
@@ -341,10 +337,12 @@ __global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, 
 // =================================================================== GEMV kernel
 constexpr int kGemvWarps = 16;
 constexpr int kStageBytes = 6144;
-constexpr int kLutBytes = 4096 * 4;
+constexpr int kLutEntries = 4096;
+constexpr int kLutBytes = kLutEntries * 4;
 constexpr int kRexpOff = kLutBytes;
-constexpr int kBarOff = kRexpOff + 16;
-constexpr int kStageOff = 16768;  // 128-aligned, after LUT, rank table and 2 barriers/warp
+constexpr int kLutBarOff = kRexpOff + 16;
+constexpr int kBarOff = kLutBarOff + 8;
+constexpr int kStageOff = 16768;  // 128-aligned, after LUT, rank table and barriers
 constexpr int kGemvSmem = kStageOff + kGemvWarps * 2 * kStageBytes;
 static_assert(kBarOff + kGemvWarps * 2 * 8 <= kStageOff, "smem layout");
 
@@ -381,31 +379,37 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint3
                  : "memory");
 }
 
-// LUT entry for a 12-bit peek P (first stream bit = bit 11): both codes complete give
-// hi1 | hi2 << 16 | (L1 + L2), where hi = BF16 high part (s << 15 | exponent << 7); anything
-// else (escape, second code cut off, fp8 subnormal/NaN-capable exponents) is kFlagGen.
+// LUT entry for a 12-bit peek P (first stream bit = bit 11), one code per entry:
+//   bits 0..4   code length L (rank + 2; for the escape prefix n_ranked)
+//   bits 5..6   zero (whole entries may be subtracted from the bit counter)
+//   bits 7..15  the code as a BF16 high part (s << 15 | exponent << 7)
+//   bit 16      kEsc
+// fp8 exponents e are stored as BF16 exponents e + 120 (exact for normal e4m3 values;
+// subnormals are corrected after assembly). A 12-bit peek holds any ranked code (at most
+// n_ranked + 1 <= 12 bits), which is why at most 11 exponents are ranked.
 template <int ELEM>
 __device__ uint32_t lut_entry(uint32_t P, int nr, const uint8_t *rexp) {
     const uint32_t bits = P << 20;
-    const int ones1 = __clz(~bits);
-    if (ones1 >= nr) return kFlagGen;
-    const int L1 = ones1 + 2;
-    const uint32_t s1 = (bits >> (30 - ones1)) & 1u, v1 = rexp[ones1];
-    const uint32_t rest = bits << L1;
-    const int avail = 12 - L1;
-    const int ones2 = __clz(~rest);
-    if (ones2 >= nr || ones2 + 2 > avail) return kFlagGen;
-    const uint32_t s2 = (rest >> (30 - ones2)) & 1u, v2 = rexp[ones2];
-    const int L = L1 + ones2 + 2;
-    if (ELEM == 0) return (s1 << 15) | (v1 << 7) | (((s2 << 15) | (v2 << 7)) << 16) | (uint32_t)L;
-    if (v1 == 0 || v1 == 15 || v2 == 0 || v2 == 15) return kFlagGen;
-    return (s1 << 15) | ((v1 + 120u) << 7) | (((s2 << 15) | ((v2 + 120u) << 7)) << 16) | (uint32_t)L;
+    const int ones = __clz(~bits);
+    if (ones >= nr) return kEsc | (uint32_t)nr;
+    const uint32_t s = (bits >> (30 - ones)) & 1u, v = rexp[ones];
+    return (s << 15) | ((ELEM == 0 ? v : v + 120u) << 7) | ((uint32_t)ones + 2);
 }
 
-// Pair p's two mantissas (even t at bits 0.., odd t at bits 16..) from a full lane's words.
+template <int ELEM>
+__global__ void __launch_bounds__(256) lut_kernel(Mat m, uint32_t *lut, uint32_t *counters, uint64_t n_counters) {
+    __shared__ uint8_t rexp[16];
+    load_rank_table(m, rexp);
+    __syncthreads();
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < (uint32_t)kLutEntries) lut[i] = lut_entry<ELEM>(i, m.nr, rexp);
+    for (uint64_t c = i; c < n_counters; c += (uint64_t)gridDim.x * blockDim.x) counters[c] = 0;
+}
+
+// Pair q's two mantissas (even t at bits 0.., odd t at bits 16..) from a group's words.
 template <int F>
-__device__ __forceinline__ uint32_t xpair(const uint32_t *mw, int p) {
-    const int bit = F * p, k = bit >> 4, o = bit & 15;
+__device__ __forceinline__ uint32_t xpair(const uint32_t *mw, int q) {
+    const int bit = F * q, k = bit >> 4, o = bit & 15;
     if (o + F <= 16) return mw[k] >> o;
     const uint32_t M = (0xFFFFu >> o) * 0x10001u;
     return ((mw[k] >> o) & M) | ((mw[k + 1] << (16 - o)) & ~M);
@@ -439,11 +443,114 @@ __device__ __forceinline__ float transpose_reduce(float (&acc)[8], int lane) {
     return a1;
 }
 
+// Fast-path stream state in registers: window wh:wl (most significant bit first); V holds
+// (valid bits - 1) in its low 7 bits (at most 64 bits are buffered), so whole LUT entries,
+// whose bits 5..6 are zero and whose low five bits are the length, can be subtracted from it;
+// pa = shared-memory address of the next code word. Reads past a lane's words stay inside the
+// staged region (its mantissa regions follow the code streams), so a malformed stream yields
+// garbage but no out-of-bounds access; the bit count check flags it.
+struct Fs32 {
+    uint32_t wh, wl, V, pa, nw;  // nw = the word at pa, loaded one refill ahead
+};
+
+// Branch-free refill: when at most 32 bits are valid the next word is added right below them
+// with one wide multiply-add (the pages' "refilled with a single wide multiply-add"); otherwise
+// the multiplier is 0. The word was loaded by the previous refill, so the shared-memory latency
+// of the following word's load is off the decode chain.
+__device__ __forceinline__ void fs_refill(Fs32 &s) {
+    asm("{\n\t"
+        ".reg .pred q;\n\t"
+        ".reg .u32 t, mul;\n\t"
+        ".reg .u64 w64;\n\t"
+        "and.b32 t, %3, 127;\n\t"
+        "shf.r.clamp.b32 mul, 0x80000000, 0, t;\n\t"
+        "setp.ne.u32 q, mul, 0;\n\t"
+        "mov.b64 w64, {%1, %0};\n\t"
+        "mad.wide.u32 w64, %4, mul, w64;\n\t"
+        "mov.b64 {%1, %0}, w64;\n\t"
+        "@q add.u32 %2, %2, 4;\n\t"
+        "@q add.u32 %3, %3, 32;\n\t"
+        "@q ld.shared.u32 %4, [%2];\n\t"
+        "}"
+        : "+r"(s.wh), "+r"(s.wl), "+r"(s.pa), "+r"(s.V), "+r"(s.nw));
+}
+
+__device__ __forceinline__ void fs_consume(Fs32 &s, uint32_t e) {  // e mod 32 bits
+    const uint32_t h = __funnelshift_l(s.wl, s.wh, e);
+    s.wl = __funnelshift_l(0u, s.wl, e);
+    s.wh = h;
+    s.V -= e;
+}
+
+__device__ __forceinline__ uint32_t lut_at(const Fs32 &s, uint32_t lutb) {
+    uint32_t e;
+    asm("{\n\t.reg .u32 a;\n\tshr.u32 a, %1, 20;\n\tmad.lo.u32 a, a, 4, %2;\n\tld.shared.u32 %0, [a];\n\t}"
+        : "=r"(e)
+        : "r"(s.wh), "r"(lutb));
+    return e;
+}
+
+// Raw escape payload at the window: EB exponent bits (most significant first), then the sign;
+// returned as a BF16 high part (fp8: exponent + 120).
+template <int ELEM>
+__device__ __forceinline__ uint32_t raw_hi(Fs32 &s) {
+    constexpr int EB = ELEM == 0 ? 8 : 4;
+    const uint32_t v = s.wh >> (32 - EB);
+    const uint32_t sg = (s.wh >> (31 - EB)) & 1u;
+    fs_consume(s, EB + 1);
+    return (sg << 15) | ((ELEM == 0 ? v : v + 120u) << 7);
+}
+
+// fp8 only: an e4m3 subnormal (exponent field 0, stored as BF16 exponent 120) assembled as
+// +-2^-7 (1 + m/8) becomes +-m 2^-9 = (w -+ 2^-7) * 2, exactly.
+__device__ __forceinline__ float fp8_subnormal_fix(float w) {
+    return (w - copysignf(0.0078125f, w)) * 2.0f;
+}
+
+// One row pair: two single-code lookups, BF16x2 assembly with the raw mantissas. Escapes are
+// rare; one branch re-decodes the pair from the state after the first lookup.
+template <int ELEM>
+__device__ __forceinline__ void pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
+    fs_refill(s);  // a pair of ranked codes takes at most 24 bits; a refill leaves at least 33
+    const uint32_t e1 = lut_at(s, lutb);
+    fs_consume(s, e1);
+    const Fs32 after1 = s;
+    const uint32_t e2 = lut_at(s, lutb);
+    fs_consume(s, e2);
+    uint32_t e = __byte_perm(e1, e2, 0x5410);
+    if ((e1 | e2) & kEsc) {
+        s = after1;
+        uint32_t hi1 = e1 & 0xFF80u;
+        if (e1 & kEsc) hi1 = raw_hi<ELEM>(s);
+        fs_refill(s);
+        const uint32_t f = lut_at(s, lutb);
+        fs_consume(s, f);
+        uint32_t hi2 = f & 0xFF80u;
+        if (f & kEsc) {
+            fs_refill(s);
+            hi2 = raw_hi<ELEM>(s);
+        }
+        e = hi1 | (hi2 << 16);
+    }
+    uint32_t bf;
+    if (ELEM == 0) bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
+    else bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
+    w0 = __uint_as_float(bf << 16);
+    w1 = __uint_as_float(bf & 0xFFFF0000u);
+    if (ELEM == 1) {
+        if ((bf & 0x7F80u) == (120u << 7)) w0 = fp8_subnormal_fix(w0);
+        if ((bf & 0x7F800000u) == (120u << 23)) w1 = fp8_subnormal_fix(w1);
+    }
+}
+
+// Interior block from its staged region: 4 groups of 4 columns (16 row pairs each); the
+// group loop stays rolled so the hot loop fits the instruction cache.
 template <int ELEM>
 __device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const uint32_t *lut, const uint8_t *rexp,
-                                           int nr, const float (&x)[16], float (&acc)[8], bool &bad) {
+                                           int nr, const uint16_t *xl, float (&acc)[8], bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
+    constexpr int MWG = MW / 4;              // words per group of 4 columns
     const uint32_t lw = reg[lane];
     uint32_t incl = lw;
 #pragma unroll
@@ -452,48 +559,49 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const u
         if (lane >= d) incl += o;
     }
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    const uint32_t *code = reinterpret_cast<const uint32_t *>(reg + 32) + (incl - lw);
-    const uint4 *man4 = reinterpret_cast<const uint4 *>(reg + up16(32 + 4 * (uint64_t)total) + (uint64_t)lane * MW * 4);
-    uint32_t mw[MW + 1];
-#pragma unroll
-    for (int i = 0; i < MW / 4; i++) {
-        uint4 q = man4[i];
-        mw[4 * i] = q.x;
-        mw[4 * i + 1] = q.y;
-        mw[4 * i + 2] = q.z;
-        mw[4 * i + 3] = q.w;
+    const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
+    const uint32_t code = regs + 32 + 4 * (incl - lw);
+    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * MW * 4;
+    Fs32 s;
+    {
+        uint32_t w0 = 0, w1 = 0;
+        if (lw > 0) asm("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(code));
+        if (lw > 1) asm("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(code + 4));
+        s.wh = w0;
+        s.wl = w1;
+        s.pa = code + 8;
+        s.V = 63u;
+        asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
     }
-    mw[MW] = 0;
-    LaneStream ls;
-    ls.init(code, lw);
+    const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
+    const uint2 *xp = reinterpret_cast<const uint2 *>(xl);
+    uint2 xq = __ldg(xp);
+#pragma unroll 1
+    for (int g = 0; g < 4; g++) {
+        const uint2 xn = __ldg(xp + (g < 3 ? g + 1 : 3));
+        const float xf[4] = {__uint_as_float(xq.x << 16), __uint_as_float(xq.x & 0xFFFF0000u),
+                             __uint_as_float(xq.y << 16), __uint_as_float(xq.y & 0xFFFF0000u)};
+        uint32_t mw[MWG];
 #pragma unroll
-    for (int p = 0; p < 64; p++) {
-        const int c = p >> 2, pp = p & 3;
-        const uint32_t X = xpair<F>(mw, p);
-        ls.refill();
-        const uint32_t e = lut[(uint32_t)(ls.win >> 52)];
-        float w0, w1;
-        if (e & kFlagGen) {
-            uint32_t s0, v0, s1, v1;
-            decode_one<ELEM>(ls, nr, rexp, s0, v0);
-            decode_one<ELEM>(ls, nr, rexp, s1, v1);
-            constexpr uint32_t FM = (1u << F) - 1u;
-            w0 = elem_value<ELEM>(s0, v0, X & FM);
-            w1 = elem_value<ELEM>(s1, v1, (X >> 16) & FM);
-        } else {
-            ls.consume((int)(e & 31u));
-            uint32_t bf;
-            if (ELEM == 0) bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
-            else bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
-            w0 = __uint_as_float(bf << 16);
-            w1 = __uint_as_float(bf & 0xFFFF0000u);
+        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * (MWG * g + i)));
+#pragma unroll
+        for (int q = 0; q < 16; q++) {
+            const int pp = q & 3;
+            const float xc = xf[q >> 2];
+            const uint32_t X = xpair<F>(mw, q);
+            float w0, w1;
+            pair_step<ELEM>(s, lutb, X, w0, w1);
+            const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
+                                        make_float2(acc[2 * pp], acc[2 * pp + 1]));
+            acc[2 * pp] = r.x;
+            acc[2 * pp + 1] = r.y;
         }
-        const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(x[c], x[c]),
-                                    make_float2(acc[2 * pp], acc[2 * pp + 1]));
-        acc[2 * pp] = r.x;
-        acc[2 * pp + 1] = r.y;
+        xq = xn;
     }
-    bad |= ls.overrun();
+    // consumed bits = 32 * words inserted - valid bits
+    const uint32_t valid = (s.V & 127u) + 1u;
+    const uint32_t inserted = (s.pa - code) * 8u;
+    bad |= inserted - valid > 32u * lw;
 }
 
 template <int ELEM>
@@ -513,23 +621,27 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, int lane, cons
 
 template <int ELEM>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1)
-    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, float *partial, uint32_t *counters,
-                uint64_t n_pad) {
+    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, const uint32_t *lut_g,
+                float *partial, uint32_t *counters, uint64_t n_pad) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint8_t *rexp = smem + kRexpOff;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    load_rank_table(m, rexp);
-    __syncthreads();
-    for (uint32_t i = threadIdx.x; i < 4096; i += blockDim.x) lut[i] = lut_entry<ELEM>(i, m.nr, rexp);
+    const uint32_t lut_bar = smem_u32(smem + kLutBarOff);
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16), bar1 = bar0 + 8;
     uint8_t *stage0 = smem + kStageOff + warp * 2 * kStageBytes, *stage1 = stage0 + kStageBytes;
+    load_rank_table(m, rexp);
+    if (threadIdx.x == 0) mbar_init(lut_bar);
     if (lane == 0) {
         mbar_init(bar0);
         mbar_init(bar1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (threadIdx.x == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(lut_bar, kLutBytes);
+        tma_load_1d(smem_u32(lut), lut_g, kLutBytes, lut_bar);
+    }
 
     const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
     uint64_t b = (uint64_t)blockIdx.x * kGemvWarps + warp;
@@ -561,7 +673,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     };
 
     if (b < m.nb) issue(b, 0);
-    for (int it = 0; b < m.nb; it++) {
+    const bool lut_ok = mbar_wait(lut_bar, 0);
+    if (!lut_ok) timed_out = true;
+    for (int it = 0; lut_ok && b < m.nb; it++) {
         const int cur = it & 1;
         const uint64_t nxt = b + total_warps;
         __syncwarp();
@@ -570,7 +684,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         uint32_t bytes;
         region(b, src, bytes);
         const uint8_t *reg = src;
-        if (bytes <= (uint32_t)kStageBytes) {
+        const bool staged = bytes <= (uint32_t)kStageBytes;
+        if (staged) {
             const uint32_t bar = cur ? bar1 : bar0;
             if (!mbar_wait(bar, (phase >> cur) & 1u)) {
                 timed_out = true;
@@ -581,29 +696,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         }
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
-        // activations of this lane's 16 columns, zero past K
-        float xv[16];
         const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
-        const int cols = real_cols(m.k, cb, lane);
-        if (cols == 16 && (reinterpret_cast<uintptr_t>(x + col0) & 15) == 0) {
-            const uint4 *xp = reinterpret_cast<const uint4 *>(x + col0);
-            uint4 q0 = __ldg(xp), q1 = __ldg(xp + 1);
-            const uint32_t u[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                xv[2 * i] = __uint_as_float(u[i] << 16);
-                xv[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 16; c++) xv[c] = c < cols ? __uint_as_float((uint32_t)x[col0 + c] << 16) : 0.0f;
-        }
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; r++) acc[r] = 0.0f;
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
-        if (interior) block_fast<ELEM>(reg, lane, lut, rexp, m.nr, xv, acc, bad);
-        else block_generic<ELEM>(reg, lane, rexp, m.nr, rows, m.k, cb, xv, acc, bad);
+        if (interior && staged) {
+            block_fast<ELEM>(cur ? stage1 : stage0, lane, lut, rexp, m.nr, x + col0, acc, bad);
+        } else {
+            // activations of this lane's 16 columns, zero past K
+            float xv[16];
+            const int cols = real_cols(m.k, cb, lane);
+#pragma unroll
+            for (int c = 0; c < 16; c++) xv[c] = c < cols ? __uint_as_float((uint32_t)x[col0 + c] << 16) : 0.0f;
+            block_generic<ELEM>(reg, lane, rexp, m.nr, rows, m.k, cb, xv, acc, bad);
+        }
         const float sum = transpose_reduce(acc, lane);
         const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
         const uint64_t row = rb * kRows + (uint64_t)row_in;
@@ -612,13 +719,15 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
             if (writer) y[row] = ELEM == 0 ? sum : sum * m.scales[row];
         } else {
             if (writer) partial[cb * n_pad + row] = sum;
-            __threadfence();
             __syncwarp();
             uint32_t ticket = 0;
-            if (lane == 0) ticket = atomicAdd(&counters[rb], 1u);
+            // release: the warp's partial sums (ordered before lane 0 by the warp barrier) are
+            // visible to whoever takes the last ticket; acquire on that side below
+            if (lane == 0)
+                asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
             if (ticket == (uint32_t)m.cbs - 1) {
-                __threadfence();
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
                 if (lane < kRows && rb * kRows + (uint64_t)lane < m.n) {
                     const uint64_t r2 = rb * kRows + (uint64_t)lane;
                     float s = 0.0f;
@@ -635,6 +744,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         // let this warp's own copies land before the CTA's shared memory goes away
         mbar_wait(bar0, phase & 1u);
         mbar_wait(bar1, (phase >> 1) & 1u);
+        if (threadIdx.x == 0) mbar_wait(lut_bar, 0);
     }
     if (bad) raise_error(kErrFormat);
 }
@@ -701,16 +811,40 @@ extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64
     return launched();
 }
 
+namespace {
+// Workspace: [LUT 16 KB][partials fp32 col_blocks x n_pad][counters u32 row_blocks]
+uint64_t ws_partial_off() { return kLutBytes; }
+uint64_t ws_counter_off(const nwc_matrix &m) {
+    return m.col_blocks > 1 ? kLutBytes + 4 * (uint64_t)m.col_blocks * pad_rows(m) : kLutBytes;
+}
+}  // namespace
+
 extern "C" size_t nwc_gemv_workspace_bytes(const nwc_matrix *mp) {
-    if (!mp || mp->col_blocks <= 1) return 0;
-    return (size_t)(4 * (uint64_t)mp->col_blocks * pad_rows(*mp) + 4 * (uint64_t)mp->row_blocks);
+    if (!mp) return 0;
+    uint64_t b = ws_counter_off(*mp);
+    if (mp->col_blocks > 1) b += 4 * (uint64_t)mp->row_blocks;
+    return (size_t)up16(b);
+}
+
+extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws_bytes, nwc_stream stream) {
+    if (!mp || !ws || ws_bytes < nwc_gemv_workspace_bytes(mp) || (reinterpret_cast<uintptr_t>(ws) & 15))
+        return NWC_ERR_INVALID_ARG;
+    const Mat m = to_mat(*mp);
+    uint32_t *lut = static_cast<uint32_t *>(ws);
+    const uint64_t n_counters = mp->col_blocks > 1 ? (uint64_t)mp->row_blocks : 0;
+    uint32_t *counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + ws_counter_off(*mp));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = kLutEntries / 256;
+    if (m.elem == NWC_ELEM_BF16) lut_kernel<0><<<grid, 256, 0, s>>>(m, lut, counters, n_counters);
+    else lut_kernel<1><<<grid, 256, 0, s>>>(m, lut, counters, n_counters);
+    return launched();
 }
 
 extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                                nwc_stream stream) {
-    if (!mp || !x || !y) return NWC_ERR_INVALID_ARG;
-    const size_t need = nwc_gemv_workspace_bytes(mp);
-    if (need && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15))) return NWC_ERR_INVALID_ARG;
+    if (!mp || !x || !y || !ws) return NWC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
+    if (ws_bytes < nwc_gemv_workspace_bytes(mp)) return NWC_ERR_INVALID_ARG;
     const Mat m = to_mat(*mp);
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
@@ -720,15 +854,17 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     std::call_once(once[1], [] { smem_ok[1] = set_smem(gemv_kernel<1>, kGemvSmem); });
     if (!smem_ok[m.elem]) return NWC_ERR_CUDA;
     const uint64_t n_pad = pad_rows(*mp);
-    float *partial = static_cast<float *>(ws);
-    uint32_t *counters = need ? reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + 4 * m.cbs * n_pad) : nullptr;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    const uint32_t *lut = reinterpret_cast<const uint32_t *>(w8);
+    float *partial = reinterpret_cast<float *>(w8 + ws_partial_off());
+    uint32_t *counters = reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp));
     const uint64_t want = (m.nb + kGemvWarps - 1) / kGemvWarps;
     const int grid = (int)(want < (uint64_t)sms ? want : (uint64_t)sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (m.elem == NWC_ELEM_BF16)
-        gemv_kernel<0><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, partial, counters, n_pad);
+        gemv_kernel<0><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, lut, partial, counters, n_pad);
     else
-        gemv_kernel<1><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, partial, counters, n_pad);
+        gemv_kernel<1><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, lut, partial, counters, n_pad);
     return launched();
 }
 

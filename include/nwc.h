@@ -133,19 +133,27 @@ nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *sca
                       nwc_stream stream);
 
 /*
- * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (0 when K <= 512): FP32
- * partial sums per (row, 512-column block) and one counter per 8-row block. The caller zeroes
- * it once after allocating; every nwc_gemv call leaves the counters at zero again, so the
- * same workspace serves repeated calls and CUDA-graph replays. Calls sharing one workspace
- * must not overlap on the GPU.
+ * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 KB): the 4096-entry
+ * decode table of this matrix's rank table (built once by nwc_gemv_prepare), FP32 partial sums
+ * per (row, 512-column block) and one counter per 8-row block (both only when K > 512).
  */
 size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
 
 /*
- * nwc_gemv -- batch-1 y = W x with W decoded in registers ("Fused kernel"): x is BF16[K],
- * y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
- * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes as returned
- * by nwc_gemv_workspace_bytes (16-byte aligned; may be NULL when that size is 0).
+ * nwc_gemv_prepare -- fills a workspace for m: builds the decode table ("A 12-bit peek into a
+ * 16 KB lookup table in shared memory", here kept in the workspace and copied to shared memory
+ * by each CTA) and zeroes the counters. Call once per workspace before its first nwc_gemv; every
+ * nwc_gemv leaves the counters at zero again, so the workspace serves repeated calls and CUDA-
+ * graph replays. ws is 16-byte aligned, ws_bytes >= nwc_gemv_workspace_bytes(m). Calls sharing
+ * one workspace must not overlap on the GPU.
+ */
+nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_stream stream);
+
+/*
+ * nwc_gemv -- batch-1 y = W x with W decoded in registers ("Fused kernel"): x is BF16[K] (16-byte
+ * aligned), y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
+ * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes: a workspace
+ * prepared by nwc_gemv_prepare for this matrix.
  */
 nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                     nwc_stream stream);
