@@ -66,11 +66,12 @@ def lib():
     L.nwc_gemv_workspace_bytes.restype = sz
     L.nwc_gemv_prepare.argtypes = [ctypes.POINTER(NwcMatrix), p, sz, p]
     L.nwc_gemv.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, p]
+    L.nwc_gemv_noalloc.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p]
     L.nwc_gather.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, i64, p]
     L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
     L.nwc_sm_count.restype = i32
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
-                 "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gather", "nwc_check"):
+                 "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gather", "nwc_check"):
         getattr(L, name).restype = i32
     _lib = L
     return L

@@ -868,6 +868,44 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     return launched();
 }
 
+// ---------------------------------------------------------------- allocation-free GEMV
+// Scratch of nwc_gemv_noalloc: the decode table, partial sums and counters of one call live in
+// this file-scope array, which every GPU that loads the library holds until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+extern "C" nwc_status nwc_gemv_noalloc(const nwc_matrix *mp, const uint16_t *x, float *y, nwc_stream stream) {
+    if (!mp || !x || !y) return NWC_ERR_INVALID_ARG;
+    const size_t need = nwc_gemv_workspace_bytes(mp);
+    if (need == 0 || need > kNoAllocScratchBytes) return NWC_ERR_INVALID_ARG;  // matrix too large for the array
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NWC_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return NWC_ERR_UNSUPPORTED;
+    void *ptr = nullptr;
+    {
+        // Host code cannot use the array's name as a device address: resolve it once per device,
+        // with that device current.
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return NWC_ERR_CUDA;
+            g_noalloc_ptr[dev] = p;
+        }
+        ptr = g_noalloc_ptr[dev];
+    }
+    // The array keeps whatever the previous call left: rebuild the decode table and zero the
+    // counters for this matrix, then run the GEMV on the same stream.
+    nwc_status st = nwc_gemv_prepare(mp, ptr, kNoAllocScratchBytes, stream);
+    if (st != NWC_OK) return st;
+    return nwc_gemv(mp, x, y, ptr, kNoAllocScratchBytes, stream);
+}
+
 extern "C" nwc_status nwc_check(nwc_stream stream, uint32_t *flags) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return NWC_ERR_CUDA;

@@ -159,6 +159,23 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
                     nwc_stream stream);
 
 /*
+ * nwc_gemv_noalloc -- nwc_gemv for callers that cannot allocate device memory: no workspace
+ * argument, and no call to cudaMalloc, cudaFree or any allocating routine. The pages have no
+ * counterpart; it exists for hosts where device memory belongs to someone else (for example a
+ * plugin inside an inference server whose allocator owns the whole device, or a real-time loop
+ * where an allocation's implicit device synchronization is not acceptable).
+ * The scratch (decode table, partial sums, counters) is a file-scope 4 MiB device array inside
+ * this library, held by every GPU that loads it until the process exits. A matrix whose
+ * nwc_gemv_workspace_bytes exceeds 4 MiB (about 1M rows x 512-column blocks) is rejected with
+ * NWC_ERR_INVALID_ARG. Every call rebuilds the table and zeroes the counters there, then runs
+ * the GEMV on the stream; results equal nwc_gemv's. All calls share the one array, so calls that
+ * overlap on the GPU (different streams, or different host threads without ordering) race.
+ * The first call on a device resolves the array's device address with cudaGetSymbolAddress
+ * (device current at that moment), so make that first call before any stream capture.
+ */
+nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
+
+/*
  * nwc_gather -- embedding lookup on the same decoder ("Dequantization and embedding lookup
  * (tied lm_head) run on the same decoder"): out row i = row ids[i] of the stored matrix,
  * bit-exact (uint16 BF16 or uint8 e4m3), out[i*ld_out + k]. An id outside [0, N) writes a

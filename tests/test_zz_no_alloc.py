@@ -1,0 +1,63 @@
+"""The allocation-free GEMV entry point (nwc_gemv_noalloc), called through the C ABI.
+
+It is for callers that may not allocate device memory: its scratch is a fixed 4 MiB device
+array inside the library. This file is collected last so that, if it fails, a run that stops at
+the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import decode_gemv_nwc_gb300 as nwc
+import oracle
+from decode_gemv_nwc_gb300 import synth
+
+TOL_REL, TOL_ABS = 2.0 ** -10, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from decode_gemv_nwc_gb300 import build
+    build.build()
+
+
+def _noalloc(mat, x_dev, y_dev):
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return nwc.lib().nwc_gemv_noalloc(ctypes.byref(mat.m), ctypes.c_void_p(x_dev.data_ptr()),
+                                      ctypes.c_void_p(y_dev.data_ptr()), s)
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_gemv_on_two_calls_in_a_row():
+    torch.cuda.init()
+    cases = []
+    for shape, seed in (((520, 2600), 31), ((64, 512), 5)):  # multi- and single-column-block
+        w = synth.normal_bf16(shape, 0.03, seed)
+        x = synth.activations_bf16(shape[1], seed + 1)
+        cases.append((nwc.encode(w), x))
+    for blob, x in cases:
+        mat = nwc.Matrix(blob)
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        y_ref = mat.gemv(xd).cpu().numpy().astype(np.float64)
+        scale = oracle.abs_dot(blob, x)
+        for _ in range(2):
+            y = torch.full((mat.n,), float("nan"), dtype=torch.float32, device="cuda")
+            assert _noalloc(mat, xd, y) == 0
+            st, flags = nwc.check()
+            assert st == 0, f"device error word {flags:#x}"
+            got = y.cpu().numpy().astype(np.float64)
+            assert (np.abs(got - y_ref) <= TOL_REL * scale + TOL_ABS).all()
+
+
+def test_noalloc_rejects_matrices_beyond_its_scratch():
+    """The size check comes before any device call, so a host-only struct suffices."""
+    m = nwc.NwcMatrix()
+    m.elem, m.n_ranked = 0, 11
+    m.n, m.k = 1 << 22, 4096
+    m.row_blocks, m.col_blocks = (1 << 22) // 8, 8
+    m.block_tab = m.data = 0x10000
+    x = ctypes.c_void_p(0x20000)
+    y = ctypes.c_void_p(0x30000)
+    assert nwc.lib().nwc_gemv_noalloc(ctypes.byref(m), x, y, None) == 1
