@@ -68,36 +68,38 @@ def recorded_traffic(workload_key):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clocks and throttle reasons sampled every 100 ms (nvidia-smi loop mode) while running."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
+        self.proc = None
         self.samples = []
-        self._stop = threading.Event()
-        self._t = None
-
-    def _run(self):
-        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
-                vals = [v.strip() for v in out.stdout.strip().split(",")]
-                if len(vals) == 6:
-                    self.samples.append(vals)
-            except Exception:
-                pass
-            self._stop.wait(0.2)
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
-        self._t.join(timeout=10)
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            vals = [v.strip() for v in line.split(",")]
+            if len(vals) == 6:
+                self.samples.append(vals)
 
     def summary(self):
         if not self.samples:
@@ -156,6 +158,133 @@ def oracle_sample(seconds_budget=12.0):
     return statistics.median(times) * 1e6, len(times)
 
 
+def time_graph(fn, stream, steps, warmup=3):
+    """Captures fn() (launches on `stream`) once as a CUDA graph; returns ms per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def encode_on_host(w_dev, elem=0):
+    """Device BF16 bits -> blob (the host encoder runs on the CPU cores)."""
+    import decode_gemv_nwc_gb300 as nwc
+    w = w_dev.cpu().numpy().view(np.uint16)
+    return nwc.encode(w, elem=elem)
+
+
+def extra_workloads(dev, stream, steps):
+    """The other configurations of the pages' workloads, measured the same way."""
+    import torch
+    import decode_gemv_nwc_gb300 as nwc
+    from decode_gemv_nwc_gb300 import synth
+    out = {}
+    peak, _ = peaks()
+
+    # 36-layer decoder stack, one token = one GEMV per matrix (252), as one CUDA graph
+    t0 = time.time()
+    mats, xs, ys, wbf = [], {}, [], []
+    comp_bytes = 0
+    for layer in range(synth.N_LAYERS):
+        for name, n, k in synth.LAYER_SHAPES:
+            w = synth.layer_matrix(layer, name, device=dev)
+            blob = encode_on_host(w)
+            comp_bytes += len(blob)
+            mats.append(nwc.Matrix(blob, device=dev))
+            wbf.append(w.view(torch.bfloat16))
+            if k not in xs:
+                xs[k] = torch.from_numpy(synth.activations_bf16(k, 2000 + k).view(np.int16)).to(dev)
+            ys.append(torch.empty(n, dtype=torch.float32, device=dev))
+    build_s = time.time() - t0
+
+    def stack():
+        for m, y in zip(mats, ys):
+            m.gemv(xs[m.k], y=y, stream=stream)
+
+    yb = [torch.empty(w.shape[0], dtype=torch.bfloat16, device=dev) for w in wbf]
+
+    def stack_bf16():
+        for w, y in zip(wbf, yb):
+            torch.mv(w, xs[w.shape[1]].view(torch.bfloat16), out=y)
+
+    tok_ms = time_graph(stack, stream, max(3, steps // 2))
+    tok_bf16 = time_graph(stack_bf16, stream, max(3, steps // 2))
+    bf16_bytes = sum(2 * w.numel() for w in wbf)
+    out["stack_token"] = {
+        "workload": "36-layer stack (q,k,v,o,gate,up,down), one batch-1 GEMV per matrix, one CUDA graph",
+        "gemvs": len(mats), "us_per_token": tok_ms * 1e3, "compressed_bytes": comp_bytes,
+        "compressed_gbs": comp_bytes / (tok_ms * 1e-3) / 1e9, "frac_of_measured_hbm": comp_bytes / (tok_ms * 1e-3) / 1e9 / peak,
+        "bf16_cublas_us_per_token": tok_bf16 * 1e3, "bf16_bytes": bf16_bytes, "speedup_vs_bf16": tok_bf16 / tok_ms,
+        "build_seconds": build_s}
+    del mats, wbf, ys, yb
+    torch.cuda.empty_cache()
+
+    # tied embedding / lm_head 151936 x 2560: gather 4096 ids, then the lm_head GEMV
+    w = synth.normal_bf16((synth.VOCAB, synth.HIDDEN), 0.02, 7, device=dev)
+    blob = encode_on_host(w)
+    m = nwc.Matrix(blob, device=dev)
+    x = torch.from_numpy(synth.activations_bf16(synth.HIDDEN, 9).view(np.int16)).to(dev)
+    y = torch.empty(synth.VOCAB, dtype=torch.float32, device=dev)
+    ids = torch.from_numpy(synth.token_ids(4096, synth.VOCAB, seed=8)).to(dev)
+    g_out = torch.empty((4096, synth.HIDDEN), dtype=torch.int16, device=dev)
+    lm_ms = time_graph(lambda: m.gemv(x, y=y, stream=stream), stream, steps)
+    ga_ms = time_graph(lambda: m.gather(ids, out=g_out, stream=stream), stream, steps)
+    wb = w.view(torch.bfloat16)
+    yb = torch.empty(synth.VOCAB, dtype=torch.bfloat16, device=dev)
+    lm_bf16 = time_graph(lambda: torch.mv(wb, x.view(torch.bfloat16), out=yb), stream, steps)
+    out["lm_head"] = {"workload": "lm_head GEMV 151936x2560", "us": lm_ms * 1e3, "compressed_bytes": len(blob),
+                      "compressed_gbs": len(blob) / (lm_ms * 1e-3) / 1e9,
+                      "frac_of_measured_hbm": len(blob) / (lm_ms * 1e-3) / 1e9 / peak,
+                      "bf16_cublas_us": lm_bf16 * 1e3, "speedup_vs_bf16": lm_bf16 / lm_ms}
+    out["gather"] = {"workload": "gather 4096 ids from the 151936x2560 table", "us": ga_ms * 1e3,
+                     "rows_per_s": 4096 / (ga_ms * 1e-3), "out_gbs": 4096 * synth.HIDDEN * 2 / (ga_ms * 1e-3) / 1e9}
+    del m, w, wb
+    torch.cuda.empty_cache()
+
+    # fp8 gate 9728x2560 and down 2560x9728, 12 rotated copies each (> L2)
+    for name, (n, k) in (("gate", (9728, 2560)), ("down", (2560, 9728))):
+        w = synth.normal_bf16((n, k), 0.02, 50 + n, device=dev)
+        blob = encode_on_host(w, elem=1)
+        host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+        ms8 = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(12)]
+        x = torch.from_numpy(synth.activations_bf16(k, 77).view(np.int16)).to(dev)
+        y = torch.empty(n, dtype=torch.float32, device=dev)
+
+        def run8():
+            for mm in ms8:
+                mm.gemv(x, y=y, stream=stream)
+        t = time_graph(run8, stream, steps) / len(ms8)
+        wbs = [w.view(torch.bfloat16).clone() for _ in range(12)]
+        yb = torch.empty(n, dtype=torch.bfloat16, device=dev)
+
+        def runbf():
+            for ww in wbs:
+                torch.mv(ww, x.view(torch.bfloat16), out=yb)
+        tb = time_graph(runbf, stream, steps) / len(wbs)
+        out[f"fp8_{name}"] = {"workload": f"fp8 e4m3 {name} {n}x{k}, 12 rotated copies", "us": t * 1e3,
+                              "compressed_bytes": len(blob), "fp8_bytes": n * k,
+                              "compressed_gbs": len(blob) / (t * 1e-3) / 1e9,
+                              "frac_of_measured_hbm": len(blob) / (t * 1e-3) / 1e9 / peak,
+                              "bf16_cublas_us": tb * 1e3}
+        del ms8, wbs
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -182,10 +311,11 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="nwc", choices=["nwc", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -300,6 +430,18 @@ def main():
     st, flags = nwc.check(stream)
     assert st == 0, f"device error word {flags:#x}"
 
+    # decode to BF16 (dequantization) of the same matrix: writes 2NK bytes
+    dec_out = torch.empty((N_ROWS, K_COLS), dtype=torch.int16, device=dev)
+    dec_ms = time_graph(lambda: mats[0].decode(out=dec_out, stream=stream), stream, args.steps)
+    extras = {"decode": {"workload": "decode 4096x4096 to BF16", "us": dec_ms * 1e3,
+                         "write_gbs": 2 * N_ROWS * K_COLS / (dec_ms * 1e-3) / 1e9}}
+    del mats[1:]
+    torch.cuda.empty_cache()
+    if not args.quick:
+        extras.update(extra_workloads(dev, stream, args.steps))
+    st, flags = nwc.check(stream)
+    assert st == 0, f"device error word {flags:#x}"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us, n = oracle_sample()
@@ -330,6 +472,7 @@ def main():
             "clocks": clocks.summary(),
             "sm_count": nwc.sm_count(),
             "cpu_baseline": cpu,
+            "workloads": extras,
         }
         print(json.dumps(line))
     if world > 1:
