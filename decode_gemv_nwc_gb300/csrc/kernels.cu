@@ -335,16 +335,26 @@ __global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, 
 }
 
 // =================================================================== GEMV kernel
-constexpr int kGemvWarps = 16;
+// Warps per CTA (one CTA per SM) and block-region stages per warp. With one stage the next
+// region is prefetched into L2 while the current one is decoded, then copied in.
+#ifndef NWC_GEMV_WARPS
+#define NWC_GEMV_WARPS 32
+#endif
+#ifndef NWC_GEMV_STAGES
+#define NWC_GEMV_STAGES 1
+#endif
+constexpr int kGemvWarps = NWC_GEMV_WARPS;
+constexpr int kStagesPerWarp = NWC_GEMV_STAGES;
 constexpr int kStageBytes = 6144;
 constexpr int kLutEntries = 4096;
 constexpr int kLutBytes = kLutEntries * 4;
 constexpr int kRexpOff = kLutBytes;
 constexpr int kLutBarOff = kRexpOff + 16;
 constexpr int kBarOff = kLutBarOff + 8;
-constexpr int kStageOff = 16768;  // 128-aligned, after LUT, rank table and barriers
-constexpr int kGemvSmem = kStageOff + kGemvWarps * 2 * kStageBytes;
-static_assert(kBarOff + kGemvWarps * 2 * 8 <= kStageOff, "smem layout");
+constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
+constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes;
+static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
+static_assert(kGemvSmem <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -629,7 +639,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lut_bar = smem_u32(smem + kLutBarOff);
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16), bar1 = bar0 + 8;
-    uint8_t *stage0 = smem + kStageOff + warp * 2 * kStageBytes, *stage1 = stage0 + kStageBytes;
+    uint8_t *stage0 = smem + kStageOff + warp * kStagesPerWarp * kStageBytes,
+            *stage1 = stage0 + (kStagesPerWarp - 1) * kStageBytes;
     load_rank_table(m, rexp);
     if (threadIdx.x == 0) mbar_init(lut_bar);
     if (lane == 0) {
@@ -676,10 +687,19 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     const bool lut_ok = mbar_wait(lut_bar, 0);
     if (!lut_ok) timed_out = true;
     for (int it = 0; lut_ok && b < m.nb; it++) {
-        const int cur = it & 1;
+        const int cur = kStagesPerWarp == 2 ? (it & 1) : 0;
         const uint64_t nxt = b + total_warps;
         __syncwarp();
-        if (nxt < m.nb) issue(nxt, cur ^ 1);
+        if (kStagesPerWarp == 2) {
+            if (nxt < m.nb) issue(nxt, cur ^ 1);
+        } else if (nxt < m.nb && lane == 0) {
+            const uint8_t *nsrc;
+            uint32_t nbytes;
+            const uint32_t s0 = m.tab[nxt], s1 = m.tab[nxt + 1];
+            nsrc = m.data + 16 * (uint64_t)s0;
+            nbytes = 16 * (s1 - s0);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nsrc), "r"(nbytes) : "memory");
+        }
         const uint8_t *src;
         uint32_t bytes;
         region(b, src, bytes);
@@ -737,13 +757,17 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
                 if (lane == 0) counters[rb] = 0;
             }
         }
+        if (kStagesPerWarp == 1) {
+            __syncwarp();
+            if (nxt < m.nb) issue(nxt, 0);
+        }
         b = nxt;
     }
     if (timed_out) {
         raise_error(kErrTimeout);
         // let this warp's own copies land before the CTA's shared memory goes away
         mbar_wait(bar0, phase & 1u);
-        mbar_wait(bar1, (phase >> 1) & 1u);
+        if (kStagesPerWarp == 2) mbar_wait(bar1, (phase >> 1) & 1u);
         if (threadIdx.x == 0) mbar_wait(lut_bar, 0);
     }
     if (bad) raise_error(kErrFormat);
