@@ -126,14 +126,20 @@ def dist_setup(gpus):
     return rank, world, local
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """Max of a per-rank float over all ranks (the job's time is its slowest replica)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_us_per_matrix(max_ms, launches_per_rank, world):
+    """Whole-job value: the slowest rank's time divided by the matrices all ranks processed."""
+    return max_ms * 1e3 / (launches_per_rank * world)
 
 
 def barrier(world):
@@ -373,7 +379,7 @@ def main():
     ms_local = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms_local, world)
     launches = args.steps * COPIES
-    us_per_matrix_job = ms * 1e3 / (launches * world)
+    us_per_matrix_job = job_us_per_matrix(ms, launches, world)
     us_per_launch = ms_local * 1e3 / launches
 
     # algorithmic bytes per launch: the whole blob + x (BF16) + y (FP32)
