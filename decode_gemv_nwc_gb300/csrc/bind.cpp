@@ -2,10 +2,12 @@
 //
 // Validation covers everything the kernels trust without checking: header fields, the rank
 // table ("the exponent is ranked by frequency", at most 11 ranked values), the block table,
-// and each block region's size, which must equal its 32 lane word counts plus the mantissa
+// each block region's size, which must equal its 32 lane word counts plus the mantissa
 // regions implied by the block's real rows and columns (fillers carry no mantissa, as the
-// "How it works" section of "NWC -- Neural Weight Compression" states). Stream contents are
-// checked on the device while decoding.
+// "How it works" section of "NWC -- Neural Weight Compression" states) plus its escape list,
+// and the escape list itself: every entry names a real element of the block, in (lane, t)
+// order without repeats, with an unranked exponent, followed by fewer than four padding words.
+// Lane stream contents are checked on the device while decoding.
 #include <cstring>
 
 #include "nwc.h"
@@ -88,7 +90,27 @@ nwc_status parse_and_check(const uint8_t *b, uint64_t bytes, Parsed &p) {
             words += lw[l];
             man += man_words(rows, real_cols(p.k, cb, l), F);
         }
-        if (up16(32 + 4 * words) + 4 * man != len) return NWC_ERR_FORMAT;
+        const uint64_t esc_off = up16(32 + 4 * words) + 4 * man;
+        if (esc_off > len) return NWC_ERR_FORMAT;
+        const uint64_t slots = (len - esc_off) / 4;
+        int64_t last = -1;
+        uint64_t entries = 0;
+        for (uint64_t j = 0; j < slots; j++) {
+            const uint32_t e = rd32(lw + esc_off + 4 * j);
+            if (e == kEscPad) continue;
+            if (entries != j) return NWC_ERR_FORMAT;  // an entry after padding
+            const int64_t key = (int64_t)esc_lane(e) * kSyms + esc_t(e);
+            if (key <= last) return NWC_ERR_FORMAT;
+            last = key;
+            const int t = (int)esc_t(e);
+            if (t % kRows >= rows || t / kRows >= real_cols(p.k, cb, (int)esc_lane(e))) return NWC_ERR_FORMAT;
+            const uint32_t bits = esc_bits(e);
+            if (bits >> (p.elem == NWC_ELEM_BF16 ? 16 : 8)) return NWC_ERR_FORMAT;
+            const uint32_t v = p.elem == NWC_ELEM_BF16 ? (bits >> 7) & 0xFFu : (bits >> 3) & 0xFu;
+            if (seen[v]) return NWC_ERR_FORMAT;  // a ranked exponent is never escaped
+            entries++;
+        }
+        if (slots - entries > 3) return NWC_ERR_FORMAT;
         if (len > p.max_block) p.max_block = len;
     }
     p.data_bytes = bytes - p.off_data;
@@ -110,7 +132,7 @@ extern "C" const char *nwc_status_str(nwc_status s) {
     return "unknown status";
 }
 
-extern "C" const char *nwc_version(void) { return "nwc 1 (format 1, sm_103a)"; }
+extern "C" const char *nwc_version(void) { return "nwc 2 (format 2, sm_103a)"; }
 
 extern "C" nwc_status nwc_validate(const void *blob_host, size_t bytes) {
     Parsed p;

@@ -2,9 +2,10 @@
 //
 // "NWC -- Neural Weight Compression", section "How it works": a BF16 weight is split into a
 // raw mantissa plane and an exponent/sign part; the exponent is ranked by frequency and
-// written as a unary rank code plus a raw sign bit, with an escape (followed by the raw
-// exponent bits) for rare values; every lane of a block of 8 rows x 512 columns has its own
-// bit stream; padding to any shape costs 2 bits per filler weight and no mantissa.
+// written as a unary rank code plus a raw sign bit, with an escape for rare values (in the
+// stream n_ranked ones and the sign; the element's bits go to the block's escape list, so that
+// no in-stream code is longer than 12 bits); every lane of a block of 8 rows x 512 columns has
+// its own bit stream; padding to any shape costs 2 bits per filler weight and no mantissa.
 // "Qwen3-4B-NWC-fp8": weight-only e4m3, symmetric per-output-channel scale, bytes coded
 // losslessly with the same code (4-bit exponent, 3-bit raw mantissa).
 //
@@ -30,6 +31,7 @@ struct Codebook {
     uint32_t code[256];  // code of the exponent value with its sign slot (sign bit = 0)
     uint8_t len[256];    // code length including the sign bit
     uint8_t rank_exp[16];
+    bool escaped[256];
 };
 
 // Ranking: values with a nonzero count, most frequent first, ties to the lower value;
@@ -46,15 +48,17 @@ Codebook make_codebook(const uint64_t *hist, int elem) {
     std::stable_sort(vals.begin(), vals.end(), [&](int a, int b) { return hist[a] > hist[b]; });
     cb.nr = std::min<int>((int)vals.size(), kMaxRanked);
     std::memset(cb.rank_exp, 0, sizeof(cb.rank_exp));
-    for (int v = 0; v < nv; v++) {  // escape: nr ones, raw exponent, sign
-        cb.code[v] = (((1u << cb.nr) - 1u) << (cb.eb + 1)) | ((uint32_t)v << 1);
-        cb.len[v] = (uint8_t)(cb.nr + cb.eb + 1);
+    for (int v = 0; v < nv; v++) {  // escape: nr ones, sign
+        cb.code[v] = ((1u << cb.nr) - 1u) << 1;
+        cb.len[v] = (uint8_t)(cb.nr + 1);
+        cb.escaped[v] = true;
     }
     for (int p = 0; p < cb.nr; p++) {  // rank p: p ones, a zero, sign
         int v = vals[p];
         cb.rank_exp[p] = (uint8_t)v;
         cb.code[v] = ((1u << p) - 1u) << 2;
         cb.len[v] = (uint8_t)(p + 2);
+        cb.escaped[v] = false;
     }
     return cb;
 }
@@ -121,7 +125,7 @@ struct HalfSink {
 template <class E>
 uint64_t block_size(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *lw) {
     int rows = real_rows(src.n, rb);
-    uint64_t code_words = 0, man = 0;
+    uint64_t code_words = 0, man = 0, n_esc = 0;
     for (int l = 0; l < kLanes; l++) {
         int cols = real_cols(src.k, cbi, l);
         uint32_t bits = 2u * (uint32_t)(kSyms - rows * cols);  // fillers
@@ -130,17 +134,18 @@ uint64_t block_size(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_
                 uint32_t s, v, m;
                 fields(cbk.elem, src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m);
                 bits += cbk.len[v];
+                n_esc += cbk.escaped[v];
             }
         uint32_t nw = (bits + 31) / 32;
         if (lw) lw[l] = (uint8_t)nw;
         code_words += nw;
         man += man_words(rows, cols, cbk.F);
     }
-    return up16(32 + 4 * code_words) + 4 * man;
+    return up16(32 + 4 * code_words) + 4 * man + up16(4 * n_esc);
 }
 
 template <class E>
-void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *dst) {
+void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *dst, uint64_t size) {
     int rows = real_rows(src.n, rb);
     uint32_t *words = reinterpret_cast<uint32_t *>(dst + 32);  // dst is 16-byte aligned
     uint32_t pos = 0;
@@ -180,6 +185,20 @@ void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t c
         }
         man += 4 * mw;
     }
+    // escape list: lanes in order, t increasing; padding to the region's end
+    uint32_t *esc = reinterpret_cast<uint32_t *>(man);
+    uint32_t *esc_end = reinterpret_cast<uint32_t *>(dst + size);
+    for (int l = 0; l < kLanes; l++) {
+        int cols = real_cols(src.k, cbi, l);
+        for (int t = 0; t < kSyms; t++) {
+            int c = t / kRows, r = t % kRows;
+            if (r >= rows || c >= cols) continue;
+            uint32_t x = src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m;
+            fields(cbk.elem, x, s, v, m);
+            if (cbk.escaped[v]) *esc++ = esc_entry((uint32_t)t, (uint32_t)l, x);
+        }
+    }
+    while (esc < esc_end) *esc++ = kEscPad;
 }
 
 int pick_threads(int threads) {
@@ -283,10 +302,10 @@ nwc_status encode_impl(const Src<E> &src, int elem, const float *scales, int thr
             uint8_t *dst = b + off_data + off[bi];
             if (aligned) {
                 std::memset(dst, 0, size[bi]);
-                write_block(src, cbk, rb, c, dst);
+                write_block(src, cbk, rb, c, dst, size[bi]);
             } else {
                 tmp.assign(size[bi] / 4, 0);
-                write_block(src, cbk, rb, c, reinterpret_cast<uint8_t *>(tmp.data()));
+                write_block(src, cbk, rb, c, reinterpret_cast<uint8_t *>(tmp.data()), size[bi]);
                 std::memcpy(dst, tmp.data(), size[bi]);
             }
         }

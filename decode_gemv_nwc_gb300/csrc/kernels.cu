@@ -9,6 +9,12 @@
 //   * a 12-bit peek into a 16 KB shared-memory lookup table yields two complete codes per
 //     step; the bit window is shifted and refilled from the lane's words;
 //   * dequantization and embedding lookup run on the same decoder.
+// Escapes ("escape for rare values"): the stream holds n_ranked ones and the sign, the element's
+// bits are in the block's escape list. Every in-stream code thus fits the 12-bit peek and the
+// GEMV's hot loop has no escape branch: it multiplies a placeholder (the sign and raw mantissa
+// with exponent field 0, a subnormal) and the warp adds (true - placeholder) * x for each list
+// entry before its row reduction. Decode and gather write the listed elements over the
+// placeholders.
 // "Qwen3-4B-NWC-fp8": the per-channel scale is applied at the end of the matvec.
 //
 // GB300 choices: the GEMV is a persistent grid sized from the queried SM count; each warp
@@ -28,16 +34,14 @@
 
 using namespace nwcf;
 
-// Device error word: bit 0 = malformed stream (a lane read past its words), bit 1 = gather
-// id out of range, bit 2 = a bounded wait ran out. Read and cleared by nwc_check.
+// Device error word: bit 0 = malformed stream (a lane read past its words, or an escape list
+// that does not match the lane streams), bit 1 = gather id out of range, bit 2 = a bounded wait
+// ran out. Read and cleared by nwc_check.
 __device__ uint32_t g_nwc_error;
 
 namespace {
 
 constexpr uint32_t kErrFormat = 1u, kErrId = 2u, kErrTimeout = 4u;
-// LUT entry flag: the code at the peek is the escape prefix (n_ranked ones); the raw exponent
-// and the sign follow it in the stream.
-constexpr uint32_t kEsc = 1u << 16;
 
 struct Mat {
     int elem, nr;
@@ -115,25 +119,24 @@ struct LaneStream {
     }
 };
 
-// One code: rank p < nr is p ones, a zero, the sign; an escape is nr ones, the raw exponent
-// (EB bits, most significant first), the sign.
-template <int ELEM, class S>
-__device__ __forceinline__ void decode_one(S &ls, int nr, const uint8_t *rexp, uint32_t &s, uint32_t &v) {
-    constexpr int EB = ELEM == 0 ? 8 : 4;
+// One code: rank p < nr is p ones, a zero, the sign; an escape is nr ones and the sign (its
+// exponent is in the escape list; v is returned as 0). Returns whether it was an escape.
+template <class S>
+__device__ __forceinline__ bool decode_one(S &ls, int nr, const uint8_t *rexp, uint32_t &s, uint32_t &v) {
     ls.refill();
     const uint32_t top = ls.top();
     const int ones = __clz(~top);
-    int L;
-    if (ones < nr) {
+    const bool esc = ones >= nr;
+    if (!esc) {
         v = rexp[ones];
         s = (top >> (30 - ones)) & 1u;
-        L = ones + 2;
+        ls.consume((uint32_t)ones + 2u);
     } else {
-        v = (top << nr) >> (32 - EB);
-        s = (top >> (31 - nr - EB)) & 1u;
-        L = nr + EB + 1;
+        v = 0;
+        s = (top >> (31 - nr)) & 1u;
+        ls.consume((uint32_t)nr + 1u);
     }
-    ls.consume(L);
+    return esc;
 }
 
 // Field j of the even (odd = 0) or odd (odd = 1) mantissa half-stream of a lane region.
@@ -167,35 +170,63 @@ __device__ __forceinline__ uint32_t elem_bits(uint32_t s, uint32_t v, uint32_t m
     return ELEM == 0 ? ((s << 15) | (v << 7) | m) : ((s << 7) | (v << 3) | m);
 }
 
-// Generic decode of one lane of one block: calls fn(t, s, v, m) for each real element t
-// (t = 8c + r, both static after unrolling). rows/cols are the lane's real extent.
+// Generic decode of one lane of one block: calls fn(t, s, v, m, esc) for each real element t
+// (t = 8c + r, both static after unrolling). rows/cols are the lane's real extent. Returns the
+// number of escape codes in the lane's 128 codes.
 template <int ELEM, class Fn>
-__device__ __forceinline__ void lane_generic(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
-                                             const uint8_t *rexp, Fn &&fn) {
+__device__ __forceinline__ uint32_t lane_generic(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
+                                                 const uint8_t *rexp, Fn &&fn) {
     constexpr int F = ELEM == 0 ? 7 : 3;
-    uint32_t je = 0, jo = 0;
+    uint32_t je = 0, jo = 0, n_esc = 0;
 #pragma unroll
     for (int t = 0; t < kSyms; t++) {
         const int c = t >> 3, r = t & 7;
         uint32_t s, v;
-        decode_one<ELEM>(ls, nr, rexp, s, v);
+        const bool esc = decode_one(ls, nr, rexp, s, v);
+        n_esc += esc;
         if (r < rows && c < cols) {
             uint32_t m;
             if (r & 1) m = half_field<F>(man, 1, jo++);
             else m = half_field<F>(man, 0, je++);
-            fn(t, s, v, m);
+            fn(t, s, v, m, esc);
         }
     }
+    return n_esc;
 }
 
-// Layout facts of one block region at `reg` for this lane.
+// The same decode with the column loop rolled (rows unrolled): fn(c, r, s, v, m, esc) with c
+// dynamic. Smaller code and fewer live registers, for callers that need no static column.
+template <int ELEM, class Fn>
+__device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
+                                                const uint8_t *rexp, Fn &&fn) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    uint32_t je = 0, jo = 0, n_esc = 0;
+#pragma unroll 1
+    for (int c = 0; c < kLaneCols; c++) {
+#pragma unroll
+        for (int r = 0; r < kRows; r++) {
+            uint32_t s, v;
+            const bool esc = decode_one(ls, nr, rexp, s, v);
+            n_esc += esc;
+            if (r < rows && c < cols) {
+                uint32_t m;
+                if (r & 1) m = half_field<F>(man, 1, jo++);
+                else m = half_field<F>(man, 0, je++);
+                fn(c, r, s, v, m, esc);
+            }
+        }
+    }
+    return n_esc;
+}
+
+// Layout facts of one block region at `reg` (`bytes` long) for this lane.
 struct LaneRegion {
-    const uint32_t *code, *man;
-    uint32_t nwords;
+    const uint32_t *code, *man, *esc;
+    uint32_t nwords, slots;  // slots = escape-list words (entries and padding)
 };
 
-__device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, int lane, int rows, uint64_t k,
-                                                  uint64_t cb, int F) {
+__device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, uint32_t bytes, int lane, int rows,
+                                                  uint64_t k, uint64_t cb, int F) {
     const uint32_t lw = reg[lane];
     uint32_t incl = lw;
 #pragma unroll
@@ -215,8 +246,56 @@ __device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, int lane, 
         uint32_t o = __shfl_up_sync(0xFFFFFFFFu, mincl, d);
         if (lane >= d) mincl += o;
     }
-    lr.man = reinterpret_cast<const uint32_t *>(reg + up16(32 + 4 * (uint64_t)total)) + (mincl - mw);
+    const uint32_t man0 = (uint32_t)up16(32 + 4 * (uint64_t)total);
+    lr.man = reinterpret_cast<const uint32_t *>(reg + man0) + (mincl - mw);
+    const uint32_t esc0 = man0 + 4 * __shfl_sync(0xFFFFFFFFu, mincl, 31);
+    lr.esc = reinterpret_cast<const uint32_t *>(reg + esc0);
+    lr.slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
     return lr;
+}
+
+// This lane's slice [start, start + cnt) of the block's escape list, from the lanes' escape
+// counts; flags a list whose entry count differs from the streams' total or that is followed by
+// more than three padding words.
+__device__ __forceinline__ uint32_t esc_slice(const LaneRegion &lr, uint32_t cnt, int lane, bool &bad) {
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (lane == 0) {
+        if (total > lr.slots || lr.slots - total > 3) bad = true;
+        else if (total < lr.slots && lr.esc[total] != kEscPad) bad = true;
+    }
+    return incl - cnt;
+}
+
+// Writes this lane's escape-list entries [start, start + cnt) over their placeholders in the
+// output: element (r, c) of the lane goes to out[(row0 + r) * ld_out + col0 + c], only for
+// r == want when want >= 0. Checks that each entry names this lane and a real element of it;
+// returns false if one does not. Kept out of line: inlined after the fully unrolled lane
+// decode it more than doubled the decoders' register use.
+template <int ELEM>
+__device__ __noinline__ bool esc_patch(const uint32_t *esc, uint32_t slots, uint32_t start, uint32_t cnt, int lane,
+                                       int rows, int cols, int want, void *out, int64_t ld_out, int64_t row0,
+                                       uint64_t col0) {
+    bool ok = true;
+    for (uint32_t i = 0; i < cnt; i++) {
+        const uint32_t j = start + i;
+        const uint32_t e = j < slots ? esc[j] : kEscPad;
+        const int t = (int)esc_t(e), c = t >> 3, r = t & 7;
+        if (e == kEscPad || (int)esc_lane(e) != lane || r >= rows || c >= cols) {
+            ok = false;
+            continue;
+        }
+        if (want >= 0 && r != want) continue;
+        const uint64_t at = (uint64_t)(row0 + r) * (uint64_t)ld_out + col0 + (uint64_t)c;
+        if (ELEM == 0) static_cast<uint16_t *>(out)[at] = (uint16_t)esc_bits(e);
+        else static_cast<uint8_t *>(out)[at] = (uint8_t)esc_bits(e);
+    }
+    return ok;
 }
 
 // =================================================================== decode kernel
@@ -231,8 +310,9 @@ __global__ void __launch_bounds__(256) decode_kernel(Mat m, void *out, int64_t l
     for (uint64_t b = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < m.nb; b += warps) {
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb), cols = real_cols(m.k, cb, lane);
-        const uint8_t *reg = m.data + 16 * (uint64_t)m.tab[b];
-        LaneRegion lr = lane_region(reg, lane, rows, m.k, cb, F);
+        const uint32_t t0 = m.tab[b], t1 = m.tab[b + 1];
+        const uint8_t *reg = m.data + 16 * (uint64_t)t0;
+        LaneRegion lr = lane_region(reg, 16 * (t1 - t0), lane, rows, m.k, cb, F);
         LaneStream ls;
         ls.init(lr.code, lr.nwords);
         uint32_t o[8][8];  // [row][column pair] two elements per word (BF16) / [row][4 bytes]
@@ -240,13 +320,15 @@ __global__ void __launch_bounds__(256) decode_kernel(Mat m, void *out, int64_t l
         for (int r = 0; r < 8; r++)
 #pragma unroll
             for (int i = 0; i < 8; i++) o[r][i] = 0;
-        lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
-            const int c = t >> 3, r = t & 7;
-            const uint32_t e = elem_bits<ELEM>(s, v, mm);
-            if (ELEM == 0) o[r][c >> 1] |= e << (16 * (c & 1));
-            else o[r][c >> 2] |= e << (8 * (c & 3));
-        });
-        if (ls.overrun()) raise_error(kErrFormat);
+        const uint32_t n_esc =
+            lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm, bool) {
+                const int c = t >> 3, r = t & 7;
+                const uint32_t e = elem_bits<ELEM>(s, v, mm);
+                if (ELEM == 0) o[r][c >> 1] |= e << (16 * (c & 1));
+                else o[r][c >> 2] |= e << (8 * (c & 3));
+            });
+        bool bad = ls.overrun();
+        const uint32_t esc_start = esc_slice(lr, n_esc, lane, bad);
         const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
 #pragma unroll
         for (int r = 0; r < 8; r++) {
@@ -273,6 +355,11 @@ __global__ void __launch_bounds__(256) decode_kernel(Mat m, void *out, int64_t l
                 }
             }
         }
+        // escaped elements over their placeholders (same thread, so after the stores above)
+        if (!esc_patch<ELEM>(lr.esc, lr.slots, esc_start, n_esc, lane, rows, cols, -1, out, ld_out,
+                             (int64_t)(rb * kRows), col0))
+            bad = true;
+        if (bad) raise_error(kErrFormat);
     }
 }
 
@@ -295,17 +382,24 @@ __global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, 
         uint32_t o[8];
 #pragma unroll
         for (int c = 0; c < 8; c++) o[c] = 0;
-        if (id < 0 || (uint64_t)id >= m.n) {
+        LaneRegion lr{};
+        uint32_t n_esc = 0, esc_start = 0;
+        int rows = 0, want = 0;
+        bool bad = false;
+        const bool valid = id >= 0 && (uint64_t)id < m.n;
+        if (!valid) {
             if (lane == 0 && cb == 0) raise_error(kErrId);
         } else {
             const uint64_t rb = (uint64_t)id >> 3;
-            const int want = (int)(id & 7);
-            const int rows = real_rows(m.n, rb);
-            const uint8_t *reg = m.data + 16 * (uint64_t)m.tab[rb * m.cbs + cb];
-            LaneRegion lr = lane_region(reg, lane, rows, m.k, cb, F);
+            want = (int)(id & 7);
+            rows = real_rows(m.n, rb);
+            const uint32_t t0 = m.tab[rb * m.cbs + cb], t1 = m.tab[rb * m.cbs + cb + 1];
+            const uint8_t *reg = m.data + 16 * (uint64_t)t0;
+            lr = lane_region(reg, 16 * (t1 - t0), lane, rows, m.k, cb, F);
             LaneStream ls;
             ls.init(lr.code, lr.nwords);
-            lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
+            n_esc = lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp,
+                                       [&](int t, uint32_t s, uint32_t v, uint32_t mm, bool) {
                 const int c = t >> 3, r = t & 7;
                 if (r == want) {
                     const uint32_t e = elem_bits<ELEM>(s, v, mm);
@@ -313,7 +407,8 @@ __global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, 
                     else o[c >> 2] |= e << (8 * (c & 3));
                 }
             });
-            if (ls.overrun()) raise_error(kErrFormat);
+            bad = ls.overrun();
+            esc_start = esc_slice(lr, n_esc, lane, bad);
         }
         if (ELEM == 0) {
             uint16_t *dst = static_cast<uint16_t *>(out) + i * (uint64_t)ld_out + col0;
@@ -321,15 +416,27 @@ __global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, 
                 reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
             } else {
-                for (int c = 0; c < cols; c++) dst[c] = (uint16_t)(o[c >> 1] >> (16 * (c & 1)));
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    if (c < cols) dst[c] = (uint16_t)(o[c >> 1] >> (16 * (c & 1)));
             }
         } else {
             uint8_t *dst = static_cast<uint8_t *>(out) + i * (uint64_t)ld_out + col0;
             if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
                 reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
             } else {
-                for (int c = 0; c < cols; c++) dst[c] = (uint8_t)(o[c >> 2] >> (8 * (c & 3)));
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    if (c < cols) dst[c] = (uint8_t)(o[c >> 2] >> (8 * (c & 3)));
             }
+        }
+        if (valid) {
+            // escaped elements of the wanted row over their placeholders (same thread: after
+            // the stores above)
+            if (!esc_patch<ELEM>(lr.esc, lr.slots, esc_start, n_esc, lane, rows, cols, want, out, ld_out,
+                                 (int64_t)i - want, col0))
+                bad = true;
+            if (bad) raise_error(kErrFormat);
         }
     }
 }
@@ -390,18 +497,18 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint3
 }
 
 // LUT entry for a 12-bit peek P (first stream bit = bit 11), one code per entry:
-//   bits 0..4   code length L (rank + 2; for the escape prefix n_ranked)
+//   bits 0..4   code length L (rank + 2; an escape n_ranked + 1)
 //   bits 5..6   zero (whole entries may be subtracted from the bit counter)
-//   bits 7..15  the code as a BF16 high part (s << 15 | exponent << 7)
-//   bit 16      kEsc
+//   bits 7..15  the code as a BF16 high part (s << 15 | exponent << 7); an escape gets
+//               exponent field 0, the placeholder that the escape list corrects
 // fp8 exponents e are stored as BF16 exponents e + 120 (exact for normal e4m3 values;
-// subnormals are corrected after assembly). A 12-bit peek holds any ranked code (at most
+// subnormals are corrected after assembly). A 12-bit peek holds any code (at most
 // n_ranked + 1 <= 12 bits), which is why at most 11 exponents are ranked.
 template <int ELEM>
 __device__ uint32_t lut_entry(uint32_t P, int nr, const uint8_t *rexp) {
     const uint32_t bits = P << 20;
     const int ones = __clz(~bits);
-    if (ones >= nr) return kEsc | (uint32_t)nr;
+    if (ones >= nr) return (((bits >> (31 - nr)) & 1u) << 15) | (uint32_t)(nr + 1);
     const uint32_t s = (bits >> (30 - ones)) & 1u, v = rexp[ones];
     return (s << 15) | ((ELEM == 0 ? v : v + 120u) << 7) | ((uint32_t)ones + 2);
 }
@@ -500,48 +607,22 @@ __device__ __forceinline__ uint32_t lut_at(const Fs32 &s, uint32_t lutb) {
     return e;
 }
 
-// Raw escape payload at the window: EB exponent bits (most significant first), then the sign;
-// returned as a BF16 high part (fp8: exponent + 120).
-template <int ELEM>
-__device__ __forceinline__ uint32_t raw_hi(Fs32 &s) {
-    constexpr int EB = ELEM == 0 ? 8 : 4;
-    const uint32_t v = s.wh >> (32 - EB);
-    const uint32_t sg = (s.wh >> (31 - EB)) & 1u;
-    fs_consume(s, EB + 1);
-    return (sg << 15) | ((ELEM == 0 ? v : v + 120u) << 7);
-}
-
 // fp8 only: an e4m3 subnormal (exponent field 0, stored as BF16 exponent 120) assembled as
 // +-2^-7 (1 + m/8) becomes +-m 2^-9 = (w -+ 2^-7) * 2, exactly.
 __device__ __forceinline__ float fp8_subnormal_fix(float w) {
     return (w - copysignf(0.0078125f, w)) * 2.0f;
 }
 
-// One row pair: two single-code lookups, BF16x2 assembly with the raw mantissas. Escapes are
-// rare; one branch re-decodes the pair from the state after the first lookup.
+// One row pair: two single-code lookups, BF16x2 assembly with the raw mantissas. No branch:
+// an escape yields its placeholder, corrected from the block's escape list.
 template <int ELEM>
 __device__ __forceinline__ void pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
-    fs_refill(s);  // a pair of ranked codes takes at most 24 bits; a refill leaves at least 33
+    fs_refill(s);  // two codes take at most 24 bits; a refill leaves at least 33
     const uint32_t e1 = lut_at(s, lutb);
     fs_consume(s, e1);
-    const Fs32 after1 = s;
     const uint32_t e2 = lut_at(s, lutb);
     fs_consume(s, e2);
-    uint32_t e = __byte_perm(e1, e2, 0x5410);
-    if ((e1 | e2) & kEsc) {
-        s = after1;
-        uint32_t hi1 = e1 & 0xFF80u;
-        if (e1 & kEsc) hi1 = raw_hi<ELEM>(s);
-        fs_refill(s);
-        const uint32_t f = lut_at(s, lutb);
-        fs_consume(s, f);
-        uint32_t hi2 = f & 0xFF80u;
-        if (f & kEsc) {
-            fs_refill(s);
-            hi2 = raw_hi<ELEM>(s);
-        }
-        e = hi1 | (hi2 << 16);
-    }
+    const uint32_t e = __byte_perm(e1, e2, 0x5410);
     uint32_t bf;
     if (ELEM == 0) bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
     else bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
@@ -553,11 +634,44 @@ __device__ __forceinline__ void pair_step(Fs32 &s, uint32_t lutb, uint32_t X, fl
     }
 }
 
-// Interior block from its staged region: 4 groups of 4 columns (16 row pairs each); the
-// group loop stays rolled so the hot loop fits the instruction cache.
+// Placeholder that the decoders produce for an escaped element with the given bits: its sign
+// and raw mantissa under exponent field 0, as BF16 (the fast path's assembly).
 template <int ELEM>
-__device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const uint32_t *lut, const uint8_t *rexp,
-                                           int nr, const uint16_t *xl, float (&acc)[8], bool &bad) {
+__device__ __forceinline__ float esc_placeholder(uint32_t bits) {
+    if (ELEM == 0) return __uint_as_float((bits & 0x807Fu) << 16);
+    return __uint_as_float((((bits & 0x80u) << 8) | ((bits & 7u) << 4)) << 16);
+}
+
+// Adds (w - placeholder) * x to acc[row] for every entry of a block's escape list (`slots`
+// words at `list`), the entries spread over the lanes; the transposed reduction then sums them
+// with the rows. xb = activations from the block's first column; rows, kc = the block's real
+// extent.
+template <int ELEM>
+__device__ __forceinline__ void esc_correct(const uint32_t *list, uint32_t slots, int lane, const uint16_t *xb,
+                                            int rows, int kc, float (&acc)[8], bool &bad) {
+    for (uint32_t j = (uint32_t)lane; j < slots; j += 32) {
+        const uint32_t e = list[j];
+        if (e == kEscPad) continue;
+        const uint32_t t = esc_t(e), bits = esc_bits(e);
+        const int r = (int)(t & 7u), c = (int)esc_lane(e) * kLaneCols + (int)(t >> 3);
+        if (r >= rows || c >= kc) {
+            bad = true;
+            continue;
+        }
+        const float xv = __uint_as_float((uint32_t)__ldg(xb + c) << 16);
+        const float w = ELEM == 0 ? __uint_as_float(bits << 16) : elem_value<1>(bits >> 7, (bits >> 3) & 15u, bits & 7u);
+        const float d = fmaf(w, xv, -(esc_placeholder<ELEM>(bits) * xv));
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            if (i == r) acc[i] += d;
+    }
+}
+
+// Interior block from its staged region (`bytes` long): 4 groups of 4 columns (16 row pairs
+// each); the group loop stays rolled so the hot loop fits the instruction cache.
+template <int ELEM>
+__device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
+                                           const uint16_t *xb, float (&acc)[8], bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
     constexpr int MWG = MW / 4;              // words per group of 4 columns
@@ -584,7 +698,7 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const u
         asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
     }
     const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
-    const uint2 *xp = reinterpret_cast<const uint2 *>(xl);
+    const uint2 *xp = reinterpret_cast<const uint2 *>(xb + lane * kLaneCols);
     uint2 xq = __ldg(xp);
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
@@ -612,19 +726,29 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, int lane, const u
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
     bad |= inserted - valid > 32u * lw;
+    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
+    esc_correct<ELEM>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0, lane,
+                      xb, kRows, kCols, acc, bad);
 }
 
+// Any block (edge, or a region too large to stage) from shared or global memory; escaped
+// elements contribute the same placeholder as on the fast path, which the list corrects (first,
+// so that the list's registers are free before the decode).
 template <int ELEM>
-__device__ __forceinline__ void block_generic(const uint8_t *reg, int lane, const uint8_t *rexp, int nr, int rows,
-                                              uint64_t k, uint64_t cb, const float (&x)[16], float (&acc)[8],
-                                              bool &bad) {
+__device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes, int lane, const uint8_t *rexp,
+                                              int nr, int rows, uint64_t k, uint64_t cb, const uint16_t *xb,
+                                              float (&acc)[8], bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     const int cols = real_cols(k, cb, lane);
-    LaneRegion lr = lane_region(reg, lane, rows, k, cb, F);
+    LaneRegion lr = lane_region(reg, bytes, lane, rows, k, cb, F);
+    const uint64_t kc = k - cb * kCols;
+    esc_correct<ELEM>(lr.esc, lr.slots, lane, xb, rows, kc < (uint64_t)kCols ? (int)kc : kCols, acc, bad);
+    const uint16_t *xl = xb + lane * kLaneCols;
     LaneStream ls;
     ls.init(lr.code, lr.nwords);
-    lane_generic<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm) {
-        acc[t & 7] = fmaf(elem_value<ELEM>(s, v, mm), x[t >> 3], acc[t & 7]);
+    lane_rolled<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int c, int r, uint32_t s, uint32_t v, uint32_t mm, bool esc) {
+        const float w = esc ? esc_placeholder<ELEM>(elem_bits<ELEM>(s, 0, mm)) : elem_value<ELEM>(s, v, mm);
+        acc[r] = fmaf(w, __uint_as_float((uint32_t)__ldg(xl + c) << 16), acc[r]);
     });
     bad |= ls.overrun();
 }
@@ -716,20 +840,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         }
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
-        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; r++) acc[r] = 0.0f;
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         if (interior && staged) {
-            block_fast<ELEM>(cur ? stage1 : stage0, lane, lut, rexp, m.nr, x + col0, acc, bad);
+            block_fast<ELEM>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, acc, bad);
         } else {
-            // activations of this lane's 16 columns, zero past K
-            float xv[16];
-            const int cols = real_cols(m.k, cb, lane);
-#pragma unroll
-            for (int c = 0; c < 16; c++) xv[c] = c < cols ? __uint_as_float((uint32_t)x[col0 + c] << 16) : 0.0f;
-            block_generic<ELEM>(reg, lane, rexp, m.nr, rows, m.k, cb, xv, acc, bad);
+            block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + cb * kCols, acc, bad);
         }
         const float sum = transpose_reduce(acc, lane);
         const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);

@@ -5,7 +5,10 @@
 // from the data section), fp32 row scales (fp8 only), then one region per 8x512 block in
 // row-block-major order: u8 lane_words[32] | 32 code streams (u32 words, most significant bit
 // first) | zero pad to 16 B | 32 mantissa regions (even-t half-stream in the low halves, odd-t
-// half-stream in the high halves, F-bit fields least significant bit first, 16-byte multiple).
+// half-stream in the high halves, F-bit fields least significant bit first, 16-byte multiple) |
+// escape list (u32 t | lane << 7 | element bits << 12 per escaped element, lanes in order, t
+// increasing, padded to 16 B with kEscPad). An escape code in a lane stream is n_ranked ones and
+// the sign; the escaped element's exponent (with the rest of its bits) is in the list.
 #pragma once
 #include <stdint.h>
 
@@ -18,10 +21,11 @@
 namespace nwcf {
 
 constexpr uint32_t kMagic = 0x3143574Eu;  // "NWC1"
-constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersion = 2;
 constexpr int kRows = 8, kCols = 512, kLanes = 32, kLaneCols = 16, kSyms = 128;
 constexpr int kMaxRanked = 11;
-constexpr int kMaxLaneWords = 80;  // 128 codes x (11 + 8 + 1) bits / 32
+constexpr int kMaxLaneWords = 48;  // 128 codes x 12 bits / 32
+constexpr uint32_t kEscPad = 0xFFFFFFFFu;
 constexpr uint64_t kHeaderBytes = 64, kRankOff = 64, kBlockTabOff = 80;
 
 // header field offsets
@@ -48,5 +52,11 @@ NWC_HD uint32_t man_words(int rows, int cols, int F) {
     uint32_t half_words = (uint32_t)cdiv((uint64_t)F * n_even, 16);
     return (uint32_t)(cdiv(half_words, 4) * 4);
 }
+
+// Escape-list entry fields.
+NWC_HD uint32_t esc_entry(uint32_t t, uint32_t lane, uint32_t bits) { return t | (lane << 7) | (bits << 12); }
+NWC_HD uint32_t esc_t(uint32_t e) { return e & 127u; }
+NWC_HD uint32_t esc_lane(uint32_t e) { return (e >> 7) & 31u; }
+NWC_HD uint32_t esc_bits(uint32_t e) { return e >> 12; }
 
 }  // namespace nwcf

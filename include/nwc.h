@@ -6,7 +6,9 @@
  *   "NWC -- Neural Weight Compression" (PyPI project page, v0.9.0), section "How it works":
  *     a BF16 weight splits into a raw mantissa plane and an entropy-coded exponent/sign part;
  *     the exponent is ranked by frequency and written as a unary rank code plus a raw sign
- *     bit, with an escape for rare values; lanes decode their own bit streams over blocks of
+ *     bit, with an escape for rare values (in this format the escape code is n_ranked ones
+ *     and the sign, and the escaped element's bits sit in a per-block escape list after the
+ *     mantissa regions); lanes decode their own bit streams over blocks of
  *     8 rows x 512 columns inside the matrix-vector kernel; dequantization and the embedding
  *     lookup run on the same decoder; any shape works (2 bits per filler, no mantissa).
  *   "Qwen3-4B-NWC-fp8" (model card): weight-only e4m3 with a symmetric per-output-channel
@@ -18,7 +20,8 @@
  *     by the caller; the library allocates no device or pinned memory, ever.
  *   - GPU calls are asynchronous on the given stream (NULL = the legacy default stream).
  *     A launch failure returns NWC_ERR_CUDA. Data errors found on the device (a lane
- *     stream that runs past its words, a gather id out of range) do not fault: the kernel
+ *     stream that runs past its words, an escape list that does not match the stream's
+ *     escape codes, a gather id out of range) do not fault: the kernel
  *     skips the bad access, writes zeros and raises the device error word, which
  *     nwc_check() reads and clears.
  *   - Matrices are row-major: element (n, k) of an N x K matrix is at index n*ld + k.
@@ -77,7 +80,7 @@ typedef struct nwc_matrix {
 /* Human-readable name of a status code (static string). */
 const char *nwc_status_str(nwc_status s);
 
-/* Library version string, e.g. "nwc 1 (format 1, sm_103a)". */
+/* Library version string, e.g. "nwc 2 (format 2, sm_103a)". */
 const char *nwc_version(void);
 
 /*
@@ -111,8 +114,10 @@ nwc_status nwc_quantize_fp8(const uint16_t *w, int64_t n, int64_t k, int64_t ld,
                             int64_t ldq, float *scales);
 
 /*
- * nwc_validate -- host check of a blob: header, rank table, block table, and every block
- * region's size against its lane word counts and real-element counts. NWC_ERR_FORMAT if any
+ * nwc_validate -- host check of a blob: header, rank table, block table, every block
+ * region's size against its lane word counts and real-element counts, and every escape list
+ * (entries name real elements with unranked exponents, in lane-then-t order, then at most
+ * three padding words). NWC_ERR_FORMAT if any
  * check fails. Stream contents are checked by the kernels while decoding.
  */
 nwc_status nwc_validate(const void *blob_host, size_t bytes);

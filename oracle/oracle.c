@@ -21,7 +21,7 @@
  *
  * FORMAT (little-endian):
  *   header, 64 bytes
- *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 1
+ *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 2
  *     6  u8  elem (0 = BF16, 1 = FP8 e4m3)  7  u8  n_ranked (1..11)
  *     8  u64 N    16 u64 K    24 u64 n_blocks = ceil(N/8) * ceil(K/512)
  *     32 u64 off_blocks   40 u64 off_scales (0 for BF16)   48 u64 off_data
@@ -33,7 +33,10 @@
  *   off_data: block regions, row-block-major (b = rb * CB + cb)
  *   block region: u8 lane_words[32]; then the 32 lane code streams (lane 0 first),
  *     each a whole number of u32 words; zero padding to 16 bytes; then the 32 lane
- *     mantissa regions (lane 0 first), each a multiple of 16 bytes.
+ *     mantissa regions (lane 0 first), each a multiple of 16 bytes; then the block's
+ *     escape list: one u32 per escaped element, t | lane << 7 | value << 12 (value =
+ *     the element's full bit pattern), lanes in order and t increasing within a lane,
+ *     padded to 16 bytes with 0xFFFFFFFF.
  *
  *   Fields of one element (READING: BF16 splits into a raw 7-bit mantissa and a
  *   coded 8-bit exponent with a raw sign; fp8 likewise with 4-bit exponent, 3-bit
@@ -45,8 +48,10 @@
  *     ranked code with its sign fits a 12-bit peek.)
  *   Code of one element, bits appended in order:
  *     ranked (rank p < n_ranked): p one-bits, one zero-bit, the sign bit;
- *     escape (v unranked): n_ranked one-bits, v as 8 (BF16) / 4 (FP8) bits most
- *     significant first, the sign bit.
+ *     escape (v unranked): n_ranked one-bits, the sign bit; the element's exponent
+ *     bits (8 BF16 / 4 fp8, with the rest of the element) are in the block's escape
+ *     list. (READING: "escape for rare values" with the raw exponent kept outside the
+ *     lane stream, so that every in-stream code is at most 12 bits.)
  *     filler (row >= N or col >= K): the rank-0 code with sign 0, i.e. two zero
  *     bits, and no mantissa.
  *   Lane stream of block (rb, cb), lane l: elements t = 8c + r, c = 0..15,
@@ -75,7 +80,7 @@
 #include <string.h>
 
 #define ORC_MAGIC 0x3143574Eu
-#define ORC_VERSION 1
+#define ORC_VERSION 2
 #define ORC_R 11
 #define ORC_ROWS 8
 #define ORC_COLS 512
@@ -197,6 +202,8 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
         uint64_t rb = b / CB, cb = b % CB;
         static bitw code[ORC_LANES];
         static halfw even[ORC_LANES], odd[ORC_LANES];
+        static uint32_t esc[ORC_LANES * ORC_SYMS];
+        uint64_t n_esc = 0;
         memset(code, 0, sizeof(code));
         memset(even, 0, sizeof(even));
         memset(odd, 0, sizeof(odd));
@@ -218,7 +225,7 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
                     bw_put(&code[l], 0);
                 } else {
                     for (int i = 0; i < nr; i++) bw_put(&code[l], 1);
-                    for (int i = exp_bits(elem) - 1; i >= 0; i--) bw_put(&code[l], (v >> i) & 1);
+                    esc[n_esc++] = (uint32_t)t | ((uint32_t)l << 7) | ((uint32_t)e[row * K + col] << 12);
                 }
                 bw_put(&code[l], s);
                 if (t % 2 == 0) hw_put_field(&even[l], m, F);
@@ -233,6 +240,8 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
         }
         uint64_t len = pad16(32 + 4 * code_words);
         for (int l = 0; l < ORC_LANES; l++) len += 4 * man_words[l];
+        uint64_t esc_at = len;
+        len += pad16(4 * n_esc);
         uint8_t *r = (uint8_t *)calloc(len, 1);
         if (!r) return -2;
         uint64_t pos = 32;
@@ -246,6 +255,8 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
             for (uint64_t k = 0; k < man_words[l]; k++, pos += 4)
                 put_u32(r + pos, (uint32_t)even[l].h[k] | ((uint32_t)odd[l].h[k] << 16));
         }
+        for (uint64_t i = 0; esc_at + 4 * i < len; i++)
+            put_u32(r + esc_at + 4 * i, i < n_esc ? esc[i] : 0xFFFFFFFFu);
         reg[b] = r;
         reg_len[b] = len;
     }
@@ -358,10 +369,34 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
     pos = pad16(pos);
     int F = man_bits(h->elem);
     int ok = 0;
+    /* the mantissa regions' sizes follow from the real extents; the escape list follows them */
+    uint64_t man_at = pos, esc_at = pos;
+    for (int l = 0; l < ORC_LANES; l++) {
+        uint64_t n_even = 0, n_odd = 0;
+        for (int t = 0; t < ORC_SYMS; t++) {
+            uint64_t row, col;
+            position(rb, cb, l, t, &row, &col);
+            if (row < h->N && col < h->K) { if (t % 2 == 0) n_even++; else n_odd++; }
+        }
+        uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
+        esc_at += 4 * (ceil_div(ceil_div(bits, 16), 4) * 4);
+    }
+    if (start + esc_at > end) return -1;
+    static uint32_t esc_value[ORC_LANES][ORC_SYMS];
+    static int esc_seen[ORC_LANES][ORC_SYMS];
+    memset(esc_seen, 0, sizeof(esc_seen));
+    for (uint64_t at = esc_at; start + at + 4 <= end; at += 4) {
+        uint32_t ent = get_u32(reg + at);
+        if (ent == 0xFFFFFFFFu) continue;
+        int t = (int)(ent & 127u), l = (int)((ent >> 7) & 31u);
+        esc_value[l][t] = ent >> 12;
+        esc_seen[l][t] = 1;
+    }
+    pos = man_at;
     for (int l = 0; l < ORC_LANES; l++) {
         bitr br = {lane_code[l], reg[l], 0, 0};
         uint32_t sv[ORC_SYMS], vv[ORC_SYMS];
-        int real[ORC_SYMS];
+        int real[ORC_SYMS], escaped[ORC_SYMS];
         uint64_t n_even = 0, n_odd = 0;
         for (int t = 0; t < ORC_SYMS; t++) {
             uint64_t row, col;
@@ -369,27 +404,25 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
             real[t] = row < h->N && col < h->K;
             int ones = 0;
             while (ones < h->nr && br_get(&br) == 1) ones++;
-            uint32_t v;
-            if (ones < h->nr) {
-                v = h->rank_exp[ones];
-            } else {
-                v = 0;
-                for (int i = 0; i < exp_bits(h->elem); i++) v = (v << 1) | br_get(&br);
-            }
+            escaped[t] = ones >= h->nr;
+            vv[t] = escaped[t] ? 0 : h->rank_exp[ones];
             sv[t] = br_get(&br);
-            vv[t] = v;
             if (real[t]) { if (t % 2 == 0) n_even++; else n_odd++; }
         }
         if (br.bad) ok = -1;
         uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
         uint64_t words = ceil_div(ceil_div(bits, 16), 4) * 4;
-        if (start + pos + 4 * words > end) return -1;
         const uint8_t *man = reg + pos;
         uint64_t je = 0, jo = 0;
         for (int t = 0; t < ORC_SYMS; t++) {
             if (!real[t]) continue;
             uint32_t m = (t % 2 == 0) ? half_field(man, 0, je++, F) : half_field(man, 1, jo++, F);
-            tile[t % ORC_ROWS][l * ORC_LANE_COLS + t / ORC_ROWS] = (uint16_t)join(h->elem, sv[t], vv[t], m);
+            uint32_t value = join(h->elem, sv[t], vv[t], m);
+            if (escaped[t]) {
+                if (!esc_seen[l][t]) return -1;
+                value = esc_value[l][t];
+            }
+            tile[t % ORC_ROWS][l * ORC_LANE_COLS + t / ORC_ROWS] = (uint16_t)value;
         }
         pos += 4 * words;
     }

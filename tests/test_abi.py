@@ -59,22 +59,72 @@ def test_bind_geometry_and_workspace():
     assert bind_host(blob, dev_ptr=0x10008)[0] == 1  # misaligned device pointer
 
 
+def _esc_list(blob, i, n, k):
+    """(byte offset, u32 words) of the escape list of block i (BF16, n x k matrix, one
+    column block): after the code streams and the closed-form mantissa regions."""
+    b = np.frombuffer(bytes(blob), np.uint8)
+    nb = int(b[24:32].view(np.uint64)[0])
+    off_data = int(b[48:56].view(np.uint64)[0])
+    tab = b[80:80 + 4 * (nb + 1)].view(np.uint32)
+    start, end = off_data + 16 * int(tab[i]), off_data + 16 * int(tab[i + 1])
+    at = start + -(-(32 + 4 * int(b[start:start + 32].astype(np.int64).sum())) // 16) * 16
+    rows = min(8, n - 8 * i)
+    for lane in range(32):
+        cols = max(0, min(16, k - 16 * lane))
+        at += 4 * (-(-(-(-7 * cols * ((rows + 1) // 2) // 16)) // 4) * 4)
+    return at, b[at:end].view(np.uint32)
+
+
 def test_validate_rejects_corruption():
-    w = synth.normal_bf16((20, 1030), 0.02, seed=4)
+    # exponents 120..127 only: at most 8 distinct values, so no escapes and an empty list
+    rng = np.random.default_rng(4)
+    w = ((rng.integers(120, 128, (20, 1030)) << 7) | rng.integers(0, 128, (20, 1030))).astype(np.uint16)
     blob = bytearray(nwc.encode(w))
     assert nwc.validate(bytes(blob)) == 0
-    def bad(mut):
-        b = bytearray(blob)
+    def bad(mut, base=blob):
+        b = bytearray(base)
         mut(b)
         return nwc.validate(bytes(b))
     assert bad(lambda b: b.__setitem__(0, 0)) == 2           # magic
+    assert bad(lambda b: b.__setitem__(4, 1)) == 2           # format version
     assert bad(lambda b: b.__setitem__(7, 12)) == 2          # n_ranked > 11
     assert bad(lambda b: b.__setitem__(64 + 1, b[64])) == 2  # duplicate ranked exponent
     assert nwc.validate(bytes(blob[:-16])) == 2              # truncated
     off_data = int(np.frombuffer(bytes(blob[48:56]), np.uint64)[0])
     assert bad(lambda b: b.__setitem__(off_data, b[off_data] + 4)) == 2  # lane word count (beyond padding)
-    assert bad(lambda b: b.__setitem__(off_data + 3, 200)) == 2           # > 80 words
+    assert bad(lambda b: b.__setitem__(off_data + 3, 200)) == 2           # > 48 words
     assert nwc.validate(bytes(blob) + b"\0" * 16) == 2       # trailing bytes
+
+
+def test_validate_checks_escape_lists():
+    w = synth.small_matrix_with_outliers(seed=0)  # 64 x 512, one block, escapes present
+    blob = bytearray(nwc.encode(w))
+    assert nwc.validate(bytes(blob)) == 0
+    at, words = _esc_list(blob, 0, 64, 512)
+    entries = [i for i in range(len(words)) if words[i] != 0xFFFFFFFF]
+    assert len(entries) >= 2 and entries == list(range(len(entries)))
+    n_pad = len(words) - len(entries)
+    assert n_pad <= 3
+    def with_word(off, value, base=blob):
+        b = bytearray(base)
+        b[off:off + 4] = int(value).to_bytes(4, "little")
+        return nwc.validate(bytes(b))
+    e0 = int(words[0])
+    assert with_word(at, e0 | 0xFFF) == 2                      # lane 31, t 127: out of order
+    assert with_word(at, 0xFFFFFFFF) == 2                      # padding before an entry
+    ranked_exp = blob[64]
+    assert with_word(at, (e0 & 0xFFF) | (ranked_exp << 7) << 12) == 2  # ranked exponent listed
+    assert with_word(at, (e0 & 0xFFF) | (1 << 16) << 12) == 2          # bits wider than BF16
+    assert with_word(at + 4, e0) == 2                          # repeated entry
+    if n_pad > 0:  # an entry after the last one that is out of order
+        assert with_word(at + 4 * len(entries), e0) == 2
+    # a ragged block: an entry moved onto a filler position (row 5 of a 5-row block)
+    blob2 = bytearray(nwc.encode(w[:5, :300]))
+    at, words = _esc_list(blob2, 0, 5, 300)
+    assert nwc.validate(bytes(blob2)) == 0 and words[0] != 0xFFFFFFFF
+    assert with_word(at, (int(words[0]) & ~0x7) | 5, blob2) == 2
+    # a column past K = 300 (lane 18, c 12 would be column 300)
+    assert with_word(at, (int(words[0]) & ~0xFFF) | (18 << 7) | (12 << 3), blob2) == 2
 
 
 def test_encode_argument_errors():

@@ -109,6 +109,48 @@ def test_gemv_special_values():
     gemv_check(nwc.encode(w), x)
 
 
+def test_gemv_escape_heavy_staged_blocks():
+    """About 3% of the elements get exponents far from the bulk (escaped): the regions
+    still fit the shared-memory stage, so the fast path's placeholder products and the
+    escape-list corrections carry them."""
+    rng = np.random.default_rng(23)
+    w = synth.normal_bf16((256, 4096), 0.02, seed=23)
+    hit = rng.random(w.shape) < 0.03
+    odd = (rng.integers(0, 2, w.shape) << 15) | (rng.integers(100, 150, w.shape) << 7) | rng.integers(0, 128, w.shape)
+    w = np.where(hit, odd, w).astype(np.uint16)
+    blob = nwc.encode(w)
+    assert blob == oracle.encode(w)
+    mat = nwc.Matrix(blob)
+    assert np.array_equal(mat.decode().cpu().numpy().view(np.uint16), w)
+    assert_clean()
+    gemv_check(blob, synth.activations_bf16(4096, 24), mat=mat)
+
+
+def test_escape_list_mismatch_is_flagged_not_faulted():
+    """An escape list one entry short (still a valid list on the host) leaves a lane
+    stream's escape without its entry: decode and the check word report it."""
+    w = synth.small_matrix_with_outliers(seed=0)  # 64 x 512: 8 full blocks
+    blob = bytearray(nwc.encode(w))
+    b = np.frombuffer(bytes(blob), np.uint8)
+    off_data = int(b[48:56].view(np.uint64)[0])
+    tab = b[80:80 + 4 * 9].view(np.uint32)
+    for i in range(8):
+        start, end = off_data + 16 * int(tab[i]), off_data + 16 * int(tab[i + 1])
+        # escape list: after the code streams and 32 full mantissa regions of 28 words
+        at = start + -(-(32 + 4 * int(b[start:start + 32].astype(np.int64).sum())) // 16) * 16 + 32 * 28 * 4
+        words = b[at:end].view(np.uint32)
+        n_entries = int((words != 0xFFFFFFFF).sum())
+        if n_entries >= 1 and len(words) - n_entries < 3:
+            blob[at + 4 * (n_entries - 1):at + 4 * n_entries] = b"\xff\xff\xff\xff"
+            break
+    else:
+        pytest.skip("no block with room for one more padding word")
+    assert nwc.validate(bytes(blob)) == 0
+    nwc.Matrix(bytes(blob)).decode()
+    st, flags = nwc.check()
+    assert st == 5 and flags & 1
+
+
 def test_gemv_repeat_graph_and_stream():
     w = synth.normal_bf16((520, 2600), 0.03, seed=31)
     x = synth.activations_bf16(2600, 32)

@@ -50,11 +50,12 @@ def ranks_of(values, nvals):
 
 def code_bits_per_lane(v, nvals, exp_bits):
     """Closed-form lane stream lengths: rank+2 bits per ranked element,
-    n_ranked + exp_bits + 1 per escaped one, 2 per filler. Returns (RB*CB, 32)."""
+    n_ranked + 1 per escaped one (its exponent lives in the escape list), 2 per
+    filler. Returns (RB*CB, 32)."""
     n, k = v.shape
     ranked = ranks_of(v, nvals)
     nr = len(ranked)
-    length = np.full(nvals, nr + exp_bits + 1, np.int64)
+    length = np.full(nvals, nr + 1, np.int64)
     for p, e in enumerate(ranked):
         length[e] = p + 2
     rb, cb = -(-n // 8), -(-k // 512)
@@ -173,6 +174,60 @@ def test_outlier_matrix_escapes_and_zeros():
     assert np.array_equal(back, w)
     bits, _ = code_bits_per_lane(e, 256, 8)
     assert np.array_equal(lane_words(blob), -(-bits // 32))
+
+
+def escape_lists(blob, elem_bits_F):
+    """Per block, the escape-list entries read straight from the blob: the
+    region's tail after the code streams and the closed-form mantissa regions."""
+    h = hdr(blob)
+    b = np.frombuffer(blob, np.uint8)
+    tab = b[h["off_blocks"]:h["off_blocks"] + 4 * (h["nb"] + 1)].view(np.uint32)
+    N, K = h["N"], h["K"]
+    cb_n = -(-K // 512)
+    out = []
+    for i in range(h["nb"]):
+        start, end = h["off_data"] + 16 * int(tab[i]), h["off_data"] + 16 * int(tab[i + 1])
+        lw = b[start:start + 32].astype(np.int64)
+        at = start + -(-(32 + 4 * int(lw.sum())) // 16) * 16
+        rb, cb = divmod(i, cb_n)
+        rows = min(8, N - 8 * rb)
+        for lane in range(32):
+            cols = int(np.clip(K - 512 * cb - 16 * lane, 0, 16))
+            n_even = cols * ((rows + 1) // 2)
+            words = -(-(-(-elem_bits_F * n_even // 16)) // 4) * 4
+            at += 4 * words
+        ent = b[at:end].view(np.uint32)
+        out.append([int(e) for e in ent if e != 0xFFFFFFFF])
+        assert all(e == 0xFFFFFFFF for e in ent[len(out[-1]):]), "padding must follow the entries"
+    return out
+
+
+def test_escape_list_holds_every_unranked_element_in_lane_t_order():
+    """Each escaped element appears once, as t | lane << 7 | bits << 12, lanes in
+    order and t increasing; no ranked element appears."""
+    for w, elem, F, nvals, ebits in [
+        (synth.small_matrix_with_outliers(seed=0), oracle.BF16, 7, 256, 8),
+        (np.random.default_rng(3).permutation(np.arange(65536, dtype=np.uint32)).astype(np.uint16)
+         .reshape(128, 512)[:13, :700 - 188], oracle.BF16, 7, 256, 8),
+    ]:
+        e = (w.astype(np.int64) >> 7) & 0xFF
+        ranked = ranks_of(e, nvals)
+        blob = oracle.encode(w)
+        lists = escape_lists(blob, F)
+        n, k = w.shape
+        cb_n = -(-k // 512)
+        total = 0
+        for i, ent in enumerate(lists):
+            rb, cb = divmod(i, cb_n)
+            want = []
+            for lane in range(32):
+                for t in range(128):
+                    r, c = 8 * rb + t % 8, 512 * cb + 16 * lane + t // 8
+                    if r < n and c < k and e[r, c] not in ranked:
+                        want.append(t | lane << 7 | int(w[r, c]) << 12)
+            assert ent == want
+            total += len(ent)
+        assert total == int((~np.isin(e, ranked)).sum()) > 0
 
 
 def test_encoding_is_deterministic():
