@@ -151,8 +151,8 @@ class Matrix:
     """A blob resident in device memory and bound through nwc_bind.
 
     ``device_blob`` is a torch uint8 CUDA tensor holding the blob (caller-visible so that
-    benchmarks can keep several copies); the GEMV workspace is allocated once, zeroed, and
-    reused by every call (prepared once here: decode table built, counters zeroed).
+    benchmarks can keep several copies); the GEMV workspace is allocated once, its counters
+    zeroed by nwc_gemv_prepare, and reused by every call.
     """
 
     def __init__(self, blob: bytes, device="cuda", device_blob=None):

@@ -291,7 +291,7 @@ nwc_status encode_impl(const Src<E> &src, int elem, const float *scales, int thr
         uint32_t u = (uint32_t)(off[i] / 16);
         std::memcpy(b + off_blocks + 4 * i, &u, 4);
     }
-    if (elem == 1) std::memcpy(b + off_scales, scales, 4 * src.n);
+    if (elem == 1 && scales) std::memcpy(b + off_scales, scales, 4 * src.n);
     // Regions are written at 16-byte aligned offsets into a 16-byte aligned scratch when the
     // caller's buffer is not aligned; otherwise in place.
     const bool aligned = (reinterpret_cast<uintptr_t>(b + off_data) % 16) == 0;

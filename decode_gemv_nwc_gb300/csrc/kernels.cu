@@ -456,8 +456,7 @@ constexpr int kStageBytes = 6144;
 constexpr int kLutEntries = 4096;
 constexpr int kLutBytes = kLutEntries * 4;
 constexpr int kRexpOff = kLutBytes;
-constexpr int kLutBarOff = kRexpOff + 16;
-constexpr int kBarOff = kLutBarOff + 8;
+constexpr int kBarOff = kRexpOff + 16;
 constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
 constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes;
 static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
@@ -505,22 +504,25 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint3
 // subnormals are corrected after assembly). A 12-bit peek holds any code (at most
 // n_ranked + 1 <= 12 bits), which is why at most 11 exponents are ranked.
 template <int ELEM>
-__device__ uint32_t lut_entry(uint32_t P, int nr, const uint8_t *rexp) {
+__device__ __forceinline__ uint32_t lut_entry(uint32_t P, int nr, const uint32_t (&rank4)[3]) {
     const uint32_t bits = P << 20;
     const int ones = __clz(~bits);
     if (ones >= nr) return (((bits >> (31 - nr)) & 1u) << 15) | (uint32_t)(nr + 1);
-    const uint32_t s = (bits >> (30 - ones)) & 1u, v = rexp[ones];
+    const uint32_t word = ones < 4 ? rank4[0] : (ones < 8 ? rank4[1] : rank4[2]);
+    const uint32_t s = (bits >> (30 - ones)) & 1u, v = (word >> (8 * (ones & 3))) & 0xFFu;
     return (s << 15) | ((ELEM == 0 ? v : v + 120u) << 7) | ((uint32_t)ones + 2);
 }
 
+// Builds the 4096-entry table in shared memory with all threads of the CTA; the rank table is
+// read from the kernel parameter with static offsets only (packed four values per word).
 template <int ELEM>
-__global__ void __launch_bounds__(256) lut_kernel(Mat m, uint32_t *lut, uint32_t *counters, uint64_t n_counters) {
-    __shared__ uint8_t rexp[16];
-    load_rank_table(m, rexp);
-    __syncthreads();
-    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < (uint32_t)kLutEntries) lut[i] = lut_entry<ELEM>(i, m.nr, rexp);
-    for (uint64_t c = i; c < n_counters; c += (uint64_t)gridDim.x * blockDim.x) counters[c] = 0;
+__device__ __forceinline__ void build_lut(const Mat &m, uint32_t *lut) {
+    uint32_t rank4[3];
+#pragma unroll
+    for (int i = 0; i < 3; i++)
+        rank4[i] = (uint32_t)m.rank_exp[4 * i] | (uint32_t)m.rank_exp[4 * i + 1] << 8 |
+                   (uint32_t)m.rank_exp[4 * i + 2] << 16 | (uint32_t)m.rank_exp[4 * i + 3] << 24;
+    for (uint32_t i = threadIdx.x; i < (uint32_t)kLutEntries; i += blockDim.x) lut[i] = lut_entry<ELEM>(i, m.nr, rank4);
 }
 
 // Pair q's two mantissas (even t at bits 0.., odd t at bits 16..) from a group's words.
@@ -755,31 +757,22 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes
 
 template <int ELEM>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1)
-    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, const uint32_t *lut_g,
-                float *partial, uint32_t *counters, uint64_t n_pad) {
+    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, float *partial, uint32_t *counters,
+                uint64_t n_pad) {
+    // A kernel launched after this one with programmatic stream serialization may start as soon
+    // as SMs free up; it waits (griddepcontrol.wait) before touching anything this one writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint8_t *rexp = smem + kRexpOff;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t lut_bar = smem_u32(smem + kLutBarOff);
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16), bar1 = bar0 + 8;
     uint8_t *stage0 = smem + kStageOff + warp * kStagesPerWarp * kStageBytes,
             *stage1 = stage0 + (kStagesPerWarp - 1) * kStageBytes;
-    load_rank_table(m, rexp);
-    if (threadIdx.x == 0) mbar_init(lut_bar);
-    if (lane == 0) {
-        mbar_init(bar0);
-        mbar_init(bar1);
-    }
-    if (threadIdx.x == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        mbar_expect_tx(lut_bar, kLutBytes);
-        tma_load_1d(smem_u32(lut), lut_g, kLutBytes, lut_bar);
-    }
 
+    // Block b goes to CTA b % grid, so every SM gets within one block of the same count.
     const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
-    uint64_t b = (uint64_t)blockIdx.x * kGemvWarps + warp;
+    uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
     uint32_t phase = 0;  // bit i: parity of the next completion of stage i
     bool bad = false, timed_out = false;
 
@@ -807,10 +800,22 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         }
     };
 
+    // The warp's own barriers and first region copy go first, so that the copy is in flight
+    // while the CTA builds the decode table.
+    if (lane == 0) {
+        mbar_init(bar0);
+        mbar_init(bar1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
     if (b < m.nb) issue(b, 0);
-    const bool lut_ok = mbar_wait(lut_bar, 0);
-    if (!lut_ok) timed_out = true;
-    for (int it = 0; lut_ok && b < m.nb; it++) {
+    load_rank_table(m, rexp);
+    build_lut<ELEM>(m, lut);
+    __syncthreads();
+    // Up to here only the matrix and the kernel parameters were read. x, the workspace and y may
+    // belong to the kernel before this one on the stream: wait for it to complete.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int it = 0; b < m.nb; it++) {
         const int cur = kStagesPerWarp == 2 ? (it & 1) : 0;
         const uint64_t nxt = b + total_warps;
         __syncwarp();
@@ -866,12 +871,15 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
             if (ticket == (uint32_t)m.cbs - 1) {
                 asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                if (lane < kRows && rb * kRows + (uint64_t)lane < m.n) {
-                    const uint64_t r2 = rb * kRows + (uint64_t)lane;
-                    float s = 0.0f;
-                    for (uint64_t c2 = 0; c2 < m.cbs; c2++) s += __ldcg(partial + c2 * n_pad + r2);
-                    y[r2] = ELEM == 0 ? s : s * m.scales[r2];
-                }
+                // row lane % 8; lane / 8 sums column blocks lane / 8, + 4, ... (loads in
+                // parallel across the warp), then a fixed shuffle order adds the four
+                const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
+                float s = 0.0f;
+                if (r2 < m.n)
+                    for (uint64_t c2 = (uint64_t)(lane >> 3); c2 < m.cbs; c2 += 4) s += __ldcg(partial + c2 * n_pad + r2);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
+                if (lane < kRows && r2 < m.n) y[r2] = ELEM == 0 ? s : s * m.scales[r2];
                 if (lane == 0) counters[rb] = 0;
             }
         }
@@ -886,7 +894,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         // let this warp's own copies land before the CTA's shared memory goes away
         mbar_wait(bar0, phase & 1u);
         if (kStagesPerWarp == 2) mbar_wait(bar1, (phase >> 1) & 1u);
-        if (threadIdx.x == 0) mbar_wait(lut_bar, 0);
     }
     if (bad) raise_error(kErrFormat);
 }
@@ -954,10 +961,9 @@ extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64
 }
 
 namespace {
-// Workspace: [LUT 16 KB][partials fp32 col_blocks x n_pad][counters u32 row_blocks]
-uint64_t ws_partial_off() { return kLutBytes; }
+// Workspace: [partials fp32 col_blocks x n_pad][counters u32 row_blocks]; both only when K > 512.
 uint64_t ws_counter_off(const nwc_matrix &m) {
-    return m.col_blocks > 1 ? kLutBytes + 4 * (uint64_t)m.col_blocks * pad_rows(m) : kLutBytes;
+    return m.col_blocks > 1 ? 4 * (uint64_t)m.col_blocks * pad_rows(m) : 0;
 }
 }  // namespace
 
@@ -965,21 +971,16 @@ extern "C" size_t nwc_gemv_workspace_bytes(const nwc_matrix *mp) {
     if (!mp) return 0;
     uint64_t b = ws_counter_off(*mp);
     if (mp->col_blocks > 1) b += 4 * (uint64_t)mp->row_blocks;
-    return (size_t)up16(b);
+    return (size_t)up16(b < 16 ? 16 : b);
 }
 
 extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws_bytes, nwc_stream stream) {
     if (!mp || !ws || ws_bytes < nwc_gemv_workspace_bytes(mp) || (reinterpret_cast<uintptr_t>(ws) & 15))
         return NWC_ERR_INVALID_ARG;
-    const Mat m = to_mat(*mp);
-    uint32_t *lut = static_cast<uint32_t *>(ws);
-    const uint64_t n_counters = mp->col_blocks > 1 ? (uint64_t)mp->row_blocks : 0;
-    uint32_t *counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + ws_counter_off(*mp));
+    if (mp->col_blocks <= 1) return NWC_OK;
+    uint8_t *counters = static_cast<uint8_t *>(ws) + ws_counter_off(*mp);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = kLutEntries / 256;
-    if (m.elem == NWC_ELEM_BF16) lut_kernel<0><<<grid, 256, 0, s>>>(m, lut, counters, n_counters);
-    else lut_kernel<1><<<grid, 256, 0, s>>>(m, lut, counters, n_counters);
-    return launched();
+    return cudaMemsetAsync(counters, 0, 4 * (size_t)mp->row_blocks, s) == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 
 extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
@@ -997,21 +998,29 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     if (!smem_ok[m.elem]) return NWC_ERR_CUDA;
     const uint64_t n_pad = pad_rows(*mp);
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    const uint32_t *lut = reinterpret_cast<const uint32_t *>(w8);
-    float *partial = reinterpret_cast<float *>(w8 + ws_partial_off());
+    float *partial = reinterpret_cast<float *>(w8);
     uint32_t *counters = reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp));
-    const uint64_t want = (m.nb + kGemvWarps - 1) / kGemvWarps;
-    const int grid = (int)(want < (uint64_t)sms ? want : (uint64_t)sms);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (m.elem == NWC_ELEM_BF16)
-        gemv_kernel<0><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, lut, partial, counters, n_pad);
-    else
-        gemv_kernel<1><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, x, y, lut, partial, counters, n_pad);
-    return launched();
+    const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
+    // Programmatic dependent launch: the kernel may start while the previous kernel on the stream
+    // finishes; it streams its first block regions and builds its decode table meanwhile.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kGemvWarps * 32);
+    cfg.dynamicSmemBytes = kGemvSmem;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t rc = m.elem == NWC_ELEM_BF16
+                         ? cudaLaunchKernelEx(&cfg, gemv_kernel<0>, m, x, y, partial, counters, n_pad)
+                         : cudaLaunchKernelEx(&cfg, gemv_kernel<1>, m, x, y, partial, counters, n_pad);
+    return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- allocation-free GEMV
-// Scratch of nwc_gemv_noalloc: the decode table, partial sums and counters of one call live in
+// Scratch of nwc_gemv_noalloc: the partial sums and counters of one call live in
 // this file-scope array, which every GPU that loads the library holds until the process exits.
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -1041,8 +1050,8 @@ extern "C" nwc_status nwc_gemv_noalloc(const nwc_matrix *mp, const uint16_t *x, 
         }
         ptr = g_noalloc_ptr[dev];
     }
-    // The array keeps whatever the previous call left: rebuild the decode table and zero the
-    // counters for this matrix, then run the GEMV on the same stream.
+    // The array keeps whatever the previous call left: zero the counters for this matrix, then
+    // run the GEMV on the same stream.
     nwc_status st = nwc_gemv_prepare(mp, ptr, kNoAllocScratchBytes, stream);
     if (st != NWC_OK) return st;
     return nwc_gemv(mp, x, y, ptr, kNoAllocScratchBytes, stream);

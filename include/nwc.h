@@ -138,16 +138,16 @@ nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *sca
                       nwc_stream stream);
 
 /*
- * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 KB): the 4096-entry
- * decode table of this matrix's rank table (built once by nwc_gemv_prepare), FP32 partial sums
- * per (row, 512-column block) and one counter per 8-row block (both only when K > 512).
+ * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 bytes): FP32
+ * partial sums per (row, 512-column block) and one counter per 8-row block (both only when
+ * K > 512). The 4096-entry decode table ("A 12-bit peek into a 16 KB lookup table in shared
+ * memory") is built by every CTA in its own shared memory and needs no workspace.
  */
 size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
 
 /*
- * nwc_gemv_prepare -- fills a workspace for m: builds the decode table ("A 12-bit peek into a
- * 16 KB lookup table in shared memory", here kept in the workspace and copied to shared memory
- * by each CTA) and zeroes the counters. Call once per workspace before its first nwc_gemv; every
+ * nwc_gemv_prepare -- readies a workspace for m: zeroes its counters (asynchronously on the
+ * stream). Call once per workspace before its first nwc_gemv; every
  * nwc_gemv leaves the counters at zero again, so the workspace serves repeated calls and CUDA-
  * graph replays. ws is 16-byte aligned, ws_bytes >= nwc_gemv_workspace_bytes(m). Calls sharing
  * one workspace must not overlap on the GPU.
@@ -169,10 +169,10 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
  * counterpart; it exists for hosts where device memory belongs to someone else (for example a
  * plugin inside an inference server whose allocator owns the whole device, or a real-time loop
  * where an allocation's implicit device synchronization is not acceptable).
- * The scratch (decode table, partial sums, counters) is a file-scope 4 MiB device array inside
+ * The scratch (partial sums, counters) is a file-scope 4 MiB device array inside
  * this library, held by every GPU that loads it until the process exits. A matrix whose
  * nwc_gemv_workspace_bytes exceeds 4 MiB (about 1M rows x 512-column blocks) is rejected with
- * NWC_ERR_INVALID_ARG. Every call rebuilds the table and zeroes the counters there, then runs
+ * NWC_ERR_INVALID_ARG. Every call zeroes the counters there, then runs
  * the GEMV on the stream; results equal nwc_gemv's. All calls share the one array, so calls that
  * overlap on the GPU (different streams, or different host threads without ordering) race.
  * The first call on a device resolves the array's device address with cudaGetSymbolAddress
