@@ -17,13 +17,17 @@
 // placeholders.
 // "Qwen3-4B-NWC-fp8": the per-channel scale is applied at the end of the matvec.
 //
-// GB300 choices: the GEMV is a persistent grid sized from the queried SM count; each warp
-// streams whole block regions (counts, code streams, mantissas) from HBM into its own
-// double-buffered shared-memory stage with one TMA bulk copy (cp.async.bulk, completion on an
-// mbarrier, bounded waits); the LUT entry carries both codes as BF16 high halves so that one
-// LOP3 merges a row pair's two raw mantissas (stored 16 bits apart) into a BF16x2; products
-// accumulate with packed FP32 FMA (FFMA2). Cross-column-block sums are done by the last warp
-// to finish a row block (one counter per row block, reset by that warp), in a fixed order.
+// GB300 choices: the GEMV is a persistent grid of one 32-warp CTA per SM (block b on CTA
+// b % grid); each warp streams whole block regions (counts, code streams, mantissas, escape
+// list) from HBM into its own shared-memory stage with one TMA bulk copy (cp.async.bulk,
+// completion on an mbarrier, bounded waits) and prefetches its next region into L2; every CTA
+// builds the 4096-entry table in shared memory while its first copies are in flight; the LUT
+// entry carries the code as a BF16 high half so that one LOP3 merges a row pair's two raw
+// mantissas (stored 16 bits apart) into a BF16x2, which feeds FMAs with BF16 operands and FP32
+// accumulators (fp8: packed FP32 FMA). Cross-column-block sums are done by the last warp to
+// finish a row block (one counter per row block, reset by that warp), in a fixed order. The
+// kernel is launched with programmatic stream serialization: it may start while the previous
+// kernel on the stream drains and waits for it before touching x, the workspace or y.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -573,20 +577,19 @@ struct Fs32 {
 };
 
 // Branch-free refill: when at most 32 bits are valid the next word is added right below them
-// with one wide multiply-add (the pages' "refilled with a single wide multiply-add"); otherwise
-// the multiplier is 0. The word was loaded by the previous refill, so the shared-memory latency
-// of the following word's load is off the decode chain.
+// by a multiply-add with 2^(32 - valid) (the pages' "refilled with a single wide multiply-add",
+// here as its low and high halves: the bits below the valid ones are zero, so no carry crosses);
+// otherwise the multiplier is 0. The word was loaded by the previous refill, so the shared-memory
+// latency of the following word's load is off the decode chain.
 __device__ __forceinline__ void fs_refill(Fs32 &s) {
     asm("{\n\t"
         ".reg .pred q;\n\t"
         ".reg .u32 t, mul;\n\t"
-        ".reg .u64 w64;\n\t"
         "and.b32 t, %3, 127;\n\t"
         "shf.r.clamp.b32 mul, 0x80000000, 0, t;\n\t"
         "setp.ne.u32 q, mul, 0;\n\t"
-        "mov.b64 w64, {%1, %0};\n\t"
-        "mad.wide.u32 w64, %4, mul, w64;\n\t"
-        "mov.b64 {%1, %0}, w64;\n\t"
+        "mad.lo.u32 %1, %4, mul, %1;\n\t"
+        "mad.hi.u32 %0, %4, mul, %0;\n\t"
         "@q add.u32 %2, %2, 4;\n\t"
         "@q add.u32 %3, %3, 32;\n\t"
         "@q ld.shared.u32 %4, [%2];\n\t"
@@ -616,9 +619,11 @@ __device__ __forceinline__ float fp8_subnormal_fix(float w) {
 }
 
 // One row pair: two single-code lookups, BF16x2 assembly with the raw mantissas. No branch:
-// an escape yields its placeholder, corrected from the block's escape list.
+// an escape yields its placeholder, corrected from the block's escape list. Returns the pair as
+// packed BF16 (row r in the low half); fp8 also returns it as FP32 in w0, w1 (with the
+// subnormal fix applied).
 template <int ELEM>
-__device__ __forceinline__ void pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
+__device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
     fs_refill(s);  // two codes take at most 24 bits; a refill leaves at least 33
     const uint32_t e1 = lut_at(s, lutb);
     fs_consume(s, e1);
@@ -626,14 +631,28 @@ __device__ __forceinline__ void pair_step(Fs32 &s, uint32_t lutb, uint32_t X, fl
     fs_consume(s, e2);
     const uint32_t e = __byte_perm(e1, e2, 0x5410);
     uint32_t bf;
-    if (ELEM == 0) bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
-    else bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
-    w0 = __uint_as_float(bf << 16);
-    w1 = __uint_as_float(bf & 0xFFFF0000u);
-    if (ELEM == 1) {
+    if (ELEM == 0) {
+        bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
+    } else {
+        bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
+        w0 = __uint_as_float(bf << 16);
+        w1 = __uint_as_float(bf & 0xFFFF0000u);
         if ((bf & 0x7F80u) == (120u << 7)) w0 = fp8_subnormal_fix(w0);
         if ((bf & 0x7F800000u) == (120u << 23)) w1 = fp8_subnormal_fix(w1);
     }
+    return bf;
+}
+
+// acc0 += lo(w2) * x, acc1 += hi(w2) * x with BF16 operands and FP32 accumulation: the BF16
+// product is exact in FP32, so each equals an FP32 FMA of the widened values.
+__device__ __forceinline__ void fma_bf16x2(uint32_t w2, uint32_t x16, float &acc0, float &acc1) {
+    asm("{\n\t.reg .b16 lo, hi, xx;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.u16.u32 xx, %3;\n\t"
+        "fma.rn.f32.bf16 %0, lo, xx, %0;\n\t"
+        "fma.rn.f32.bf16 %1, hi, xx, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w2), "r"(x16));
 }
 
 // Placeholder that the decoders produce for an escaped element with the given bits: its sign
@@ -705,6 +724,8 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
         const uint2 xn = __ldg(xp + (g < 3 ? g + 1 : 3));
+        // the group's four activations: BF16 bits (BF16 path) and FP32 (fp8 path)
+        const uint32_t x16[4] = {xq.x & 0xFFFFu, xq.x >> 16, xq.y & 0xFFFFu, xq.y >> 16};
         const float xf[4] = {__uint_as_float(xq.x << 16), __uint_as_float(xq.x & 0xFFFF0000u),
                              __uint_as_float(xq.y << 16), __uint_as_float(xq.y & 0xFFFF0000u)};
         uint32_t mw[MWG];
@@ -713,14 +734,18 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
 #pragma unroll
         for (int q = 0; q < 16; q++) {
             const int pp = q & 3;
-            const float xc = xf[q >> 2];
             const uint32_t X = xpair<F>(mw, q);
             float w0, w1;
-            pair_step<ELEM>(s, lutb, X, w0, w1);
-            const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
-                                        make_float2(acc[2 * pp], acc[2 * pp + 1]));
-            acc[2 * pp] = r.x;
-            acc[2 * pp + 1] = r.y;
+            const uint32_t w2 = pair_step<ELEM>(s, lutb, X, w0, w1);
+            if (ELEM == 0) {
+                fma_bf16x2(w2, x16[q >> 2], acc[2 * pp], acc[2 * pp + 1]);
+            } else {
+                const float xc = xf[q >> 2];
+                const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
+                                            make_float2(acc[2 * pp], acc[2 * pp + 1]));
+                acc[2 * pp] = r.x;
+                acc[2 * pp + 1] = r.y;
+            }
         }
         xq = xn;
     }
