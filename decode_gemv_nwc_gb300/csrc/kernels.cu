@@ -174,32 +174,9 @@ __device__ __forceinline__ uint32_t elem_bits(uint32_t s, uint32_t v, uint32_t m
     return ELEM == 0 ? ((s << 15) | (v << 7) | m) : ((s << 7) | (v << 3) | m);
 }
 
-// Generic decode of one lane of one block: calls fn(t, s, v, m, esc) for each real element t
-// (t = 8c + r, both static after unrolling). rows/cols are the lane's real extent. Returns the
-// number of escape codes in the lane's 128 codes.
-template <int ELEM, class Fn>
-__device__ __forceinline__ uint32_t lane_generic(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
-                                                 const uint8_t *rexp, Fn &&fn) {
-    constexpr int F = ELEM == 0 ? 7 : 3;
-    uint32_t je = 0, jo = 0, n_esc = 0;
-#pragma unroll
-    for (int t = 0; t < kSyms; t++) {
-        const int c = t >> 3, r = t & 7;
-        uint32_t s, v;
-        const bool esc = decode_one(ls, nr, rexp, s, v);
-        n_esc += esc;
-        if (r < rows && c < cols) {
-            uint32_t m;
-            if (r & 1) m = half_field<F>(man, 1, jo++);
-            else m = half_field<F>(man, 0, je++);
-            fn(t, s, v, m, esc);
-        }
-    }
-    return n_esc;
-}
-
-// The same decode with the column loop rolled (rows unrolled): fn(c, r, s, v, m, esc) with c
-// dynamic. Smaller code and fewer live registers, for callers that need no static column.
+// Generic decode of one lane of one block, column loop rolled and rows unrolled: calls
+// fn(c, r, s, v, m, esc) for each real element (column c, row r of the lane). rows/cols are the
+// lane's real extent. Returns the number of escape codes in the lane's 128 codes.
 template <int ELEM, class Fn>
 __device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
                                                 const uint8_t *rexp, Fn &&fn) {
@@ -302,149 +279,6 @@ __device__ __noinline__ bool esc_patch(const uint32_t *esc, uint32_t slots, uint
     return ok;
 }
 
-// =================================================================== decode kernel
-template <int ELEM>
-__global__ void __launch_bounds__(256) decode_kernel(Mat m, void *out, int64_t ld_out) {
-    __shared__ uint8_t rexp[16];
-    load_rank_table(m, rexp);
-    __syncthreads();
-    constexpr int F = ELEM == 0 ? 7 : 3;
-    const int lane = threadIdx.x & 31;
-    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
-    for (uint64_t b = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < m.nb; b += warps) {
-        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
-        const int rows = real_rows(m.n, rb), cols = real_cols(m.k, cb, lane);
-        const uint32_t t0 = m.tab[b], t1 = m.tab[b + 1];
-        const uint8_t *reg = m.data + 16 * (uint64_t)t0;
-        LaneRegion lr = lane_region(reg, 16 * (t1 - t0), lane, rows, m.k, cb, F);
-        LaneStream ls;
-        ls.init(lr.code, lr.nwords);
-        uint32_t o[8][8];  // [row][column pair] two elements per word (BF16) / [row][4 bytes]
-#pragma unroll
-        for (int r = 0; r < 8; r++)
-#pragma unroll
-            for (int i = 0; i < 8; i++) o[r][i] = 0;
-        const uint32_t n_esc =
-            lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp, [&](int t, uint32_t s, uint32_t v, uint32_t mm, bool) {
-                const int c = t >> 3, r = t & 7;
-                const uint32_t e = elem_bits<ELEM>(s, v, mm);
-                if (ELEM == 0) o[r][c >> 1] |= e << (16 * (c & 1));
-                else o[r][c >> 2] |= e << (8 * (c & 3));
-            });
-        bool bad = ls.overrun();
-        const uint32_t esc_start = esc_slice(lr, n_esc, lane, bad);
-        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
-#pragma unroll
-        for (int r = 0; r < 8; r++) {
-            if (r >= rows) break;
-            const uint64_t row = rb * kRows + (uint64_t)r;
-            if (ELEM == 0) {
-                uint16_t *dst = static_cast<uint16_t *>(out) + row * (uint64_t)ld_out + col0;
-                if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[r][0], o[r][1], o[r][2], o[r][3]);
-                    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[r][4], o[r][5], o[r][6], o[r][7]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 16; c++)
-                        if (c < cols) dst[c] = (uint16_t)(o[r][c >> 1] >> (16 * (c & 1)));
-                }
-            } else {
-                uint8_t *dst = static_cast<uint8_t *>(out) + row * (uint64_t)ld_out + col0;
-                if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[r][0], o[r][1], o[r][2], o[r][3]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 16; c++)
-                        if (c < cols) dst[c] = (uint8_t)(o[r][c >> 2] >> (8 * (c & 3)));
-                }
-            }
-        }
-        // escaped elements over their placeholders (same thread, so after the stores above)
-        if (!esc_patch<ELEM>(lr.esc, lr.slots, esc_start, n_esc, lane, rows, cols, -1, out, ld_out,
-                             (int64_t)(rb * kRows), col0))
-            bad = true;
-        if (bad) raise_error(kErrFormat);
-    }
-}
-
-// =================================================================== gather kernel
-template <int ELEM>
-__global__ void __launch_bounds__(256) gather_kernel(Mat m, const int32_t *ids, int64_t n_ids, void *out,
-                                                     int64_t ld_out) {
-    __shared__ uint8_t rexp[16];
-    load_rank_table(m, rexp);
-    __syncthreads();
-    constexpr int F = ELEM == 0 ? 7 : 3;
-    const int lane = threadIdx.x & 31;
-    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
-    const uint64_t items = (uint64_t)n_ids * m.cbs;
-    for (uint64_t it = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
-        const uint64_t i = it / m.cbs, cb = it % m.cbs;
-        const int64_t id = ids[i];
-        const int cols = real_cols(m.k, cb, lane);
-        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
-        uint32_t o[8];
-#pragma unroll
-        for (int c = 0; c < 8; c++) o[c] = 0;
-        LaneRegion lr{};
-        uint32_t n_esc = 0, esc_start = 0;
-        int rows = 0, want = 0;
-        bool bad = false;
-        const bool valid = id >= 0 && (uint64_t)id < m.n;
-        if (!valid) {
-            if (lane == 0 && cb == 0) raise_error(kErrId);
-        } else {
-            const uint64_t rb = (uint64_t)id >> 3;
-            want = (int)(id & 7);
-            rows = real_rows(m.n, rb);
-            const uint32_t t0 = m.tab[rb * m.cbs + cb], t1 = m.tab[rb * m.cbs + cb + 1];
-            const uint8_t *reg = m.data + 16 * (uint64_t)t0;
-            lr = lane_region(reg, 16 * (t1 - t0), lane, rows, m.k, cb, F);
-            LaneStream ls;
-            ls.init(lr.code, lr.nwords);
-            n_esc = lane_generic<ELEM>(ls, lr.man, rows, cols, m.nr, rexp,
-                                       [&](int t, uint32_t s, uint32_t v, uint32_t mm, bool) {
-                const int c = t >> 3, r = t & 7;
-                if (r == want) {
-                    const uint32_t e = elem_bits<ELEM>(s, v, mm);
-                    if (ELEM == 0) o[c >> 1] |= e << (16 * (c & 1));
-                    else o[c >> 2] |= e << (8 * (c & 3));
-                }
-            });
-            bad = ls.overrun();
-            esc_start = esc_slice(lr, n_esc, lane, bad);
-        }
-        if (ELEM == 0) {
-            uint16_t *dst = static_cast<uint16_t *>(out) + i * (uint64_t)ld_out + col0;
-            if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 16; c++)
-                    if (c < cols) dst[c] = (uint16_t)(o[c >> 1] >> (16 * (c & 1)));
-            }
-        } else {
-            uint8_t *dst = static_cast<uint8_t *>(out) + i * (uint64_t)ld_out + col0;
-            if (cols == 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 16; c++)
-                    if (c < cols) dst[c] = (uint8_t)(o[c >> 2] >> (8 * (c & 3)));
-            }
-        }
-        if (valid) {
-            // escaped elements of the wanted row over their placeholders (same thread: after
-            // the stores above)
-            if (!esc_patch<ELEM>(lr.esc, lr.slots, esc_start, n_esc, lane, rows, cols, want, out, ld_out,
-                                 (int64_t)i - want, col0))
-                bad = true;
-            if (bad) raise_error(kErrFormat);
-        }
-    }
-}
-
 // =================================================================== GEMV kernel
 // Warps per CTA (one CTA per SM) and block-region stages per warp. With one stage the next
 // region is prefetched into L2 while the current one is decoded, then copied in.
@@ -504,29 +338,35 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint3
 //   bits 5..6   zero (whole entries may be subtracted from the bit counter)
 //   bits 7..15  the code as a BF16 high part (s << 15 | exponent << 7); an escape gets
 //               exponent field 0, the placeholder that the escape list corrects
+//   bit 24      set for an escape (sums of up to 128 entries stay below it, so a running sum
+//               counts a lane's escapes in its top byte)
+// RAW8 (fp8 decode and gather): s << 15 | v << 11 instead, so that with the mantissa at bits
+// 8..10 each half's high byte is the e4m3 code itself.
 // fp8 exponents e are stored as BF16 exponents e + 120 (exact for normal e4m3 values;
 // subnormals are corrected after assembly). A 12-bit peek holds any code (at most
 // n_ranked + 1 <= 12 bits), which is why at most 11 exponents are ranked.
-template <int ELEM>
+template <int ELEM, bool RAW8>
 __device__ __forceinline__ uint32_t lut_entry(uint32_t P, int nr, const uint32_t (&rank4)[3]) {
     const uint32_t bits = P << 20;
     const int ones = __clz(~bits);
-    if (ones >= nr) return (((bits >> (31 - nr)) & 1u) << 15) | (uint32_t)(nr + 1);
+    if (ones >= nr) return (1u << 24) | (((bits >> (31 - nr)) & 1u) << 15) | (uint32_t)(nr + 1);
     const uint32_t word = ones < 4 ? rank4[0] : (ones < 8 ? rank4[1] : rank4[2]);
     const uint32_t s = (bits >> (30 - ones)) & 1u, v = (word >> (8 * (ones & 3))) & 0xFFu;
+    if (RAW8) return (s << 15) | (v << 11) | ((uint32_t)ones + 2);
     return (s << 15) | ((ELEM == 0 ? v : v + 120u) << 7) | ((uint32_t)ones + 2);
 }
 
 // Builds the 4096-entry table in shared memory with all threads of the CTA; the rank table is
 // read from the kernel parameter with static offsets only (packed four values per word).
-template <int ELEM>
+template <int ELEM, bool RAW8 = false>
 __device__ __forceinline__ void build_lut(const Mat &m, uint32_t *lut) {
     uint32_t rank4[3];
 #pragma unroll
     for (int i = 0; i < 3; i++)
         rank4[i] = (uint32_t)m.rank_exp[4 * i] | (uint32_t)m.rank_exp[4 * i + 1] << 8 |
                    (uint32_t)m.rank_exp[4 * i + 2] << 16 | (uint32_t)m.rank_exp[4 * i + 3] << 24;
-    for (uint32_t i = threadIdx.x; i < (uint32_t)kLutEntries; i += blockDim.x) lut[i] = lut_entry<ELEM>(i, m.nr, rank4);
+    for (uint32_t i = threadIdx.x; i < (uint32_t)kLutEntries; i += blockDim.x)
+        lut[i] = lut_entry<ELEM, RAW8>(i, m.nr, rank4);
 }
 
 // Pair q's two mantissas (even t at bits 0.., odd t at bits 16..) from a group's words.
@@ -923,6 +763,295 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
     if (bad) raise_error(kErrFormat);
 }
 
+// =================================================================== decode and gather
+// "Dequantization and embedding lookup (tied lm_head) run on the same decoder": the same CTA
+// layout, table and staged regions as the GEMV. MODE 0 decodes every block to BF16 (fp8: e4m3
+// bytes); MODE 1 writes, for each id, that row of the block row, one block per warp item.
+
+// One row pair of the unpack path: returns rows (2pp, 2pp+1) at one column as two 16-bit
+// halves (BF16 bits; fp8: the e4m3 code in each half's high byte) and adds both entries to
+// `flags`, whose top byte then counts the lane's escapes.
+template <int ELEM>
+__device__ __forceinline__ uint32_t unpack_pair(Fs32 &s, uint32_t lutb, uint32_t X, uint32_t &flags) {
+    fs_refill(s);
+    const uint32_t e1 = lut_at(s, lutb);
+    fs_consume(s, e1);
+    const uint32_t e2 = lut_at(s, lutb);
+    fs_consume(s, e2);
+    flags += e1 + e2;
+    const uint32_t e = __byte_perm(e1, e2, 0x5410);
+    return ELEM == 0 ? (e & 0xFF80FF80u) | (X & 0x007F007Fu) : (e & 0xFF80FF80u) | ((X & 0x00070007u) << 8);
+}
+
+// Row word of 4 columns from the group's pairs p[c4 * 4 + pp]: BF16 rows give two words (cols
+// 0-1, 2-3), fp8 rows one word of four bytes. hi selects row 2pp + 1.
+template <int ELEM>
+__device__ __forceinline__ uint2 row_words(uint32_t a, uint32_t b, uint32_t c, uint32_t d, bool hi) {
+    if (ELEM == 0) {
+        const uint32_t sel = hi ? 0x7632u : 0x5410u;
+        return make_uint2(__byte_perm(a, b, sel), __byte_perm(c, d, sel));
+    }
+    const uint32_t sel = hi ? 0x0073u : 0x0051u;
+    return make_uint2(__byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410), 0u);
+}
+
+template <int ELEM>
+__device__ __forceinline__ void store_row4(void *out, uint64_t at, uint2 w, bool vec) {
+    if (ELEM == 0) {
+        uint16_t *o = static_cast<uint16_t *>(out) + at;
+        if (vec) {
+            *reinterpret_cast<uint2 *>(o) = w;
+        } else {
+            o[0] = (uint16_t)w.x;
+            o[1] = (uint16_t)(w.x >> 16);
+            o[2] = (uint16_t)w.y;
+            o[3] = (uint16_t)(w.y >> 16);
+        }
+    } else {
+        uint8_t *o = static_cast<uint8_t *>(out) + at;
+        if (vec) {
+            *reinterpret_cast<uint32_t *>(o) = w.x;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; i++) o[i] = (uint8_t)(w.x >> (8 * i));
+        }
+    }
+}
+
+// Interior block from its staged region. Decode writes rows row0 .. row0 + 7; gather writes
+// row `want` of the block to output row row0. col0 = the lane's first column.
+template <int ELEM, int MODE>
+__device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
+                                            void *out, int64_t ld_out, uint64_t row0, uint64_t col0, int want,
+                                            bool vec, bool &bad) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    constexpr int MW = ELEM == 0 ? 28 : 12;
+    constexpr int MWG = MW / 4;
+    const uint32_t lw = reg[lane];
+    uint32_t incl = lw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
+    const uint32_t code = regs + 32 + 4 * (incl - lw);
+    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * MW * 4;
+    Fs32 s;
+    {
+        uint32_t w0 = 0, w1 = 0;
+        if (lw > 0) asm("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(code));
+        if (lw > 1) asm("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(code + 4));
+        s.wh = w0;
+        s.wl = w1;
+        s.pa = code + 8;
+        s.V = 63u;
+        asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
+    }
+    const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
+    uint32_t flags = 0;
+    const int wpp = want >> 1;
+    const bool whi = want & 1;
+#pragma unroll 1
+    for (int g = 0; g < 4; g++) {
+        uint32_t mw[MWG];
+#pragma unroll
+        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * (MWG * g + i)));
+        uint32_t p[16];  // p[c4 * 4 + pp]: rows (2pp, 2pp + 1) at column 4g + c4
+#pragma unroll
+        for (int q = 0; q < 16; q++) p[q] = unpack_pair<ELEM>(s, lutb, xpair<F>(mw, q), flags);
+        const uint64_t c = col0 + 4 * (uint64_t)g;
+        if (MODE == 0) {
+#pragma unroll
+            for (int pp = 0; pp < 4; pp++) {
+                const uint64_t r = row0 + 2 * (uint64_t)pp;
+                store_row4<ELEM>(out, r * (uint64_t)ld_out + c, row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], false), vec);
+                store_row4<ELEM>(out, (r + 1) * (uint64_t)ld_out + c, row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], true), vec);
+            }
+        } else {
+            uint32_t v[4];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; c4++)
+                v[c4] = wpp == 0 ? p[c4 * 4] : (wpp == 1 ? p[c4 * 4 + 1] : (wpp == 2 ? p[c4 * 4 + 2] : p[c4 * 4 + 3]));
+            store_row4<ELEM>(out, row0 * (uint64_t)ld_out + c, row_words<ELEM>(v[0], v[1], v[2], v[3], whi), vec);
+        }
+    }
+    const uint32_t valid = (s.V & 127u) + 1u;
+    const uint32_t inserted = (s.pa - code) * 8u;
+    bad |= inserted - valid > 32u * lw;
+    // escaped elements over their placeholders: this lane's slice of the list
+    LaneRegion lr;
+    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
+    lr.esc = reinterpret_cast<const uint32_t *>(reg + esc0);
+    lr.slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
+    const uint32_t n_esc = flags >> 24;
+    const uint32_t start = esc_slice(lr, n_esc, lane, bad);
+    const uint64_t lane_col = col0;
+    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, kRows, kLaneCols, MODE == 0 ? -1 : want, out, ld_out,
+                         MODE == 0 ? (int64_t)row0 : (int64_t)row0 - want, lane_col))
+        bad = true;
+}
+
+// Any block (edge, or a region too large to stage), element by element.
+template <int ELEM, int MODE>
+__device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t bytes, int lane, const uint8_t *rexp,
+                                               int nr, int rows, uint64_t k, uint64_t cb, void *out, int64_t ld_out,
+                                               uint64_t row0, uint64_t col0, int want, bool &bad) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    const int cols = real_cols(k, cb, lane);
+    LaneRegion lr = lane_region(reg, bytes, lane, rows, k, cb, F);
+    LaneStream ls;
+    ls.init(lr.code, lr.nwords);
+    const uint32_t n_esc =
+        lane_rolled<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int c, int r, uint32_t sg, uint32_t v, uint32_t mm, bool esc) {
+            if (MODE == 1 && r != want) return;
+            const uint64_t row = MODE == 0 ? row0 + (uint64_t)r : row0;
+            const uint32_t e = elem_bits<ELEM>(sg, esc ? 0u : v, mm);
+            if (ELEM == 0) static_cast<uint16_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint16_t)e;
+            else static_cast<uint8_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint8_t)e;
+        });
+    bad |= ls.overrun();
+    const uint32_t start = esc_slice(lr, n_esc, lane, bad);
+    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, rows, cols, MODE == 0 ? -1 : want, out, ld_out,
+                         MODE == 0 ? (int64_t)row0 : (int64_t)row0 - want, col0))
+        bad = true;
+}
+
+template <int ELEM, int MODE>
+__global__ void __launch_bounds__(kGemvWarps * 32, 1)
+    unpack_kernel(Mat m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint8_t *rexp = smem + kRexpOff;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16);
+    uint8_t *stage = smem + kStageOff + warp * kStagesPerWarp * kStageBytes;
+    const uint64_t stride = (uint64_t)gridDim.x * kGemvWarps;
+    uint32_t phase = 0;
+    bool bad = false, timed_out = false;
+
+    // Work item it -> block b, wanted row (gather) and first output row. Gather ids are read by
+    // lane 0 and broadcast; an out-of-range id gives ok = false.
+    auto locate = [&](uint64_t it, uint64_t &b, int &want, uint64_t &orow, bool &ok) {
+        if (MODE == 0) {
+            b = it;
+            want = -1;
+            orow = (it / m.cbs) * kRows;
+            ok = true;
+        } else {
+            const uint64_t i = it / m.cbs, cb = it % m.cbs;
+            int32_t id = 0;
+            if (lane == 0) id = ids[i];
+            id = __shfl_sync(0xFFFFFFFFu, id, 0);
+            ok = id >= 0 && (uint64_t)id < m.n;
+            const uint64_t uid = ok ? (uint64_t)id : 0;
+            b = (uid >> 3) * m.cbs + cb;
+            want = (int)(uid & 7);
+            orow = i;
+        }
+    };
+    auto region = [&](uint64_t bb, const uint8_t *&ptr, uint32_t &bytes) {
+        uint32_t s0 = 0, s1 = 0;
+        if (lane == 0) {
+            s0 = m.tab[bb];
+            s1 = m.tab[bb + 1];
+        }
+        s0 = __shfl_sync(0xFFFFFFFFu, s0, 0);
+        s1 = __shfl_sync(0xFFFFFFFFu, s1, 0);
+        ptr = m.data + 16 * (uint64_t)s0;
+        bytes = 16 * (s1 - s0);
+    };
+    auto issue = [&](uint64_t bb) {
+        const uint8_t *src;
+        uint32_t bytes;
+        region(bb, src, bytes);
+        if (bytes <= (uint32_t)kStageBytes && lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar0, bytes);
+            tma_load_1d(smem_u32(stage), src, bytes, bar0);
+        }
+    };
+
+    if (lane == 0) {
+        mbar_init(bar0);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    uint64_t it = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
+    uint64_t b = 0, orow = 0;
+    int want = 0;
+    bool ok = false;
+    if (it < n_items) {
+        locate(it, b, want, orow, ok);
+        if (ok) issue(b);
+    }
+    load_rank_table(m, rexp);
+    build_lut<ELEM, ELEM == 1>(m, lut);
+    __syncthreads();
+
+    while (it < n_items) {
+        const uint64_t nxt = it + stride;
+        uint64_t nb_ = 0, norow = 0;
+        int nwant = 0;
+        bool nok = false;
+        if (nxt < n_items) {
+            locate(nxt, nb_, nwant, norow, nok);
+            if (nok && lane == 0) {
+                const uint32_t s0 = m.tab[nb_], s1 = m.tab[nb_ + 1];
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(m.data + 16 * (uint64_t)s0),
+                             "r"(16 * (s1 - s0))
+                             : "memory");
+            }
+        }
+        const uint64_t cb = MODE == 0 ? it % m.cbs : (it % m.cbs);
+        const uint64_t col0 = cb * kCols + (uint64_t)lane * kLaneCols;
+        if (!ok) {
+            // gather id out of range: a zero row, and the error word
+            if (lane == 0 && cb == 0) raise_error(kErrId);
+            const int cols = real_cols(m.k, cb, lane);
+            for (int c = 0; c < cols; c++) {
+                if (ELEM == 0) static_cast<uint16_t *>(out)[orow * (uint64_t)ld_out + col0 + c] = 0;
+                else static_cast<uint8_t *>(out)[orow * (uint64_t)ld_out + col0 + c] = 0;
+            }
+        } else {
+            const uint8_t *src;
+            uint32_t bytes;
+            region(b, src, bytes);
+            const uint8_t *reg = src;
+            const bool staged = bytes <= (uint32_t)kStageBytes;
+            if (staged) {
+                if (!mbar_wait(bar0, phase & 1u)) {
+                    timed_out = true;
+                    break;
+                }
+                phase ^= 1u;
+                reg = stage;
+            }
+            const uint64_t rb = b / m.cbs;
+            const int rows = real_rows(m.n, rb);
+            const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
+            if (interior && staged)
+                unpack_fast<ELEM, MODE>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec != 0, bad);
+            else
+                unpack_generic<ELEM, MODE>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, out, ld_out, orow, col0, want,
+                                           bad);
+        }
+        __syncwarp();
+        if (nxt < n_items && nok) issue(nb_);
+        it = nxt;
+        b = nb_;
+        want = nwant;
+        orow = norow;
+        ok = nok;
+    }
+    if (timed_out) {
+        raise_error(kErrTimeout);
+        mbar_wait(bar0, phase & 1u);  // let this warp's copy land before shared memory goes away
+    }
+    if (bad) raise_error(kErrFormat);
+}
+
 // =================================================================== host side
 int g_sm_count = -1;
 std::mutex g_mu;
@@ -951,17 +1080,37 @@ uint64_t pad_rows(const nwc_matrix &m) { return (uint64_t)m.row_blocks * kRows; 
 
 extern "C" int nwc_sm_count(void) { return sm_count(); }
 
+namespace {
+template <int ELEM, int MODE>
+nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec,
+                         cudaStream_t s) {
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    static bool smem_ok = false;
+    static std::once_flag once;
+    std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE>, kGemvSmem); });
+    if (!smem_ok) return NWC_ERR_CUDA;
+    const int grid = (int)(n_items < (uint64_t)sms ? n_items : (uint64_t)sms);
+    unpack_kernel<ELEM, MODE><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, ids, n_items, out, ld_out, vec);
+    return launched();
+}
+
+// Row stores of 4 columns are vectorised when every row start keeps their alignment.
+int vec_ok(const void *out, int64_t ld_out, int elem) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out);
+    return elem == NWC_ELEM_BF16 ? ((a % 8) == 0 && (ld_out % 4) == 0) : ((a % 4) == 0 && (ld_out % 4) == 0);
+}
+
+}  // namespace
+
 extern "C" nwc_status nwc_decode(const nwc_matrix *mp, void *out, int64_t ld_out, float *scales_out, nwc_stream stream) {
     if (!mp || !out || ld_out < mp->k) return NWC_ERR_INVALID_ARG;
     const Mat m = to_mat(*mp);
-    const int sms = sm_count();
-    if (sms <= 0) return NWC_ERR_CUDA;
-    const uint64_t want = (m.nb + 7) / 8;
-    const int grid = (int)(want < (uint64_t)sms * 8 ? (want ? want : 1) : (uint64_t)sms * 8);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (m.elem == NWC_ELEM_BF16) decode_kernel<0><<<grid, 256, 0, s>>>(m, out, ld_out);
-    else decode_kernel<1><<<grid, 256, 0, s>>>(m, out, ld_out);
-    if (launched() != NWC_OK) return NWC_ERR_CUDA;
+    const int vec = vec_ok(out, ld_out, m.elem);
+    const nwc_status st = m.elem == NWC_ELEM_BF16 ? launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s)
+                                                  : launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
+    if (st != NWC_OK) return st;
     if (m.elem == NWC_ELEM_FP8_E4M3 && scales_out) {
         if (cudaMemcpyAsync(scales_out, m.scales, 4 * m.n, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
             return NWC_ERR_CUDA;
@@ -975,14 +1124,11 @@ extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64
     if (n_ids == 0) return NWC_OK;
     if (!ids || !out) return NWC_ERR_INVALID_ARG;
     const Mat m = to_mat(*mp);
-    const int sms = sm_count();
-    if (sms <= 0) return NWC_ERR_CUDA;
-    const uint64_t items = (uint64_t)n_ids * m.cbs, want = (items + 7) / 8;
-    const int grid = (int)(want < (uint64_t)sms * 8 ? want : (uint64_t)sms * 8);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (m.elem == NWC_ELEM_BF16) gather_kernel<0><<<grid, 256, 0, s>>>(m, ids, n_ids, out, ld_out);
-    else gather_kernel<1><<<grid, 256, 0, s>>>(m, ids, n_ids, out, ld_out);
-    return launched();
+    const int vec = vec_ok(out, ld_out, m.elem);
+    const uint64_t items = (uint64_t)n_ids * m.cbs;
+    return m.elem == NWC_ELEM_BF16 ? launch_unpack<0, 1>(m, ids, items, out, ld_out, vec, s)
+                                   : launch_unpack<1, 1>(m, ids, items, out, ld_out, vec, s);
 }
 
 namespace {

@@ -233,6 +233,51 @@ def test_gather_ragged_width_fp8():
     assert np.array_equal(out, q[ids])
 
 
+def _escape_heavy(shape, seed):
+    rng = np.random.default_rng(seed)
+    w = synth.normal_bf16(shape, 0.02, seed=seed)
+    hit = rng.random(w.shape) < 0.03
+    odd = (rng.integers(0, 2, w.shape) << 15) | (rng.integers(100, 150, w.shape) << 7) | rng.integers(0, 128, w.shape)
+    return np.where(hit, odd, w).astype(np.uint16)
+
+
+def test_decode_and_gather_strided_unaligned_outputs():
+    """Row strides that are not multiples of 4 and an output start off 8-byte alignment take
+    the element-wise store path; untouched columns keep their sentinel."""
+    n, k = 40, 2600
+    w = _escape_heavy((n, k), 31)
+    mat = nwc.Matrix(nwc.encode(w))
+    big = torch.full((n, k + 3), -7, dtype=torch.int16, device="cuda")
+    view = big[:, 1:k + 1]
+    mat.decode(out=view)
+    assert_clean()
+    got = big.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, 1:k + 1], w)
+    assert (got[:, 0] == np.uint16(0xFFF9)).all() and (got[:, k + 1:] == np.uint16(0xFFF9)).all()
+    ids = np.array([39, 0, 17, 17, 8, 33], np.int32)
+    gbig = torch.full((len(ids), k + 1), -7, dtype=torch.int16, device="cuda")
+    mat.gather(torch.from_numpy(ids).cuda(), out=gbig[:, :k])
+    assert_clean()
+    g = gbig.cpu().numpy().view(np.uint16)
+    assert np.array_equal(g[:, :k], w[ids]) and (g[:, k] == np.uint16(0xFFF9)).all()
+    # fp8 bytes, stride k + 1
+    q, sc = oracle.quantize_fp8(w)
+    m8 = nwc.Matrix(nwc.encode_fp8(q, sc))
+    out8 = torch.zeros((n, k + 1), dtype=torch.uint8, device="cuda")
+    o8, s8 = m8.decode(out=out8[:, :k])
+    assert_clean()
+    assert np.array_equal(out8.cpu().numpy()[:, :k], q) and np.array_equal(s8.cpu().numpy(), sc)
+
+
+def test_gather_escape_heavy_rows():
+    w = _escape_heavy((512, 4096), 32)
+    mat = nwc.Matrix(nwc.encode(w))
+    ids = synth.token_ids(700, 512, seed=33)
+    out = mat.gather(torch.from_numpy(ids).cuda()).cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w[ids])
+
+
 @pytest.mark.slow
 def test_embedding_table_gather_and_lm_head_sampled():
     """151936 x 2560 tied table: 4096 random ids bit-exact, then the lm_head GEMV on
