@@ -239,6 +239,33 @@ def extra_workloads(dev, stream, steps):
     del mats, wbf, ys, yb
     torch.cuda.empty_cache()
 
+    # The same stack with fused projections ("fuse(model)" on the NWC page: q|k|v and gate|up
+    # share their input, so each group is one matrix with its rows stacked): 144 GEMVs a token.
+    t0 = time.time()
+    mats, ys, wbf = [], [], []
+    comp_bytes = 0
+    for layer in range(synth.N_LAYERS):
+        ws = {name: synth.layer_matrix(layer, name, device=dev) for name, _, _ in synth.LAYER_SHAPES}
+        for group in (("q", "k", "v"), ("o",), ("gate", "up"), ("down",)):
+            w = torch.cat([ws[g] for g in group]) if len(group) > 1 else ws[group[0]]
+            blob = encode_on_host(w)
+            comp_bytes += len(blob)
+            mats.append(nwc.Matrix(blob, device=dev))
+            wbf.append(w.view(torch.bfloat16))
+            ys.append(torch.empty(w.shape[0], dtype=torch.float32, device=dev))
+        del ws
+    build_s = time.time() - t0
+    yb = [torch.empty(w.shape[0], dtype=torch.bfloat16, device=dev) for w in wbf]
+    tok_ms = time_graph(stack, stream, max(3, steps // 2))
+    tok_bf16 = time_graph(stack_bf16, stream, max(3, steps // 2))
+    out["stack_token_fused"] = {
+        "workload": "36-layer stack with fused projections (q|k|v, o, gate|up, down), one CUDA graph",
+        "gemvs": len(mats), "us_per_token": tok_ms * 1e3, "compressed_bytes": comp_bytes,
+        "compressed_gbs": comp_bytes / (tok_ms * 1e-3) / 1e9, "frac_of_measured_hbm": comp_bytes / (tok_ms * 1e-3) / 1e9 / peak,
+        "bf16_cublas_us_per_token": tok_bf16 * 1e3, "speedup_vs_bf16": tok_bf16 / tok_ms, "build_seconds": build_s}
+    del mats, wbf, ys, yb
+    torch.cuda.empty_cache()
+
     # tied embedding / lm_head 151936 x 2560: gather 4096 ids, then the lm_head GEMV
     w = synth.normal_bf16((synth.VOCAB, synth.HIDDEN), 0.02, 7, device=dev)
     blob = encode_on_host(w)

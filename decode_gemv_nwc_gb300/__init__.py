@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "BF16", "FP8", "NwcError", "lib", "encode", "encode_fp8", "quantize_fp8", "validate",
-    "Matrix", "check", "sm_count", "status_str",
+    "Matrix", "check", "sm_count", "status_str", "save", "load",
 ]
 
 BF16, FP8 = 0, 1
@@ -198,6 +198,22 @@ class Matrix:
                              ctypes.c_void_p(scales.data_ptr()), _stream_ptr(stream)), "nwc_decode")
         return out, scales
 
+    def matmul(self, x, scratch=None, stream=None):
+        """Batch > 1 (prefill): Y[B, N] = X[B, K] W^T in BF16. The matrix is decoded into a BF16
+        scratch (allocated once and kept unless given) and multiplied by cuBLAS through torch,
+        as the NWC page describes for prefill ("dequantizes to BF16 and calls cuBLAS")."""
+        import torch
+        assert self.elem == BF16, "matmul serves BF16 matrices"
+        if scratch is None:
+            scratch = getattr(self, "_scratch", None)
+            if scratch is None:
+                scratch = torch.empty((self.n, self.k), dtype=torch.int16, device=self.device_blob.device)
+                self._scratch = scratch
+        self.decode(out=scratch, stream=stream)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            return torch.nn.functional.linear(x.view(torch.bfloat16), scratch.view(torch.bfloat16))
+
     def gather(self, ids, out=None, stream=None):
         """Rows ids (int32 CUDA tensor) of the stored matrix, bit-exact."""
         import torch
@@ -207,3 +223,45 @@ class Matrix:
         _ok(lib().nwc_gather(ctypes.byref(self.m), ctypes.c_void_p(ids.data_ptr()), ids.numel(),
                              ctypes.c_void_p(out.data_ptr()), out.stride(0), _stream_ptr(stream)), "nwc_gather")
         return out
+
+
+# ------------------------------------------------------------------ blob files
+_FILE_MAGIC = b"NWCF"
+
+
+def save(path: str, blobs: dict) -> None:
+    """Writes named blobs to one file: "NWCF", u32 count, then per entry u32 name length, the
+    UTF-8 name, u64 blob length and the blob, each blob starting on a 16-byte boundary."""
+    import struct
+    with open(path, "wb") as f:
+        f.write(_FILE_MAGIC + struct.pack("<I", len(blobs)))
+        for name, blob in blobs.items():
+            nb = name.encode()
+            f.write(struct.pack("<I", len(nb)) + nb + struct.pack("<Q", len(blob)))
+            f.write(b"\0" * (-f.tell() % 16))
+            f.write(blob)
+
+
+def load(path: str) -> dict:
+    """Reads a file written by save(); every blob is validated (nwc_validate) before it is
+    returned."""
+    import struct
+    with open(path, "rb") as f:
+        data = f.read()
+    if data[:4] != _FILE_MAGIC:
+        raise NwcError(2, "nwc load: not an NWC blob file")
+    (count,) = struct.unpack_from("<I", data, 4)
+    pos, out = 8, {}
+    for _ in range(count):
+        (ln,) = struct.unpack_from("<I", data, pos)
+        name = data[pos + 4:pos + 4 + ln].decode()
+        (size,) = struct.unpack_from("<Q", data, pos + 4 + ln)
+        pos += 4 + ln + 8
+        pos += -pos % 16
+        blob = data[pos:pos + size]
+        if len(blob) != size:
+            raise NwcError(2, f"nwc load: {name} truncated")
+        _ok(validate(blob), f"nwc load: {name}")
+        out[name] = blob
+        pos += size
+    return out

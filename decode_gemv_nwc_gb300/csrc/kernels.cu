@@ -729,13 +729,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
             if (writer) partial[cb * n_pad + row] = sum;
             __syncwarp();
             uint32_t ticket = 0;
-            // release: the warp's partial sums (ordered before lane 0 by the warp barrier) are
-            // visible to whoever takes the last ticket; acquire on that side below
+            // Release: the warp's partial sums (ordered before lane 0 by the warp barrier) are
+            // visible to whoever takes the last ticket. Acquire: the last taker's lane 0 gets
+            // it from the same atomic, and the warp barrier orders the other lanes' loads after.
             if (lane == 0)
                 asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
             if (ticket == (uint32_t)m.cbs - 1) {
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                __syncwarp();
                 // row lane % 8; lane / 8 sums column blocks lane / 8, + 4, ... (loads in
                 // parallel across the warp), then a fixed shuffle order adds the four
                 const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);

@@ -139,3 +139,17 @@ def test_encode_argument_errors():
     small = ctypes.c_size_t(size.value - 1)
     buf = np.zeros(size.value, np.uint8)
     assert L.nwc_encode(p, 2, 2, 2, 0, 1, buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(small)) == 1
+
+
+def test_blob_file_round_trip(tmp_path):
+    blobs = {"q": nwc.encode(synth.normal_bf16((9, 513), 0.02, 1)),
+             "lm_head": nwc.encode(synth.normal_bf16((17, 100), 0.02, 2))}
+    path = str(tmp_path / "model.nwc")
+    nwc.save(path, blobs)
+    back = nwc.load(path)
+    assert back == blobs
+    raw = bytearray(open(path, "rb").read())
+    raw[60] ^= 0xFF  # byte 28 of the first blob: its block count
+    open(path, "wb").write(bytes(raw))
+    with pytest.raises(nwc.NwcError):
+        nwc.load(path)

@@ -151,6 +151,21 @@ def test_escape_list_mismatch_is_flagged_not_faulted():
     assert st == 5 and flags & 1
 
 
+def test_matmul_batch_via_decode_and_cublas():
+    """Batch > 1 (prefill): decode to BF16, then cuBLAS. Output BF16, so each entry is checked
+    against the FP64 product with BF16 rounding added to the GEMV bound."""
+    w = synth.normal_bf16((300, 1100), 0.02, seed=41)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    xs = np.stack([synth.activations_bf16(1100, 50 + i) for i in range(5)])
+    y = mat.matmul(dev_bits(xs)).float().cpu().numpy().astype(np.float64)
+    assert_clean()
+    for i in range(5):
+        ref = oracle.gemv(blob, xs[i])
+        scale = oracle.abs_dot(blob, xs[i], np.arange(300))
+        assert (np.abs(y[i] - ref) <= TOL_REL * scale + 2.0 ** -8 * np.abs(ref) + TOL_ABS).all()
+
+
 def test_gemv_repeat_graph_and_stream():
     w = synth.normal_bf16((520, 2600), 0.03, seed=31)
     x = synth.activations_bf16(2600, 32)
