@@ -239,8 +239,8 @@ def extra_workloads(dev, stream, steps):
     del mats, wbf, ys, yb
     torch.cuda.empty_cache()
 
-    # The same stack with fused projections ("fuse(model)" on the NWC page: q|k|v and gate|up
-    # share their input, so each group is one matrix with its rows stacked): 144 GEMVs a token.
+    # The same stack with fused projections (the NWC page's fuse step: q|k|v and gate|up share
+    # their input, so each group is one matrix with its rows stacked): 144 GEMVs a token.
     t0 = time.time()
     mats, ys, wbf = [], [], []
     comp_bytes = 0

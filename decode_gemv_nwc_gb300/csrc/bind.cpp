@@ -1,7 +1,7 @@
 // bind.cpp -- host-side validation of an NWC blob and binding of its device copy.
 //
 // Validation covers everything the kernels trust without checking: header fields, the rank
-// table ("the exponent is ranked by frequency", at most 11 ranked values), the block table,
+// table (exponents ranked by frequency, at most 11 ranked values), the block table,
 // each block region's size, which must equal its 32 lane word counts plus the mantissa
 // regions implied by the block's real rows and columns (fillers carry no mantissa, as the
 // "How it works" section of "NWC -- Neural Weight Compression" states) plus its escape list,

@@ -9,7 +9,7 @@
 //   * a 12-bit peek into a 16 KB shared-memory lookup table yields two complete codes per
 //     step; the bit window is shifted and refilled from the lane's words;
 //   * dequantization and embedding lookup run on the same decoder.
-// Escapes ("escape for rare values"): the stream holds n_ranked ones and the sign, the element's
+// Escapes (the pages' escape for rare exponents): the stream holds n_ranked ones and the sign, the element's
 // bits are in the block's escape list. Every in-stream code thus fits the 12-bit peek and the
 // GEMV's hot loop has no escape branch: it multiplies a placeholder (the sign and raw mantissa
 // with exponent field 0, a subnormal) and the warp adds (true - placeholder) * x for each list
@@ -417,8 +417,8 @@ struct Fs32 {
 };
 
 // Branch-free refill: when at most 32 bits are valid the next word is added right below them
-// by a multiply-add with 2^(32 - valid) (the pages' "refilled with a single wide multiply-add",
-// here as its low and high halves: the bits below the valid ones are zero, so no carry crosses);
+// by a multiply-add with 2^(32 - valid) (the pages refill with one wide multiply-add; here it
+// is split into its low and high halves: the bits below the valid ones are zero, so no carry crosses);
 // otherwise the multiplier is 0. The word was loaded by the previous refill, so the shared-memory
 // latency of the following word's load is off the decode chain.
 __device__ __forceinline__ void fs_refill(Fs32 &s) {
@@ -765,7 +765,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
 }
 
 // =================================================================== decode and gather
-// "Dequantization and embedding lookup (tied lm_head) run on the same decoder": the same CTA
+// The pages run dequantization and the tied lm_head's embedding lookup on the GEMV's decoder;
+// here too: the same CTA
 // layout, table and staged regions as the GEMV. MODE 0 decodes every block to BF16 (fp8: e4m3
 // bytes); MODE 1 writes, for each id, that row of the block row, one block per warp item.
 

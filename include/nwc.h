@@ -130,8 +130,8 @@ nwc_status nwc_validate(const void *blob_host, size_t bytes);
 nwc_status nwc_bind(const void *blob_host, size_t bytes, const void *blob_dev, nwc_matrix *out);
 
 /*
- * nwc_decode -- dequantization to the stored elements, bit-exact ("decompressed weights are
- * bit-exact"): BF16 blobs write uint16 out[n*ld_out + k]; fp8 blobs write the e4m3 bytes
+ * nwc_decode -- dequantization to the stored elements, bit-exact (the NWC page, "How it
+ * works": decoding is lossless): BF16 blobs write uint16 out[n*ld_out + k]; fp8 blobs write the e4m3 bytes
  * (uint8) to out and the row scales to scales_out (fp32[N], may be NULL). ld_out >= K.
  */
 nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *scales_out,
@@ -140,8 +140,9 @@ nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *sca
 /*
  * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 bytes): FP32
  * partial sums per (row, 512-column block) and one counter per 8-row block (both only when
- * K > 512). The 4096-entry decode table ("A 12-bit peek into a 16 KB lookup table in shared
- * memory") is built by every CTA in its own shared memory and needs no workspace.
+ * K > 512). The 4096-entry decode table (the NWC page: a 16 KB shared-memory table indexed by
+ * the next 12 stream bits) is built by every CTA in its own shared memory and needs no
+ * workspace.
  */
 size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
 
@@ -155,7 +156,8 @@ size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
 nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_stream stream);
 
 /*
- * nwc_gemv -- batch-1 y = W x with W decoded in registers ("Fused kernel"): x is BF16[K] (16-byte
+ * nwc_gemv -- batch-1 y = W x with W decoded in registers (the NWC page, "How it works",
+ * fused kernel): x is BF16[K] (16-byte
  * aligned), y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
  * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes: a workspace
  * prepared by nwc_gemv_prepare for this matrix.
@@ -181,8 +183,8 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
 nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
 
 /*
- * nwc_gather -- embedding lookup on the same decoder ("Dequantization and embedding lookup
- * (tied lm_head) run on the same decoder"): out row i = row ids[i] of the stored matrix,
+ * nwc_gather -- embedding lookup on the same decoder (the NWC page, "How it works": the
+ * embedding lookup of a tied lm_head shares the GEMV's decoder): out row i = row ids[i] of the stored matrix,
  * bit-exact (uint16 BF16 or uint8 e4m3), out[i*ld_out + k]. An id outside [0, N) writes a
  * zero row and raises the device error word.
  */

@@ -50,7 +50,7 @@
  *     ranked (rank p < n_ranked): p one-bits, one zero-bit, the sign bit;
  *     escape (v unranked): n_ranked one-bits, the sign bit; the element's exponent
  *     bits (8 BF16 / 4 fp8, with the rest of the element) are in the block's escape
- *     list. (READING: "escape for rare values" with the raw exponent kept outside the
+ *     list. (READING: the pages' escape for rare exponents, with the raw exponent kept outside the
  *     lane stream, so that every in-stream code is at most 12 bits.)
  *     filler (row >= N or col >= K): the rank-0 code with sign 0, i.e. two zero
  *     bits, and no mantissa.
