@@ -336,29 +336,27 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void *src, uint3
 // LUT entry for a 12-bit peek P (first stream bit = bit 11), one code per entry:
 //   bits 0..4   code length L (rank + 2; an escape n_ranked + 1)
 //   bits 5..6   zero (whole entries may be subtracted from the bit counter)
-//   bits 7..15  the code as a BF16 high part (s << 15 | exponent << 7); an escape gets
-//               exponent field 0, the placeholder that the escape list corrects
+//   bits 7..15  BF16: the code as a BF16 high part (s << 15 | exponent << 7);
+//               fp8: s << 15 | v << 11, so that with the 3-bit mantissa at bits 8..10 each
+//               half's high byte is the e4m3 code itself.
+//               An escape gets exponent field 0, the placeholder that the escape list corrects.
 //   bit 24      set for an escape (sums of up to 128 entries stay below it, so a running sum
 //               counts a lane's escapes in its top byte)
-// RAW8 (fp8 decode and gather): s << 15 | v << 11 instead, so that with the mantissa at bits
-// 8..10 each half's high byte is the e4m3 code itself.
-// fp8 exponents e are stored as BF16 exponents e + 120 (exact for normal e4m3 values;
-// subnormals are corrected after assembly). A 12-bit peek holds any code (at most
-// n_ranked + 1 <= 12 bits), which is why at most 11 exponents are ranked.
-template <int ELEM, bool RAW8>
+// A 12-bit peek holds any code (at most n_ranked + 1 <= 12 bits), which is why at most 11
+// exponents are ranked.
+template <int ELEM>
 __device__ __forceinline__ uint32_t lut_entry(uint32_t P, int nr, const uint32_t (&rank4)[3]) {
     const uint32_t bits = P << 20;
     const int ones = __clz(~bits);
     if (ones >= nr) return (1u << 24) | (((bits >> (31 - nr)) & 1u) << 15) | (uint32_t)(nr + 1);
     const uint32_t word = ones < 4 ? rank4[0] : (ones < 8 ? rank4[1] : rank4[2]);
     const uint32_t s = (bits >> (30 - ones)) & 1u, v = (word >> (8 * (ones & 3))) & 0xFFu;
-    if (RAW8) return (s << 15) | (v << 11) | ((uint32_t)ones + 2);
-    return (s << 15) | ((ELEM == 0 ? v : v + 120u) << 7) | ((uint32_t)ones + 2);
+    return (s << 15) | (v << (ELEM == 0 ? 7 : 11)) | ((uint32_t)ones + 2);
 }
 
 // Builds the 4096-entry table in shared memory with all threads of the CTA; the rank table is
 // read from the kernel parameter with static offsets only (packed four values per word).
-template <int ELEM, bool RAW8 = false>
+template <int ELEM>
 __device__ __forceinline__ void build_lut(const Mat &m, uint32_t *lut) {
     uint32_t rank4[3];
 #pragma unroll
@@ -366,7 +364,7 @@ __device__ __forceinline__ void build_lut(const Mat &m, uint32_t *lut) {
         rank4[i] = (uint32_t)m.rank_exp[4 * i] | (uint32_t)m.rank_exp[4 * i + 1] << 8 |
                    (uint32_t)m.rank_exp[4 * i + 2] << 16 | (uint32_t)m.rank_exp[4 * i + 3] << 24;
     for (uint32_t i = threadIdx.x; i < (uint32_t)kLutEntries; i += blockDim.x)
-        lut[i] = lut_entry<ELEM, RAW8>(i, m.nr, rank4);
+        lut[i] = lut_entry<ELEM>(i, m.nr, rank4);
 }
 
 // Pair q's two mantissas (even t at bits 0.., odd t at bits 16..) from a group's words.
@@ -452,16 +450,24 @@ __device__ __forceinline__ uint32_t lut_at(const Fs32 &s, uint32_t lutb) {
     return e;
 }
 
-// fp8 only: an e4m3 subnormal (exponent field 0, stored as BF16 exponent 120) assembled as
-// +-2^-7 (1 + m/8) becomes +-m 2^-9 = (w -+ 2^-7) * 2, exactly.
-__device__ __forceinline__ float fp8_subnormal_fix(float w) {
-    return (w - copysignf(0.0078125f, w)) * 2.0f;
+// fp8: the row pair's two e4m3 codes (the high bytes of the halves) widened exactly to FP32
+// through the hardware e4m3x2 -> f16x2 conversion (subnormals included).
+__device__ __forceinline__ void e4m3_pair_to_f32(uint32_t bf, float &w0, float &w1) {
+    const uint32_t codes = __byte_perm(bf, 0u, 0x0031u);
+    asm("{\n\t.reg .b16 c, l, u;\n\t.reg .b32 h;\n\t"
+        "cvt.u16.u32 c, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, c;\n\t"
+        "mov.b32 {l, u}, h;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, u;\n\t}"
+        : "=f"(w0), "=f"(w1)
+        : "r"(codes));
 }
 
-// One row pair: two single-code lookups, BF16x2 assembly with the raw mantissas. No branch:
-// an escape yields its placeholder, corrected from the block's escape list. Returns the pair as
-// packed BF16 (row r in the low half); fp8 also returns it as FP32 in w0, w1 (with the
-// subnormal fix applied).
+// One row pair: two single-code lookups, assembly with the raw mantissas. No branch: an escape
+// yields its placeholder, corrected from the block's escape list. Returns the pair as packed
+// BF16 (row r in the low half; fp8: each half's high byte is the e4m3 code); fp8 also returns
+// the two values as FP32 in w0, w1.
 template <int ELEM>
 __device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
     fs_refill(s);  // two codes take at most 24 bits; a refill leaves at least 33
@@ -474,11 +480,8 @@ __device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X
     if (ELEM == 0) {
         bf = (e & 0xFF80FF80u) | (X & 0x007F007Fu);
     } else {
-        bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 4);
-        w0 = __uint_as_float(bf << 16);
-        w1 = __uint_as_float(bf & 0xFFFF0000u);
-        if ((bf & 0x7F80u) == (120u << 7)) w0 = fp8_subnormal_fix(w0);
-        if ((bf & 0x7F800000u) == (120u << 23)) w1 = fp8_subnormal_fix(w1);
+        bf = (e & 0xFF80FF80u) | ((X & 0x00070007u) << 8);
+        e4m3_pair_to_f32(bf, w0, w1);
     }
     return bf;
 }
@@ -496,11 +499,13 @@ __device__ __forceinline__ void fma_bf16x2(uint32_t w2, uint32_t x16, float &acc
 }
 
 // Placeholder that the decoders produce for an escaped element with the given bits: its sign
-// and raw mantissa under exponent field 0, as BF16 (the fast path's assembly).
+// and raw mantissa under exponent field 0 (BF16: a subnormal of order 2^-133; fp8: the e4m3
+// subnormal +-m 2^-9).
 template <int ELEM>
 __device__ __forceinline__ float esc_placeholder(uint32_t bits) {
     if (ELEM == 0) return __uint_as_float((bits & 0x807Fu) << 16);
-    return __uint_as_float((((bits & 0x80u) << 8) | ((bits & 7u) << 4)) << 16);
+    const float f = (float)(bits & 7u) * 0.001953125f;
+    return (bits & 0x80u) ? -f : f;
 }
 
 // Adds (w - placeholder) * x to acc[row] for every entry of a block's escape list (`slots`
@@ -989,7 +994,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1)
         if (ok) issue(b);
     }
     load_rank_table(m, rexp);
-    build_lut<ELEM, ELEM == 1>(m, lut);
+    build_lut<ELEM>(m, lut);
     __syncthreads();
 
     while (it < n_items) {
