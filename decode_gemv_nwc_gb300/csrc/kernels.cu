@@ -289,6 +289,7 @@ __device__ __noinline__ bool esc_patch(const uint32_t *esc, uint32_t slots, uint
 #define NWC_GEMV_STAGES 1
 #endif
 constexpr int kGemvWarps = NWC_GEMV_WARPS;
+constexpr int kCtasPerSm = 32 / kGemvWarps;  // 32 warps per SM at 64 registers
 constexpr int kStagesPerWarp = NWC_GEMV_STAGES;
 constexpr int kStageBytes = 6144;
 constexpr int kLutEntries = 4096;
@@ -626,7 +627,7 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes
 }
 
 template <int ELEM>
-__global__ void __launch_bounds__(kGemvWarps * 32, 1)
+__global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, float *partial, uint32_t *counters,
                 uint64_t n_pad) {
     // A kernel launched after this one with programmatic stream serialization may start as soon
@@ -926,7 +927,7 @@ __device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t byte
 }
 
 template <int ELEM, int MODE>
-__global__ void __launch_bounds__(kGemvWarps * 32, 1)
+__global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     unpack_kernel(Mat m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
@@ -1097,7 +1098,8 @@ nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, voi
     static std::once_flag once;
     std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE>, kGemvSmem); });
     if (!smem_ok) return NWC_ERR_CUDA;
-    const int grid = (int)(n_items < (uint64_t)sms ? n_items : (uint64_t)sms);
+    const uint64_t slots = (uint64_t)sms * kCtasPerSm;
+    const int grid = (int)(n_items < slots ? n_items : slots);
     unpack_kernel<ELEM, MODE><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, ids, n_items, out, ld_out, vec);
     return launched();
 }
@@ -1178,7 +1180,8 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     float *partial = reinterpret_cast<float *>(w8);
     uint32_t *counters = reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp));
-    const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
+    const uint64_t slots = (uint64_t)sms * kCtasPerSm;
+    const int grid = (int)(m.nb < slots ? m.nb : slots);
     // Programmatic dependent launch: the kernel may start while the previous kernel on the stream
     // finishes; it streams its first block regions and builds its decode table meanwhile.
     cudaLaunchConfig_t cfg = {};
