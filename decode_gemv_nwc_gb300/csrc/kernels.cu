@@ -538,7 +538,7 @@ __device__ __forceinline__ void esc_correct(const uint32_t *list, uint32_t slots
 // each); the group loop stays rolled so the hot loop fits the instruction cache.
 template <int ELEM>
 __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
-                                           const uint16_t *xb, float (&acc)[8], bool &bad) {
+                                           const uint16_t *xb, uint2 xq, float (&acc)[8], bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
     constexpr int MWG = MW / 4;              // words per group of 4 columns
@@ -566,7 +566,6 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
     }
     const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
     const uint2 *xp = reinterpret_cast<const uint2 *>(xb + lane * kLaneCols);
-    uint2 xq = __ldg(xp);
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
         const uint2 xn = __ldg(xp + (g < 3 ? g + 1 : 3));
@@ -659,13 +658,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         ptr = m.data + 16 * (uint64_t)s;
         bytes = 16 * (e - s);
     };
-    auto issue = [&](uint64_t bb, int which) {
+    // reuse = the stage held an earlier region that this warp read through the generic proxy
+    auto issue = [&](uint64_t bb, int which, bool reuse) {
         const uint8_t *src;
         uint32_t bytes;
         region(bb, src, bytes);
         if (bytes <= (uint32_t)kStageBytes && lane == 0) {
             const uint32_t bar = which ? bar1 : bar0;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (reuse) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_expect_tx(bar, bytes);
             tma_load_1d(smem_u32(which ? stage1 : stage0), src, bytes, bar);
         }
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    if (b < m.nb) issue(b, 0);
+    if (b < m.nb) issue(b, 0, false);
     load_rank_table(m, rexp);
     build_lut<ELEM>(m, lut);
     __syncthreads();
@@ -691,7 +691,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         const uint64_t nxt = b + total_warps;
         __syncwarp();
         if (kStagesPerWarp == 2) {
-            if (nxt < m.nb) issue(nxt, cur ^ 1);
+            if (nxt < m.nb) issue(nxt, cur ^ 1, it > 0);
         } else if (nxt < m.nb && lane == 0) {
             const uint8_t *nsrc;
             uint32_t nbytes;
@@ -705,6 +705,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         region(b, src, bytes);
         const uint8_t *reg = src;
         const bool staged = bytes <= (uint32_t)kStageBytes;
+        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
+        const int rows = real_rows(m.n, rb);
+        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
+        // the fast path's first activations, loaded while the region copy completes
+        uint2 xq0 = make_uint2(0u, 0u);
+        if (interior && staged) xq0 = __ldg(reinterpret_cast<const uint2 *>(x + cb * kCols + lane * kLaneCols));
         if (staged) {
             const uint32_t bar = cur ? bar1 : bar0;
             if (!mbar_wait(bar, (phase >> cur) & 1u)) {
@@ -714,14 +720,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
             phase ^= 1u << cur;
             reg = cur ? stage1 : stage0;
         }
-        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
-        const int rows = real_rows(m.n, rb);
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; r++) acc[r] = 0.0f;
-        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         if (interior && staged) {
-            block_fast<ELEM>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, acc, bad);
+            block_fast<ELEM>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, xq0, acc, bad);
         } else {
             block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + cb * kCols, acc, bad);
         }
@@ -757,7 +760,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         }
         if (kStagesPerWarp == 1) {
             __syncwarp();
-            if (nxt < m.nb) issue(nxt, 0);
+            if (nxt < m.nb) issue(nxt, 0, true);
         }
         b = nxt;
     }
