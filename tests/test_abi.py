@@ -153,3 +153,26 @@ def test_blob_file_round_trip(tmp_path):
     open(path, "wb").write(bytes(raw))
     with pytest.raises(nwc.NwcError):
         nwc.load(path)
+
+
+def test_gpu_entry_points_reject_bad_arguments_before_any_launch():
+    """Argument checks return NWC_ERR_INVALID_ARG before any CUDA call, so they run here with
+    addresses that are never dereferenced."""
+    w = synth.normal_bf16((40, 1100), 0.02, seed=3)
+    st, m = bind_host(nwc.encode(w))
+    assert st == 0
+    L = nwc.lib()
+    mp = ctypes.byref(m)
+    P = ctypes.c_void_p
+    ws = int(L.nwc_gemv_workspace_bytes(mp))
+    assert ws == 512  # partials 3 column blocks x 40 rows x 4 B + 5 counters x 4 B, to 16 B
+    assert L.nwc_gemv(mp, P(0x20002), P(0x30000), P(0x40000), ws, None) == 1   # x not 16-byte aligned
+    assert L.nwc_gemv(mp, P(0x20000), P(0x30000), P(0x40008), ws, None) == 1   # workspace not aligned
+    assert L.nwc_gemv(mp, P(0x20000), P(0x30000), P(0x40000), ws - 16, None) == 1  # workspace too small
+    assert L.nwc_gemv(mp, P(0x20000), None, P(0x40000), ws, None) == 1
+    assert L.nwc_gemv_prepare(mp, P(0x40000), ws - 16, None) == 1
+    assert L.nwc_decode(mp, P(0x50000), 1099, None, None) == 1                  # ld_out < K
+    assert L.nwc_gather(mp, P(0x60000), -1, P(0x50000), 1100, None) == 1
+    assert L.nwc_gather(mp, P(0x60000), 0, P(0x50000), 1100, None) == 0        # nothing to do
+    assert L.nwc_gather(mp, None, 3, P(0x50000), 1100, None) == 1
+    assert L.nwc_gemv_noalloc(None, P(0x20000), P(0x30000), None) == 1
