@@ -6,6 +6,8 @@
 // stream n_ranked ones and the sign; the element's bits go to the block's escape list, so that
 // no in-stream code is longer than 12 bits); every lane of a block of 8 rows x 512 columns has
 // its own bit stream; padding to any shape costs 2 bits per filler weight and no mantissa.
+// Mantissa regions are interleaved word by word across the lanes when all lanes have the same
+// word count (every block whose 512 columns are all inside K).
 // "Qwen3-4B-NWC-fp8": weight-only e4m3, symmetric per-output-channel scale, bytes coded
 // losslessly with the same code (4-bit exponent, 3-bit raw mantissa).
 //
@@ -165,6 +167,11 @@ void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t c
         pos += cs.nw;
     }
     uint8_t *man = dst + up16(32 + 4 * (uint64_t)pos);
+    // all lanes with the same word count: word k of lane l at 32k + l (interleaved)
+    bool uniform = true;
+    for (int l = 1; l < kLanes; l++)
+        uniform &= man_words(rows, real_cols(src.k, cbi, l), cbk.F) == man_words(rows, real_cols(src.k, cbi, 0), cbk.F);
+    uint32_t *man0 = reinterpret_cast<uint32_t *>(man);
     for (int l = 0; l < kLanes; l++) {
         int cols = real_cols(src.k, cbi, l);
         HalfSink ev, od;
@@ -181,7 +188,8 @@ void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t c
         uint32_t *mwp = reinterpret_cast<uint32_t *>(man);
         for (uint32_t i = 0; i < mw; i++) {
             uint32_t lo = (int)i < ev.nh ? ev.h[i] : 0, hi = (int)i < od.nh ? od.h[i] : 0;
-            mwp[i] = lo | (hi << 16);
+            if (uniform) man0[i * kLanes + (uint32_t)l] = lo | (hi << 16);
+            else mwp[i] = lo | (hi << 16);
         }
         man += 4 * mw;
     }

@@ -143,14 +143,15 @@ __device__ __forceinline__ bool decode_one(S &ls, int nr, const uint8_t *rexp, u
     return esc;
 }
 
-// Field j of the even (odd = 0) or odd (odd = 1) mantissa half-stream of a lane region.
+// Field j of the even (odd = 0) or odd (odd = 1) mantissa half-stream of a lane region whose
+// word k is man[k * stride] (stride 32 when the block's lane regions are interleaved).
 template <int F>
-__device__ __forceinline__ uint32_t half_field(const uint32_t *man, int odd, uint32_t j) {
+__device__ __forceinline__ uint32_t half_field(const uint32_t *man, uint32_t stride, int odd, uint32_t j) {
     const uint32_t bit = (uint32_t)F * j, k = bit >> 4, o = bit & 15u;
-    uint32_t w = man[k];
+    uint32_t w = man[k * stride];
     uint32_t h = odd ? (w >> 16) : (w & 0xFFFFu);
     if (o + F > 16) {
-        uint32_t w1 = man[k + 1];
+        uint32_t w1 = man[(k + 1) * stride];
         h |= (odd ? (w1 >> 16) : (w1 & 0xFFFFu)) << 16;
     }
     return (h >> o) & ((1u << F) - 1u);
@@ -178,7 +179,8 @@ __device__ __forceinline__ uint32_t elem_bits(uint32_t s, uint32_t v, uint32_t m
 // fn(c, r, s, v, m, esc) for each real element (column c, row r of the lane). rows/cols are the
 // lane's real extent. Returns the number of escape codes in the lane's 128 codes.
 template <int ELEM, class Fn>
-__device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *man, int rows, int cols, int nr,
+__device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *man, uint32_t stride, int rows,
+                                                int cols, int nr,
                                                 const uint8_t *rexp, Fn &&fn) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     uint32_t je = 0, jo = 0, n_esc = 0;
@@ -191,8 +193,8 @@ __device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *
             n_esc += esc;
             if (r < rows && c < cols) {
                 uint32_t m;
-                if (r & 1) m = half_field<F>(man, 1, jo++);
-                else m = half_field<F>(man, 0, je++);
+                if (r & 1) m = half_field<F>(man, stride, 1, jo++);
+                else m = half_field<F>(man, stride, 0, je++);
                 fn(c, r, s, v, m, esc);
             }
         }
@@ -204,6 +206,7 @@ __device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *
 struct LaneRegion {
     const uint32_t *code, *man, *esc;
     uint32_t nwords, slots;  // slots = escape-list words (entries and padding)
+    uint32_t man_stride;     // 32 when the lanes' mantissa words are interleaved, else 1
 };
 
 __device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, uint32_t bytes, int lane, int rows,
@@ -228,7 +231,9 @@ __device__ __forceinline__ LaneRegion lane_region(const uint8_t *reg, uint32_t b
         if (lane >= d) mincl += o;
     }
     const uint32_t man0 = (uint32_t)up16(32 + 4 * (uint64_t)total);
-    lr.man = reinterpret_cast<const uint32_t *>(reg + man0) + (mincl - mw);
+    const bool uniform = __all_sync(0xFFFFFFFFu, mw == __shfl_sync(0xFFFFFFFFu, mw, 0));
+    lr.man = reinterpret_cast<const uint32_t *>(reg + man0) + (uniform ? (uint32_t)lane : mincl - mw);
+    lr.man_stride = uniform ? (uint32_t)kLanes : 1u;
     const uint32_t esc0 = man0 + 4 * __shfl_sync(0xFFFFFFFFu, mincl, 31);
     lr.esc = reinterpret_cast<const uint32_t *>(reg + esc0);
     lr.slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
@@ -552,7 +557,8 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
     const uint32_t code = regs + 32 + 4 * (incl - lw);
-    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * MW * 4;
+    // interior block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
+    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
     Fs32 s;
     {
         uint32_t w0 = 0, w1 = 0;
@@ -575,7 +581,7 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
                              __uint_as_float(xq.y << 16), __uint_as_float(xq.y & 0xFFFF0000u)};
         uint32_t mw[MWG];
 #pragma unroll
-        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * (MWG * g + i)));
+        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
 #pragma unroll
         for (int q = 0; q < 16; q++) {
             const int pp = q & 3;
@@ -618,7 +624,7 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes
     const uint16_t *xl = xb + lane * kLaneCols;
     LaneStream ls;
     ls.init(lr.code, lr.nwords);
-    lane_rolled<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int c, int r, uint32_t s, uint32_t v, uint32_t mm, bool esc) {
+    lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, [&](int c, int r, uint32_t s, uint32_t v, uint32_t mm, bool esc) {
         const float w = esc ? esc_placeholder<ELEM>(elem_bits<ELEM>(s, 0, mm)) : elem_value<ELEM>(s, v, mm);
         acc[r] = fmaf(w, __uint_as_float((uint32_t)__ldg(xl + c) << 16), acc[r]);
     });
@@ -848,7 +854,8 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
     const uint32_t code = regs + 32 + 4 * (incl - lw);
-    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * MW * 4;
+    // interior block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
+    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
     Fs32 s;
     {
         uint32_t w0 = 0, w1 = 0;
@@ -868,7 +875,7 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     for (int g = 0; g < 4; g++) {
         uint32_t mw[MWG];
 #pragma unroll
-        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * (MWG * g + i)));
+        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
         uint32_t p[16];  // p[c4 * 4 + pp]: rows (2pp, 2pp + 1) at column 4g + c4
 #pragma unroll
         for (int q = 0; q < 16; q++) p[q] = unpack_pair<ELEM>(s, lutb, xpair<F>(mw, q), flags);
@@ -915,7 +922,7 @@ __device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t byte
     LaneStream ls;
     ls.init(lr.code, lr.nwords);
     const uint32_t n_esc =
-        lane_rolled<ELEM>(ls, lr.man, rows, cols, nr, rexp, [&](int c, int r, uint32_t sg, uint32_t v, uint32_t mm, bool esc) {
+        lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, [&](int c, int r, uint32_t sg, uint32_t v, uint32_t mm, bool esc) {
             if (MODE == 1 && r != want) return;
             const uint64_t row = MODE == 0 ? row0 + (uint64_t)r : row0;
             const uint32_t e = elem_bits<ELEM>(sg, esc ? 0u : v, mm);

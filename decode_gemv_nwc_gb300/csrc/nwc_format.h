@@ -5,7 +5,9 @@
 // from the data section), fp32 row scales (fp8 only), then one region per 8x512 block in
 // row-block-major order: u8 lane_words[32] | 32 code streams (u32 words, most significant bit
 // first) | zero pad to 16 B | 32 mantissa regions (even-t half-stream in the low halves, odd-t
-// half-stream in the high halves, F-bit fields least significant bit first, 16-byte multiple) |
+// half-stream in the high halves, F-bit fields least significant bit first, 16-byte multiple;
+// when all lanes have the same word count W, word k of lane l is word 32k + l of the section,
+// otherwise the regions follow one another) |
 // escape list (u32 t | lane << 7 | element bits << 12 per escaped element, lanes in order, t
 // increasing, padded to 16 B with kEscPad). An escape code in a lane stream is n_ranked ones and
 // the sign; the escaped element's exponent (with the rest of its bits) is in the list.
@@ -21,7 +23,7 @@
 namespace nwcf {
 
 constexpr uint32_t kMagic = 0x3143574Eu;  // "NWC1"
-constexpr uint32_t kVersion = 2;
+constexpr uint32_t kVersion = 3;
 constexpr int kRows = 8, kCols = 512, kLanes = 32, kLaneCols = 16, kSyms = 128;
 constexpr int kMaxRanked = 11;
 constexpr int kMaxLaneWords = 48;  // 128 codes x 12 bits / 32

@@ -21,7 +21,7 @@
  *
  * FORMAT (little-endian):
  *   header, 64 bytes
- *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 2
+ *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 3
  *     6  u8  elem (0 = BF16, 1 = FP8 e4m3)  7  u8  n_ranked (1..11)
  *     8  u64 N    16 u64 K    24 u64 n_blocks = ceil(N/8) * ceil(K/512)
  *     32 u64 off_blocks   40 u64 off_scales (0 for BF16)   48 u64 off_data
@@ -67,6 +67,10 @@
  *     rounded up to a multiple of 4. (READING: bit packed, so that the raw plane
  *     costs F bits per element; even/odd halves so that the two mantissas of a row
  *     pair sit 16 bits apart.)
+ *   Mantissa regions of a block: when all 32 lanes have the same word count W, word k of
+ *     lane l is word 32k + l of the block's mantissa section (interleaved, so that the 32
+ *     lanes reading their word k touch 32 consecutive words); otherwise the lanes' regions
+ *     follow one another, lane 0 first. (READING: a layout choice with no size cost.)
  *   FP8 quantization of row n (READING of [P2]): a = max_k |w[n,k]| in FP32;
  *     s_n = a / 448 in FP32 (s_n = 1 when a = 0); q = e4m3 nearest to
  *     fp32(w) / s_n (FP32 division), ties to even, saturating at +-448.
@@ -80,7 +84,7 @@
 #include <string.h>
 
 #define ORC_MAGIC 0x3143574Eu
-#define ORC_VERSION 2
+#define ORC_VERSION 3
 #define ORC_R 11
 #define ORC_ROWS 8
 #define ORC_COLS 512
@@ -251,9 +255,14 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
             for (uint64_t i = 0; i < nw; i++, pos += 4) put_u32(r + pos, code[l].w[i]);
         }
         pos = pad16(pos);
+        int uniform = 1;
+        for (int l = 1; l < ORC_LANES; l++) uniform &= man_words[l] == man_words[0];
+        uint64_t man0 = pos;
         for (int l = 0; l < ORC_LANES; l++) {
-            for (uint64_t k = 0; k < man_words[l]; k++, pos += 4)
-                put_u32(r + pos, (uint32_t)even[l].h[k] | ((uint32_t)odd[l].h[k] << 16));
+            for (uint64_t k = 0; k < man_words[l]; k++, pos += 4) {
+                uint64_t at = uniform ? man0 + 4 * (k * ORC_LANES + (uint64_t)l) : pos;
+                put_u32(r + at, (uint32_t)even[l].h[k] | ((uint32_t)odd[l].h[k] << 16));
+            }
         }
         for (uint64_t i = 0; esc_at + 4 * i < len; i++)
             put_u32(r + esc_at + 4 * i, i < n_esc ? esc[i] : 0xFFFFFFFFu);
@@ -339,11 +348,13 @@ static uint32_t br_get(bitr *b) {
     return (get_u32(b->p + 4 * word) >> bitpos) & 1;
 }
 
-static uint32_t half_field(const uint8_t *region, int odd, uint64_t j, int F) {
+/* field j of a lane's even (odd = 0) or odd half-stream; the lane's word k is at
+   region + 4 * k * stride */
+static uint32_t half_field(const uint8_t *region, uint64_t stride, int odd, uint64_t j, int F) {
     uint32_t v = 0;
     for (int i = 0; i < F; i++) {
         uint64_t bit = (uint64_t)F * j + (uint64_t)i;
-        uint32_t word = get_u32(region + 4 * (bit / 16));
+        uint32_t word = get_u32(region + 4 * (bit / 16) * stride);
         uint32_t half = odd ? (word >> 16) : (word & 0xFFFF);
         v |= ((half >> (bit % 16)) & 1u) << i;
     }
@@ -370,7 +381,7 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
     int F = man_bits(h->elem);
     int ok = 0;
     /* the mantissa regions' sizes follow from the real extents; the escape list follows them */
-    uint64_t man_at = pos, esc_at = pos;
+    uint64_t man_at = pos, esc_at = pos, mwords[ORC_LANES];
     for (int l = 0; l < ORC_LANES; l++) {
         uint64_t n_even = 0, n_odd = 0;
         for (int t = 0; t < ORC_SYMS; t++) {
@@ -379,8 +390,11 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
             if (row < h->N && col < h->K) { if (t % 2 == 0) n_even++; else n_odd++; }
         }
         uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
-        esc_at += 4 * (ceil_div(ceil_div(bits, 16), 4) * 4);
+        mwords[l] = ceil_div(ceil_div(bits, 16), 4) * 4;
+        esc_at += 4 * mwords[l];
     }
+    int uniform = 1;
+    for (int l = 1; l < ORC_LANES; l++) uniform &= mwords[l] == mwords[0];
     if (start + esc_at > end) return -1;
     static uint32_t esc_value[ORC_LANES][ORC_SYMS];
     static int esc_seen[ORC_LANES][ORC_SYMS];
@@ -412,11 +426,12 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
         if (br.bad) ok = -1;
         uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
         uint64_t words = ceil_div(ceil_div(bits, 16), 4) * 4;
-        const uint8_t *man = reg + pos;
+        const uint8_t *man = uniform ? reg + man_at + 4 * (uint64_t)l : reg + pos;
+        uint64_t stride = uniform ? ORC_LANES : 1;
         uint64_t je = 0, jo = 0;
         for (int t = 0; t < ORC_SYMS; t++) {
             if (!real[t]) continue;
-            uint32_t m = (t % 2 == 0) ? half_field(man, 0, je++, F) : half_field(man, 1, jo++, F);
+            uint32_t m = (t % 2 == 0) ? half_field(man, stride, 0, je++, F) : half_field(man, stride, 1, jo++, F);
             uint32_t value = join(h->elem, sv[t], vv[t], m);
             if (escaped[t]) {
                 if (!esc_seen[l][t]) return -1;

@@ -131,6 +131,41 @@ def test_roundtrip_random_shapes(shape):
     assert np.array_equal(lane_words(blob), -(-bits // 32))
 
 
+def test_mantissas_interleaved_when_lanes_agree():
+    """A full block (every lane 28 words): word k of lane l is word 32k + l of the mantissa
+    section. The ragged block (columns 512..599) keeps the lanes' regions one after another.
+    Reading the fields back that way gives every element's raw 7-bit mantissa."""
+    K = 600
+    w = synth.normal_bf16((8, K), 0.02, seed=13)
+    blob = oracle.encode(w)
+    h = hdr(blob)
+    b = np.frombuffer(blob, np.uint8)
+    tab = b[h["off_blocks"]:h["off_blocks"] + 4 * (h["nb"] + 1)].view(np.uint32)
+    for cb in range(2):
+        start = h["off_data"] + 16 * int(tab[cb])
+        lw = b[start:start + 32].astype(np.int64)
+        man0 = start + -(-(32 + 4 * int(lw.sum())) // 16) * 16
+        cols = [min(16, max(0, K - 512 * cb - 16 * l)) for l in range(32)]
+        mw = [-(-(-(-7 * c * 4 // 16)) // 4) * 4 for c in cols]
+        uniform = len(set(mw)) == 1
+        assert uniform == (cb == 0)
+        words = b[man0:man0 + 4 * sum(mw)].view(np.uint32)
+        off = 0
+        for l in range(32):
+            lane_words = [int(words[32 * j + l]) if uniform else int(words[off + j]) for j in range(mw[l])]
+            off += mw[l]
+            for half, rows in ((0, (0, 2, 4, 6)), (1, (1, 3, 5, 7))):
+                stream = 0
+                for j, wd in enumerate(lane_words):
+                    stream |= ((wd >> (16 * half)) & 0xFFFF) << (16 * j)
+                jfield = 0
+                for c in range(cols[l]):
+                    for r in rows:
+                        m = (stream >> (7 * jfield)) & 0x7F
+                        assert m == int(w[r, 512 * cb + 16 * l + c]) & 0x7F
+                        jfield += 1
+
+
 def test_filler_costs_two_bits_and_no_mantissa():
     """A 1x1 matrix: lanes 1..31 hold 128 fillers = 256 bits = 8 words; the
     only mantissa region is lane 0's 16 bytes."""
