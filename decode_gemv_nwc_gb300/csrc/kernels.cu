@@ -305,6 +305,16 @@ constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
 constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes;
 static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
 static_assert(kGemvSmem <= 232448, "shared memory per CTA");
+// Decode: 16 warps per SM with up to 128 registers each, so that a lane holds its whole 8x16
+// output tile and writes every 32-byte row segment with full-sector stores. Gather keeps one
+// row per lane and runs 32 warps.
+template <int MODE>
+struct UnpackCfg {
+    static constexpr int kWarps = MODE == 0 ? 16 : kGemvWarps;
+    static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
+    static constexpr int kSmem = kStageOff + kWarps * kStageBytes;
+};
+static_assert(UnpackCfg<0>::kSmem <= 232448 && UnpackCfg<1>::kSmem <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -812,25 +822,26 @@ __device__ __forceinline__ uint2 row_words(uint32_t a, uint32_t b, uint32_t c, u
     return make_uint2(__byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410), 0u);
 }
 
+// One lane's 16-column row segment (BF16: 8 words, fp8: 4 words) to out[at ..]: two (one)
+// 16-byte stores when vec (out and the row stride keep 16-byte alignment), else element-wise.
 template <int ELEM>
-__device__ __forceinline__ void store_row4(void *out, uint64_t at, uint2 w, bool vec) {
+__device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32_t (&w)[8], bool vec) {
     if (ELEM == 0) {
         uint16_t *o = static_cast<uint16_t *>(out) + at;
         if (vec) {
-            *reinterpret_cast<uint2 *>(o) = w;
+            reinterpret_cast<uint4 *>(o)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4 *>(o)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         } else {
-            o[0] = (uint16_t)w.x;
-            o[1] = (uint16_t)(w.x >> 16);
-            o[2] = (uint16_t)w.y;
-            o[3] = (uint16_t)(w.y >> 16);
+#pragma unroll
+            for (int i = 0; i < 16; i++) o[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
         }
     } else {
         uint8_t *o = static_cast<uint8_t *>(out) + at;
         if (vec) {
-            *reinterpret_cast<uint32_t *>(o) = w.x;
+            *reinterpret_cast<uint4 *>(o) = make_uint4(w[0], w[1], w[2], w[3]);
         } else {
 #pragma unroll
-            for (int i = 0; i < 4; i++) o[i] = (uint8_t)(w.x >> (8 * i));
+            for (int i = 0; i < 16; i++) o[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
         }
     }
 }
@@ -871,29 +882,60 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     uint32_t flags = 0;
     const int wpp = want >> 1;
     const bool whi = want & 1;
-#pragma unroll 1
-    for (int g = 0; g < 4; g++) {
+    // the lane's output tile: o[r][k] = row r, words k (BF16: 2 columns a word, fp8: 4)
+    uint32_t o[MODE == 0 ? 8 : 1][8];
+    auto group = [&](int g) {
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
         uint32_t p[16];  // p[c4 * 4 + pp]: rows (2pp, 2pp + 1) at column 4g + c4
 #pragma unroll
         for (int q = 0; q < 16; q++) p[q] = unpack_pair<ELEM>(s, lutb, xpair<F>(mw, q), flags);
-        const uint64_t c = col0 + 4 * (uint64_t)g;
-        if (MODE == 0) {
+        if (MODE == 0) {  // g static here (unrolled)
 #pragma unroll
             for (int pp = 0; pp < 4; pp++) {
-                const uint64_t r = row0 + 2 * (uint64_t)pp;
-                store_row4<ELEM>(out, r * (uint64_t)ld_out + c, row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], false), vec);
-                store_row4<ELEM>(out, (r + 1) * (uint64_t)ld_out + c, row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], true), vec);
+                const uint2 lo = row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], false);
+                const uint2 hi = row_words<ELEM>(p[pp], p[4 + pp], p[8 + pp], p[12 + pp], true);
+                if (ELEM == 0) {
+                    o[2 * pp][2 * g] = lo.x;
+                    o[2 * pp][2 * g + 1] = lo.y;
+                    o[2 * pp + 1][2 * g] = hi.x;
+                    o[2 * pp + 1][2 * g + 1] = hi.y;
+                } else {
+                    o[2 * pp][g] = lo.x;
+                    o[2 * pp + 1][g] = hi.x;
+                }
             }
-        } else {
+        } else {  // g dynamic: the wanted row's words shift in from the top
             uint32_t v[4];
 #pragma unroll
             for (int c4 = 0; c4 < 4; c4++)
                 v[c4] = wpp == 0 ? p[c4 * 4] : (wpp == 1 ? p[c4 * 4 + 1] : (wpp == 2 ? p[c4 * 4 + 2] : p[c4 * 4 + 3]));
-            store_row4<ELEM>(out, row0 * (uint64_t)ld_out + c, row_words<ELEM>(v[0], v[1], v[2], v[3], whi), vec);
+            const uint2 wd = row_words<ELEM>(v[0], v[1], v[2], v[3], whi);
+            if (ELEM == 0) {
+#pragma unroll
+                for (int i = 0; i < 6; i++) o[0][i] = o[0][i + 2];
+                o[0][6] = wd.x;
+                o[0][7] = wd.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 3; i++) o[0][i] = o[0][i + 1];
+                o[0][3] = wd.x;
+            }
         }
+    };
+    if (MODE == 0) {
+#pragma unroll
+        for (int g = 0; g < 4; g++) group(g);
+    } else {
+#pragma unroll 1
+        for (int g = 0; g < 4; g++) group(g);
+    }
+    if (MODE == 0) {
+#pragma unroll
+        for (int r = 0; r < 8; r++) store_row16<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], vec);
+    } else {
+        store_row16<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], vec);
     }
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
@@ -937,15 +979,15 @@ __device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t byte
 }
 
 template <int ELEM, int MODE>
-__global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
+__global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
     unpack_kernel(Mat m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint8_t *rexp = smem + kRexpOff;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16);
-    uint8_t *stage = smem + kStageOff + warp * kStagesPerWarp * kStageBytes;
-    const uint64_t stride = (uint64_t)gridDim.x * kGemvWarps;
+    uint8_t *stage = smem + UnpackCfg<MODE>::kStageOff + warp * kStageBytes;
+    const uint64_t stride = (uint64_t)gridDim.x * UnpackCfg<MODE>::kWarps;
     uint32_t phase = 0;
     bool bad = false, timed_out = false;
 
@@ -1106,18 +1148,19 @@ nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, voi
     if (sms <= 0) return NWC_ERR_CUDA;
     static bool smem_ok = false;
     static std::once_flag once;
-    std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE>, kGemvSmem); });
+    using C = UnpackCfg<MODE>;
+    std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE>, C::kSmem); });
     if (!smem_ok) return NWC_ERR_CUDA;
-    const uint64_t slots = (uint64_t)sms * kCtasPerSm;
-    const int grid = (int)(n_items < slots ? n_items : slots);
-    unpack_kernel<ELEM, MODE><<<grid, kGemvWarps * 32, kGemvSmem, s>>>(m, ids, n_items, out, ld_out, vec);
+    const int grid = (int)(n_items < (uint64_t)sms ? n_items : (uint64_t)sms);
+    unpack_kernel<ELEM, MODE><<<grid, C::kWarps * 32, C::kSmem, s>>>(m, ids, n_items, out, ld_out, vec);
     return launched();
 }
 
-// Row stores of 4 columns are vectorised when every row start keeps their alignment.
+// A lane's 16-column row segment is stored with 16-byte stores when every row start keeps that
+// alignment.
 int vec_ok(const void *out, int64_t ld_out, int elem) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(out);
-    return elem == NWC_ELEM_BF16 ? ((a % 8) == 0 && (ld_out % 4) == 0) : ((a % 4) == 0 && (ld_out % 4) == 0);
+    return elem == NWC_ELEM_BF16 ? ((a % 16) == 0 && (ld_out % 8) == 0) : ((a % 16) == 0 && (ld_out % 16) == 0);
 }
 
 }  // namespace
