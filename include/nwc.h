@@ -133,6 +133,9 @@ nwc_status nwc_bind(const void *blob_host, size_t bytes, const void *blob_dev, n
  * nwc_decode -- dequantization to the stored elements, bit-exact (the NWC page, "How it
  * works": decoding is lossless): BF16 blobs write uint16 out[n*ld_out + k]; fp8 blobs write the e4m3 bytes
  * (uint8) to out and the row scales to scales_out (fp32[N], may be NULL). ld_out >= K.
+ * Rows are written 16 columns at a time with 16-byte stores when out is 16-byte aligned and
+ * ld_out is a multiple of 8 (BF16) or 16 (fp8); any other out or ld_out is written element by
+ * element (correct, slower).
  */
 nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *scales_out,
                       nwc_stream stream);
@@ -186,7 +189,9 @@ nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nw
  * nwc_gather -- embedding lookup on the same decoder (the NWC page, "How it works": the
  * embedding lookup of a tied lm_head shares the GEMV's decoder): out row i = row ids[i] of the stored matrix,
  * bit-exact (uint16 BF16 or uint8 e4m3), out[i*ld_out + k]. An id outside [0, N) writes a
- * zero row and raises the device error word.
+ * zero row and raises the device error word. Every id decodes its whole 8-row block row (the
+ * format's unit), so a gather costs about 8x the bytes of the rows it returns. Store alignment
+ * as for nwc_decode.
  */
 nwc_status nwc_gather(const nwc_matrix *m, const int32_t *ids, int64_t n_ids, void *out,
                       int64_t ld_out, nwc_stream stream);
