@@ -207,6 +207,23 @@ def test_fp8_decode_and_gemv(shape):
     gemv_check(blob, x, rows=rows, mat=mat)
 
 
+@pytest.mark.parametrize("name", [s[0] for s in synth.LAYER_SHAPES])
+def test_decoder_stack_matrices_full_size(name):
+    """Each matrix of the 36-layer stack's first layer at full size (BF16, per-layer sigma):
+    decode bit-exact, GEMV within tolerance on 384 sampled rows (the shapes the benchmark
+    times)."""
+    w = synth.layer_matrix(0, name)  # BF16 bits, numpy uint16
+    n, k = w.shape
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    out = mat.decode().cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, w)
+    x = synth.activations_bf16(k, 2000 + k)
+    rows = np.sort(np.random.default_rng(n + k).choice(n, 384, False))
+    gemv_check(blob, x, rows=rows, mat=mat)
+
+
 def test_fp8_subnormal_and_zero_codes():
     rng = np.random.default_rng(8)
     q = rng.integers(0, 256, size=(16, 1024)).astype(np.uint8)
