@@ -132,7 +132,7 @@ extern "C" const char *nwc_status_str(nwc_status s) {
     return "unknown status";
 }
 
-extern "C" const char *nwc_version(void) { return "nwc 2 (format 2, sm_103a)"; }
+extern "C" const char *nwc_version(void) { return "nwc 3 (format 3, sm_103a)"; }
 
 extern "C" nwc_status nwc_validate(const void *blob_host, size_t bytes) {
     Parsed p;

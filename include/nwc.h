@@ -80,7 +80,7 @@ typedef struct nwc_matrix {
 /* Human-readable name of a status code (static string). */
 const char *nwc_status_str(nwc_status s);
 
-/* Library version string, e.g. "nwc 2 (format 2, sm_103a)". */
+/* Library version string, e.g. "nwc 3 (format 3, sm_103a)". */
 const char *nwc_version(void);
 
 /*
