@@ -9,6 +9,7 @@
 // order without repeats, with an unranked exponent, followed by fewer than four padding words.
 // Lane stream contents are checked on the device while decoding.
 #include <cstring>
+#include <string>
 
 #include "nwc.h"
 #include "nwc_format.h"
@@ -132,7 +133,10 @@ extern "C" const char *nwc_status_str(nwc_status s) {
     return "unknown status";
 }
 
-extern "C" const char *nwc_version(void) { return "nwc 3 (format 3, sm_103a)"; }
+extern "C" const char *nwc_version(void) {
+    static const std::string v = "nwc " + std::to_string(kVersion) + " (format " + std::to_string(kVersion) + ", sm_103a)";
+    return v.c_str();
+}
 
 extern "C" nwc_status nwc_validate(const void *blob_host, size_t bytes) {
     Parsed p;
