@@ -294,7 +294,7 @@ __device__ __noinline__ bool esc_patch(const uint32_t *esc, uint32_t slots, uint
 #define NWC_GEMV_STAGES 1
 #endif
 constexpr int kGemvWarps = NWC_GEMV_WARPS;
-constexpr int kCtasPerSm = 32 / kGemvWarps;  // 32 warps per SM at 64 registers
+
 constexpr int kStagesPerWarp = NWC_GEMV_STAGES;
 constexpr int kStageBytes = 6144;
 constexpr int kLutEntries = 4096;
@@ -305,6 +305,11 @@ constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
 constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes;
 static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
 static_assert(kGemvSmem <= 232448, "shared memory per CTA");
+// CTAs per SM: 32 warps at 64 registers, and what 228 KB of shared memory holds (1 KB of it
+// reserved per CTA)
+constexpr int kCtasPerSm = (32 / kGemvWarps) < (233472 / (kGemvSmem + 1024)) ? (32 / kGemvWarps)
+                                                                               : (233472 / (kGemvSmem + 1024));
+static_assert(kCtasPerSm >= 1, "one CTA per SM at least");
 // Decode: 16 warps per SM with up to 128 registers each, so that a lane holds its whole 8x16
 // output tile and writes every 32-byte row segment with full-sector stores. Gather keeps one
 // row per lane and runs 32 warps.
