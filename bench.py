@@ -263,7 +263,32 @@ def extra_workloads(dev, stream, steps):
         "gemvs": len(mats), "us_per_token": tok_ms * 1e3, "compressed_bytes": comp_bytes,
         "compressed_gbs": comp_bytes / (tok_ms * 1e-3) / 1e9, "frac_of_measured_hbm": comp_bytes / (tok_ms * 1e-3) / 1e9 / peak,
         "bf16_cublas_us_per_token": tok_bf16 * 1e3, "speedup_vs_bf16": tok_bf16 / tok_ms, "build_seconds": build_s}
-    del mats, wbf, ys, yb
+
+    # Small-batch decoding on the fused stack: nb tokens per step through nwc_gemv_batch (each
+    # weight decoded once for all nb vectors), against cuBLAS on the BF16 weights.
+    xbat = {k: torch.from_numpy(np.stack([synth.activations_bf16(k, 3000 + k + v) for v in range(8)])
+                                .view(np.int16)).to(dev) for k in {m.k for m in mats}}
+    for nb in (2, 4, 8):
+        yB = [torch.empty((nb, m.n), dtype=torch.float32, device=dev) for m in mats]
+        ybB = [torch.empty((nb, m.n), dtype=torch.bfloat16, device=dev) for m in mats]
+
+        def stack_batch():
+            for m, y in zip(mats, yB):
+                m.gemv_batch(xbat[m.k][:nb], y=y, stream=stream)
+
+        def stack_batch_bf16():
+            for w, y in zip(wbf, ybB):
+                torch.mm(xbat[w.shape[1]][:nb].view(torch.bfloat16), w.t(), out=y)
+        b_ms = time_graph(stack_batch, stream, max(3, steps // 2))
+        b_bf16 = time_graph(stack_batch_bf16, stream, max(3, steps // 2))
+        out[f"stack_fused_batch{nb}"] = {
+            "workload": f"36-layer fused stack, {nb} tokens per step (one fused GEMV per matrix for all {nb})",
+            "us_per_step": b_ms * 1e3, "tokens_per_s": nb / (b_ms * 1e-3),
+            "compressed_gbs": comp_bytes / (b_ms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": comp_bytes / (b_ms * 1e-3) / 1e9 / peak,
+            "bf16_cublas_us_per_step": b_bf16 * 1e3, "speedup_vs_bf16": b_bf16 / b_ms}
+        del yB, ybB
+    del mats, wbf, ys, yb, xbat
     torch.cuda.empty_cache()
 
     # tied embedding / lm_head 151936 x 2560: gather 4096 ids, then the lm_head GEMV

@@ -67,11 +67,16 @@ def lib():
     L.nwc_gemv_prepare.argtypes = [ctypes.POINTER(NwcMatrix), p, sz, p]
     L.nwc_gemv.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, p]
     L.nwc_gemv_noalloc.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p]
+    L.nwc_gemv_batch_workspace_bytes.argtypes = [ctypes.POINTER(NwcMatrix), i32]
+    L.nwc_gemv_batch_workspace_bytes.restype = sz
+    L.nwc_gemv_batch_prepare.argtypes = [ctypes.POINTER(NwcMatrix), i32, p, sz, p]
+    L.nwc_gemv_batch.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, i32, p, i64, p, sz, p]
     L.nwc_gather.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, i64, p]
     L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
     L.nwc_sm_count.restype = i32
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
-                 "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gather", "nwc_check"):
+                 "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gemv_batch_prepare",
+                 "nwc_gemv_batch", "nwc_gather", "nwc_check"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -181,6 +186,25 @@ class Matrix:
         _ok(lib().nwc_gemv(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
                            ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes,
                            _stream_ptr(stream)), "nwc_gemv")
+        return y
+
+    def gemv_batch(self, x, y=None, stream=None):
+        """Y (float32[nb, N]) = W x[v] for the nb <= 8 rows of x (BF16 [nb, K] as an int16/bfloat16
+        CUDA tensor, row stride a multiple of 8): one fused pass that decodes every weight once.
+        The batch workspace (sized for 8 vectors) is allocated and prepared on first use."""
+        import torch
+        assert x.dim() == 2 and x.shape[1] == self.k and x.is_cuda and x.stride(1) == 1
+        nb = x.shape[0]
+        if y is None:
+            y = torch.empty((nb, self.n), dtype=torch.float32, device=x.device)
+        if getattr(self, "_bws", None) is None:
+            bws = int(lib().nwc_gemv_batch_workspace_bytes(ctypes.byref(self.m), 8))
+            self._bws = torch.empty(bws, dtype=torch.uint8, device=self.device_blob.device)
+            _ok(lib().nwc_gemv_batch_prepare(ctypes.byref(self.m), 8, ctypes.c_void_p(self._bws.data_ptr()), bws,
+                                             _stream_ptr(stream)), "nwc_gemv_batch_prepare")
+        _ok(lib().nwc_gemv_batch(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), x.stride(0), nb,
+                                 ctypes.c_void_p(y.data_ptr()), y.stride(0), ctypes.c_void_p(self._bws.data_ptr()),
+                                 self._bws.numel(), _stream_ptr(stream)), "nwc_gemv_batch")
         return y
 
     def decode(self, out=None, stream=None):

@@ -794,6 +794,281 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     if (bad) raise_error(kErrFormat);
 }
 
+// =================================================================== small-batch GEMV
+// Y[v] = W x[v] for up to 8 activation vectors ("batch > 1" without leaving the fused kernel):
+// each weight is decoded once and multiplied into every vector, NB accumulators per row. One
+// CTA per SM of 16 warps (12 for NB = 8, whose 64 accumulators need more registers); otherwise
+// as the single-vector GEMV (staged regions,
+// shared table, escape-list corrections, ticket reduction per row block, programmatic launch).
+template <int NB>
+struct BatchCfg {
+    static constexpr int kWarps = NB <= 4 ? 16 : 12;  // 128 or 168 registers per thread
+    static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
+    static constexpr int kSmem = kStageOff + kWarps * kStageBytes;
+};
+static_assert(BatchCfg<2>::kSmem <= 232448 && BatchCfg<8>::kSmem <= 232448, "shared memory per CTA");
+
+// acc0 += lo(w2) * x, acc1 += hi(w2) * x with x the low (HI = false) or high half of xw.
+template <bool HI>
+__device__ __forceinline__ void fma_bf16x2_half(uint32_t w2, uint32_t xw, float &acc0, float &acc1) {
+    if (HI)
+        asm("{\n\t.reg .b16 lo, hi, xl, xh;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "mov.b32 {xl, xh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, lo, xh, %0;\n\t"
+            "fma.rn.f32.bf16 %1, hi, xh, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1)
+            : "r"(w2), "r"(xw));
+    else
+        asm("{\n\t.reg .b16 lo, hi, xl, xh;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "mov.b32 {xl, xh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, lo, xl, %0;\n\t"
+            "fma.rn.f32.bf16 %1, hi, xl, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1)
+            : "r"(w2), "r"(xw));
+}
+
+// The escape-list corrections of esc_correct, for every vector.
+template <int ELEM, int NB>
+__device__ __forceinline__ void esc_correct_batch(const uint32_t *list, uint32_t slots, int lane, const uint16_t *xb,
+                                                  int64_t ld_x, int nb, int rows, int kc, float (&acc)[8][NB],
+                                                  bool &bad) {
+    for (uint32_t j = (uint32_t)lane; j < slots; j += 32) {
+        const uint32_t e = list[j];
+        if (e == kEscPad) continue;
+        const uint32_t t = esc_t(e), bits = esc_bits(e);
+        const int r = (int)(t & 7u), c = (int)esc_lane(e) * kLaneCols + (int)(t >> 3);
+        if (r >= rows || c >= kc) {
+            bad = true;
+            continue;
+        }
+        const float w = ELEM == 0 ? __uint_as_float(bits << 16) : elem_value<1>(bits >> 7, (bits >> 3) & 15u, bits & 7u);
+        const float ph = esc_placeholder<ELEM>(bits);
+#pragma unroll
+        for (int v = 0; v < NB; v++) {
+            if (v >= nb) break;
+            const float xv = __uint_as_float((uint32_t)__ldg(xb + (int64_t)v * ld_x + c) << 16);
+            const float d = fmaf(w, xv, -(ph * xv));
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                if (i == r) acc[i][v] += d;
+        }
+    }
+}
+
+// Interior block from its staged region, NB vectors (the first nb real).
+template <int ELEM, int NB>
+__device__ __forceinline__ void block_fast_batch(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
+                                                 const uint16_t *xb, int64_t ld_x, int nb, float (&acc)[8][NB],
+                                                 bool &bad) {
+    constexpr int F = ELEM == 0 ? 7 : 3;
+    constexpr int MW = ELEM == 0 ? 28 : 12;
+    constexpr int MWG = MW / 4;
+    const uint32_t lw = reg[lane];
+    uint32_t incl = lw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
+    const uint32_t code = regs + 32 + 4 * (incl - lw);
+    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
+    Fs32 s;
+    {
+        uint32_t w0 = 0, w1 = 0;
+        if (lw > 0) asm("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(code));
+        if (lw > 1) asm("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(code + 4));
+        s.wh = w0;
+        s.wl = w1;
+        s.pa = code + 8;
+        s.V = 63u;
+        asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
+    }
+    const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
+#pragma unroll 1
+    for (int g = 0; g < 4; g++) {
+        uint2 xq[NB];  // the group's four activations of each vector (BF16 pairs)
+#pragma unroll
+        for (int v = 0; v < NB; v++)
+            xq[v] = v < nb ? __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)v * ld_x + lane * kLaneCols) + g)
+                           : make_uint2(0u, 0u);
+        uint32_t mw[MWG];
+#pragma unroll
+        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+#pragma unroll
+        for (int q = 0; q < 16; q++) {
+            const int pp = q & 3, c4 = q >> 2;
+            const uint32_t X = xpair<F>(mw, q);
+            float w0, w1;
+            const uint32_t w2 = pair_step<ELEM>(s, lutb, X, w0, w1);
+#pragma unroll
+            for (int v = 0; v < NB; v++) {
+                const uint32_t xw = c4 < 2 ? xq[v].x : xq[v].y;
+                if (ELEM == 0) {
+                    if (c4 & 1) fma_bf16x2_half<true>(w2, xw, acc[2 * pp][v], acc[2 * pp + 1][v]);
+                    else fma_bf16x2_half<false>(w2, xw, acc[2 * pp][v], acc[2 * pp + 1][v]);
+                } else {
+                    const float xc = __uint_as_float((c4 & 1) ? (xw & 0xFFFF0000u) : (xw << 16));
+                    const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
+                                                make_float2(acc[2 * pp][v], acc[2 * pp + 1][v]));
+                    acc[2 * pp][v] = r.x;
+                    acc[2 * pp + 1][v] = r.y;
+                }
+            }
+        }
+    }
+    const uint32_t valid = (s.V & 127u) + 1u;
+    const uint32_t inserted = (s.pa - code) * 8u;
+    bad |= inserted - valid > 32u * lw;
+    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
+    esc_correct_batch<ELEM, NB>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0,
+                                lane, xb, ld_x, nb, kRows, kCols, acc, bad);
+}
+
+template <int ELEM, int NB>
+__global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
+    gemv_batch_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, int nb, float *__restrict__ y,
+                      int64_t ld_y, float *partial, uint32_t *counters, uint64_t n_pad) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint8_t *rexp = smem + kRexpOff;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16);
+    uint8_t *stage = smem + BatchCfg<NB>::kStageOff + warp * kStageBytes;
+    const uint64_t total_warps = (uint64_t)gridDim.x * BatchCfg<NB>::kWarps;
+    uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
+    uint32_t phase = 0;
+    bool bad = false, timed_out = false;
+
+    auto region = [&](uint64_t bb, const uint8_t *&ptr, uint32_t &bytes) {
+        uint32_t s0 = 0, s1 = 0;
+        if (lane == 0) {
+            s0 = m.tab[bb];
+            s1 = m.tab[bb + 1];
+        }
+        s0 = __shfl_sync(0xFFFFFFFFu, s0, 0);
+        s1 = __shfl_sync(0xFFFFFFFFu, s1, 0);
+        ptr = m.data + 16 * (uint64_t)s0;
+        bytes = 16 * (s1 - s0);
+    };
+    auto issue = [&](uint64_t bb, bool reuse) {
+        const uint8_t *src;
+        uint32_t bytes;
+        region(bb, src, bytes);
+        if (bytes <= (uint32_t)kStageBytes && lane == 0) {
+            if (reuse) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar0, bytes);
+            tma_load_1d(smem_u32(stage), src, bytes, bar0);
+        }
+    };
+
+    if (lane == 0) {
+        mbar_init(bar0);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (b < m.nb) issue(b, false);
+    load_rank_table(m, rexp);
+    build_lut<ELEM>(m, lut);
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    while (b < m.nb) {
+        const uint64_t nxt = b + total_warps;
+        __syncwarp();
+        if (nxt < m.nb && lane == 0) {
+            const uint32_t s0 = m.tab[nxt], s1 = m.tab[nxt + 1];
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(m.data + 16 * (uint64_t)s0),
+                         "r"(16 * (s1 - s0))
+                         : "memory");
+        }
+        const uint8_t *src;
+        uint32_t bytes;
+        region(b, src, bytes);
+        const uint8_t *reg = src;
+        const bool staged = bytes <= (uint32_t)kStageBytes;
+        if (staged) {
+            if (!mbar_wait(bar0, phase & 1u)) {
+                timed_out = true;
+                break;
+            }
+            phase ^= 1u;
+            reg = stage;
+        }
+        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
+        const int rows = real_rows(m.n, rb);
+        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
+        float acc[8][NB];
+#pragma unroll
+        for (int r = 0; r < 8; r++)
+#pragma unroll
+            for (int v = 0; v < NB; v++) acc[r][v] = 0.0f;
+        if (interior && staged) {
+            block_fast_batch<ELEM, NB>(stage, bytes, lane, lut, x + cb * kCols, ld_x, nb, acc, bad);
+        } else {
+            // edge blocks: the single-vector decoder once per vector
+#pragma unroll
+            for (int v = 0; v < NB; v++) {
+                if (v >= nb) break;
+                float a1[8];
+#pragma unroll
+                for (int r = 0; r < 8; r++) a1[r] = 0.0f;
+                block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + (int64_t)v * ld_x + cb * kCols,
+                                    a1, bad);
+#pragma unroll
+                for (int r = 0; r < 8; r++) acc[r][v] = a1[r];
+            }
+        }
+        const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
+        const uint64_t row = rb * kRows + (uint64_t)row_in;
+        const bool writer = (lane & 3) == 0 && row < m.n;
+#pragma unroll
+        for (int v = 0; v < NB; v++) {
+            float a1[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) a1[r] = acc[r][v];
+            const float sum = transpose_reduce(a1, lane);
+            if (v < nb && writer) {
+                if (m.cbs == 1) y[(int64_t)v * ld_y + (int64_t)row] = ELEM == 0 ? sum : sum * m.scales[row];
+                else partial[((uint64_t)v * m.cbs + cb) * n_pad + row] = sum;
+            }
+        }
+        if (m.cbs > 1) {
+            __syncwarp();
+            uint32_t ticket = 0;
+            if (lane == 0)
+                asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
+            ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+            if (ticket == (uint32_t)m.cbs - 1) {
+                __syncwarp();
+                const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
+                for (int v = 0; v < nb; v++) {
+                    float sv = 0.0f;
+                    if (r2 < m.n)
+                        for (uint64_t c2 = (uint64_t)(lane >> 3); c2 < m.cbs; c2 += 4)
+                            sv += __ldcg(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
+                    sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 8);
+                    sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 16);
+                    if (lane < kRows && r2 < m.n) y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
+                }
+                if (lane == 0) counters[rb] = 0;
+            }
+        }
+        __syncwarp();
+        if (nxt < m.nb) issue(nxt, true);
+        b = nxt;
+    }
+    if (timed_out) {
+        raise_error(kErrTimeout);
+        mbar_wait(bar0, phase & 1u);
+    }
+    if (bad) raise_error(kErrFormat);
+}
+
 // =================================================================== decode and gather
 // The pages run dequantization and the tied lm_head's embedding lookup on the GEMV's decoder;
 // here too: the same CTA
@@ -1255,6 +1530,76 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     cudaError_t rc = m.elem == NWC_ELEM_BF16
                          ? cudaLaunchKernelEx(&cfg, gemv_kernel<0>, m, x, y, partial, counters, n_pad)
                          : cudaLaunchKernelEx(&cfg, gemv_kernel<1>, m, x, y, partial, counters, n_pad);
+    return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- small-batch GEMV
+namespace {
+// Batch workspace: [counters u32 row_blocks, padded to 16 B][partials fp32 nb x col_blocks x
+// n_pad]; both only when K > 512. The counters come first, so a workspace prepared for nb
+// vectors serves every smaller count.
+uint64_t wsb_partial_off(const nwc_matrix &m) { return up16(4 * (uint64_t)m.row_blocks); }
+
+template <int ELEM, int NB>
+cudaError_t launch_batch(const Mat &m, const uint16_t *x, int64_t ld_x, int nb, float *y, int64_t ld_y, void *ws,
+                         uint64_t n_pad, int grid, cudaStream_t s) {
+    static bool smem_ok = false;
+    static std::once_flag once;
+    std::call_once(once, [] { smem_ok = set_smem(gemv_batch_kernel<ELEM, NB>, BatchCfg<NB>::kSmem); });
+    if (!smem_ok) return cudaErrorInvalidConfiguration;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    uint32_t *counters = reinterpret_cast<uint32_t *>(w8);
+    float *partial = reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(BatchCfg<NB>::kWarps * 32);
+    cfg.dynamicSmemBytes = BatchCfg<NB>::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_batch_kernel<ELEM, NB>, m, x, ld_x, nb, y, ld_y, partial, counters, n_pad);
+}
+}  // namespace
+
+extern "C" size_t nwc_gemv_batch_workspace_bytes(const nwc_matrix *mp, int nb) {
+    if (!mp || nb < 1 || nb > NWC_GEMV_BATCH_MAX) return 0;
+    if (mp->col_blocks <= 1) return 16;
+    return (size_t)up16(wsb_partial_off(*mp) + 4 * (uint64_t)nb * mp->col_blocks * pad_rows(*mp));
+}
+
+extern "C" nwc_status nwc_gemv_batch_prepare(const nwc_matrix *mp, int nb, void *ws, size_t ws_bytes,
+                                             nwc_stream stream) {
+    const size_t need = nwc_gemv_batch_workspace_bytes(mp, nb);
+    if (need == 0 || !ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
+    if (mp->col_blocks <= 1) return NWC_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return cudaMemsetAsync(ws, 0, 4 * (size_t)mp->row_blocks, s) == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
+}
+
+extern "C" nwc_status nwc_gemv_batch(const nwc_matrix *mp, const uint16_t *x, int64_t ld_x, int nb, float *y,
+                                     int64_t ld_y, void *ws, size_t ws_bytes, nwc_stream stream) {
+    if (!mp || !x || !y || !ws || nb < 1 || nb > NWC_GEMV_BATCH_MAX) return NWC_ERR_INVALID_ARG;
+    if (ld_x < (int64_t)mp->k || ld_y < (int64_t)mp->n || (ld_x % 8) != 0) return NWC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
+    if (ws_bytes < nwc_gemv_batch_workspace_bytes(mp, nb)) return NWC_ERR_INVALID_ARG;
+    const Mat m = to_mat(*mp);
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    const uint64_t n_pad = pad_rows(*mp);
+    const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t rc;
+    if (m.elem == NWC_ELEM_BF16)
+        rc = nb <= 2 ? launch_batch<0, 2>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
+           : nb <= 4 ? launch_batch<0, 4>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
+                     : launch_batch<0, 8>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
+    else
+        rc = nb <= 2 ? launch_batch<1, 2>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
+           : nb <= 4 ? launch_batch<1, 4>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
+                     : launch_batch<1, 8>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 

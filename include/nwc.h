@@ -185,6 +185,39 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
  */
 nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
 
+/* Largest vector count of one nwc_gemv_batch call. */
+#define NWC_GEMV_BATCH_MAX 8
+
+/*
+ * nwc_gemv_batch_workspace_bytes -- device scratch nwc_gemv_batch needs for m and nb vectors
+ * (1 <= nb <= NWC_GEMV_BATCH_MAX; 0 for any other nb): one counter per 8-row block and FP32
+ * partial sums per (vector, row, 512-column block), both only when K > 512; at least 16 bytes.
+ */
+size_t nwc_gemv_batch_workspace_bytes(const nwc_matrix *m, int nb);
+
+/*
+ * nwc_gemv_batch_prepare -- as nwc_gemv_prepare, for a batch workspace sized for nb vectors: zeroes
+ * its counters on the stream. A workspace prepared for nb serves every call with nb or fewer
+ * vectors, repeated calls and graph replays included; calls sharing it must not overlap on the GPU.
+ */
+nwc_status nwc_gemv_batch_prepare(const nwc_matrix *m, int nb, void *ws, size_t ws_bytes,
+                                  nwc_stream stream);
+
+/*
+ * nwc_gemv_batch -- Y = W X for nb activation vectors at once: nwc_gemv's fused kernel with
+ * nb accumulators per row. The pages run only batch 1 fused (the NWC page, "How it works") and
+ * send batch > 1 through a decode to BF16 and cuBLAS; this call covers the small batches in
+ * between (a few tokens per step). Every weight is decoded once per call and multiplied into
+ * all nb vectors, so the matrix bytes are read, and the codes decoded, once for the whole batch. x: BF16 [nb][ld_x], vector v at x + v*ld_x,
+ * x 16-byte aligned, ld_x >= K and a multiple of 8. y: FP32 [nb][ld_y], ld_y >= N. Each
+ * y[v] meets nwc_gemv's bound for its own vector (the sum order may differ from nwc_gemv's).
+ * ws/ws_bytes: a workspace prepared by nwc_gemv_batch_prepare for this matrix and at least nb
+ * vectors. nb outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. For nb == 1, nwc_gemv
+ * is the faster call.
+ */
+nwc_status nwc_gemv_batch(const nwc_matrix *m, const uint16_t *x, int64_t ld_x, int nb, float *y,
+                          int64_t ld_y, void *ws, size_t ws_bytes, nwc_stream stream);
+
 /*
  * nwc_gather -- embedding lookup on the same decoder (the NWC page, "How it works": the
  * embedding lookup of a tied lm_head shares the GEMV's decoder): out row i = row ids[i] of the stored matrix,

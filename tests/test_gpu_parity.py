@@ -324,3 +324,72 @@ def test_embedding_table_gather_and_lm_head_sampled():
     x = synth.activations_bf16(synth.HIDDEN, 9)
     rows = np.sort(np.random.default_rng(1).choice(synth.VOCAB, 2048, False))
     gemv_check(blob, x, rows=rows, mat=mat)
+
+
+# --------------------------------------------------------------------- small-batch GEMV
+def batch_check(blob, xs, rows=None, mat=None, ld_x=None, ld_y=None, repeat=1):
+    """nwc_gemv_batch on the vectors xs (list of BF16 bit arrays) against the oracle, per vector;
+    x rows ld_x apart and y rows ld_y apart (defaults: K rounded up to 8, N)."""
+    mat = mat or nwc.Matrix(blob)
+    nb, k, n = len(xs), mat.k, mat.n
+    ld_x = ld_x or (k + 7) // 8 * 8
+    ld_y = ld_y or n
+    xb = np.zeros((nb, ld_x), np.uint16)
+    for v, x in enumerate(xs):
+        xb[v, :k] = x
+    xd = dev_bits(xb)[:, :k]
+    yd = torch.full((nb, ld_y), float("nan"), dtype=torch.float32, device="cuda")[:, :n]
+    for _ in range(repeat):
+        mat.gemv_batch(xd, yd)
+    y = yd.cpu().numpy().astype(np.float64)
+    assert_clean()
+    if rows is None:
+        rows = np.arange(n)
+    for v, x in enumerate(xs):
+        ref = oracle.gemv(blob, x, rows)
+        bound = TOL_REL * oracle.abs_dot(blob, x, rows) + TOL_ABS
+        err = np.abs(y[v, rows] - ref)
+        worst = int(np.argmax(err - bound))
+        assert (err <= bound).all(), f"vector {v} row {rows[worst]}: |{y[v, rows][worst]} - {ref[worst]}| > {bound[worst]}"
+    return y
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("shape", [(1, 1), (9, 513), (33, 4000), (40, 9728), (257, 1100)])
+def test_gemv_batch_shapes(shape, nb):
+    w = synth.normal_bf16(shape, 0.02, seed=shape[0] + 5 * shape[1])
+    xs = [synth.activations_bf16(shape[1], 100 + v) for v in range(nb)]
+    batch_check(nwc.encode(w), xs)
+
+
+@pytest.mark.parametrize("nb", [2, 4, 7])
+def test_gemv_batch_fp8(nb):
+    w = synth.normal_bf16((300, 2600), 0.02, seed=61)
+    blob = nwc.encode(w, elem=nwc.FP8)
+    xs = [synth.activations_bf16(2600, 200 + v) for v in range(nb)]
+    batch_check(blob, xs)
+
+
+def test_gemv_batch_escape_heavy_and_strided():
+    """Escape-list corrections applied to every vector; x and y with padded row strides and a
+    second call on the same workspace (counters left at zero by the first)."""
+    w = _escape_heavy((256, 4096), 29)
+    blob = nwc.encode(w)
+    xs = [synth.activations_bf16(4096, 300 + v) for v in range(6)]
+    batch_check(blob, xs, ld_x=4096 + 24, ld_y=256 + 5, repeat=2)
+
+
+def test_gemv_batch_matches_single_vector_calls_in_tolerance_full_size():
+    """The gate projection of the stack at full size, 8 vectors, sampled rows; the same vectors through
+    nwc_gemv one at a time agree with the batch within twice the tolerance."""
+    w = synth.layer_matrix(0, "gate")
+    n, k = w.shape
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    xs = [synth.activations_bf16(k, 400 + v) for v in range(8)]
+    rows = np.sort(np.random.default_rng(5).choice(n, 256, False))
+    y = batch_check(blob, xs, rows=rows, mat=mat)
+    for v in (0, 7):
+        y1 = mat.gemv(dev_bits(xs[v])).cpu().numpy().astype(np.float64)
+        bound = 2 * (TOL_REL * oracle.abs_dot(blob, xs[v], rows) + TOL_ABS)
+        assert (np.abs(y1[rows] - y[v, rows]) <= bound).all()
