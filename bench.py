@@ -266,9 +266,9 @@ def extra_workloads(dev, stream, steps):
 
     # Small-batch decoding on the fused stack: nb tokens per step through nwc_gemv_batch (each
     # weight decoded once for all nb vectors), against cuBLAS on the BF16 weights.
-    xbat = {k: torch.from_numpy(np.stack([synth.activations_bf16(k, 3000 + k + v) for v in range(8)])
+    xbat = {k: torch.from_numpy(np.stack([synth.activations_bf16(k, 3000 + k + v) for v in range(16)])
                                 .view(np.int16)).to(dev) for k in {m.k for m in mats}}
-    for nb in (2, 4, 8):
+    for nb in (2, 4, 8, 16):
         yB = [torch.empty((nb, m.n), dtype=torch.float32, device=dev) for m in mats]
         ybB = [torch.empty((nb, m.n), dtype=torch.bfloat16, device=dev) for m in mats]
 

@@ -18,6 +18,7 @@ __all__ = [
 ]
 
 BF16, FP8 = 0, 1
+BATCH_MAX = 16  # NWC_GEMV_BATCH_MAX: vectors per nwc_gemv_batch call
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libnwc.so")
 
@@ -189,18 +190,18 @@ class Matrix:
         return y
 
     def gemv_batch(self, x, y=None, stream=None):
-        """Y (float32[nb, N]) = W x[v] for the nb <= 8 rows of x (BF16 [nb, K] as an int16/bfloat16
+        """Y (float32[nb, N]) = W x[v] for the nb <= 16 rows of x (BF16 [nb, K] as an int16/bfloat16
         CUDA tensor, row stride a multiple of 8): one fused pass that decodes every weight once.
-        The batch workspace (sized for 8 vectors) is allocated and prepared on first use."""
+        The batch workspace (sized for 16 vectors) is allocated and prepared on first use."""
         import torch
         assert x.dim() == 2 and x.shape[1] == self.k and x.is_cuda and x.stride(1) == 1
         nb = x.shape[0]
         if y is None:
             y = torch.empty((nb, self.n), dtype=torch.float32, device=x.device)
         if getattr(self, "_bws", None) is None:
-            bws = int(lib().nwc_gemv_batch_workspace_bytes(ctypes.byref(self.m), 8))
+            bws = int(lib().nwc_gemv_batch_workspace_bytes(ctypes.byref(self.m), BATCH_MAX))
             self._bws = torch.empty(bws, dtype=torch.uint8, device=self.device_blob.device)
-            _ok(lib().nwc_gemv_batch_prepare(ctypes.byref(self.m), 8, ctypes.c_void_p(self._bws.data_ptr()), bws,
+            _ok(lib().nwc_gemv_batch_prepare(ctypes.byref(self.m), BATCH_MAX, ctypes.c_void_p(self._bws.data_ptr()), bws,
                                              _stream_ptr(stream)), "nwc_gemv_batch_prepare")
         _ok(lib().nwc_gemv_batch(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), x.stride(0), nb,
                                  ctypes.c_void_p(y.data_ptr()), y.stride(0), ctypes.c_void_p(self._bws.data_ptr()),

@@ -795,82 +795,65 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
 }
 
 // =================================================================== small-batch GEMV
-// Y[v] = W x[v] for up to 8 activation vectors ("batch > 1" without leaving the fused kernel):
-// each weight is decoded once and multiplied into every vector, NB accumulators per row. One
-// CTA per SM of 16 warps (12 for NB = 8, whose 64 accumulators need more registers); otherwise
-// as the single-vector GEMV (staged regions,
-// shared table, escape-list corrections, ticket reduction per row block, programmatic launch).
-template <int NB>
-struct BatchCfg {
-    static constexpr int kWarps = NB <= 4 ? 16 : 12;  // 128 or 168 registers per thread
-    static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
-    static constexpr int kSmem = kStageOff + kWarps * kStageBytes;
-};
-static_assert(BatchCfg<2>::kSmem <= 232448 && BatchCfg<8>::kSmem <= 232448, "shared memory per CTA");
+// Y[v] = W x[v] for up to 16 activation vectors (a few tokens per step) in one pass over the
+// matrix: each weight is decoded once, as in the single-vector GEMV, and the products with all
+// vectors are a dense contraction per block ([vectors x 512] . [512 x 8 rows]), done by the
+// tensor cores. Per group of 4 columns the warp writes its decoded 8 x 128 tile to shared memory
+// and runs eight m16n8k16 BF16 products with FP32 accumulation; the vectors are the M side, so
+// any count up to 16 costs the same. Escaped elements are written into the tile with their true
+// values, so no correction is needed.
+constexpr int kBatchWarps = 16;
+constexpr int kTileBytes = 8 * 32 * 8;  // 8 rows x 32 lanes x 4 columns x BF16
+constexpr int kBatchStageOff = (kBarOff + kBatchWarps * 2 * 8 + 127) / 128 * 128;
+constexpr int kBatchTileOff = kBatchStageOff + kBatchWarps * kStageBytes;
+constexpr int kBatchSmem = kBatchTileOff + kBatchWarps * kTileBytes;
+static_assert(kBatchSmem <= 232448, "shared memory per CTA");
 
-// acc0 += lo(w2) * x, acc1 += hi(w2) * x with x the low (HI = false) or high half of xw.
-template <bool HI>
-__device__ __forceinline__ void fma_bf16x2_half(uint32_t w2, uint32_t xw, float &acc0, float &acc1) {
-    if (HI)
-        asm("{\n\t.reg .b16 lo, hi, xl, xh;\n\t"
-            "mov.b32 {lo, hi}, %2;\n\t"
-            "mov.b32 {xl, xh}, %3;\n\t"
-            "fma.rn.f32.bf16 %0, lo, xh, %0;\n\t"
-            "fma.rn.f32.bf16 %1, hi, xh, %1;\n\t}"
-            : "+f"(acc0), "+f"(acc1)
-            : "r"(w2), "r"(xw));
-    else
-        asm("{\n\t.reg .b16 lo, hi, xl, xh;\n\t"
-            "mov.b32 {lo, hi}, %2;\n\t"
-            "mov.b32 {xl, xh}, %3;\n\t"
-            "fma.rn.f32.bf16 %0, lo, xl, %0;\n\t"
-            "fma.rn.f32.bf16 %1, hi, xl, %1;\n\t}"
-            : "+f"(acc0), "+f"(acc1)
-            : "r"(w2), "r"(xw));
+// Byte offset in a warp's tile of row r, lane L's 4 columns (8 bytes). The 8-byte unit is
+// L ^ 4r: a row's stores (32 lanes) and an mma operand load (rows 0..7, four consecutive lanes
+// per row) each touch 16 distinct units per half-warp, so neither has bank conflicts.
+__device__ __forceinline__ uint32_t tile_off(uint32_t r, uint32_t L) { return r * 256u + 8u * (L ^ (4u * r)); }
+
+// d += A . B for one m16n8k16 tile: a0..a3 and b0, b1 in the PTX fragment layout (BF16 pairs),
+// FP32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// The escape-list corrections of esc_correct, for every vector.
-template <int ELEM, int NB>
-__device__ __forceinline__ void esc_correct_batch(const uint32_t *list, uint32_t slots, int lane, const uint16_t *xb,
-                                                  int64_t ld_x, int nb, int rows, int kc, float (&acc)[8][NB],
-                                                  bool &bad) {
-    for (uint32_t j = (uint32_t)lane; j < slots; j += 32) {
-        const uint32_t e = list[j];
-        if (e == kEscPad) continue;
-        const uint32_t t = esc_t(e), bits = esc_bits(e);
-        const int r = (int)(t & 7u), c = (int)esc_lane(e) * kLaneCols + (int)(t >> 3);
-        if (r >= rows || c >= kc) {
-            bad = true;
-            continue;
-        }
-        const float w = ELEM == 0 ? __uint_as_float(bits << 16) : elem_value<1>(bits >> 7, (bits >> 3) & 15u, bits & 7u);
-        const float ph = esc_placeholder<ELEM>(bits);
-#pragma unroll
-        for (int v = 0; v < NB; v++) {
-            if (v >= nb) break;
-            const float xv = __uint_as_float((uint32_t)__ldg(xb + (int64_t)v * ld_x + c) << 16);
-            const float d = fmaf(w, xv, -(ph * xv));
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                if (i == r) acc[i][v] += d;
-        }
-    }
+// Two FP32 values (exact in BF16) packed as BF16x2, lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
-// Interior block from its staged region, NB vectors (the first nb real).
-template <int ELEM, int NB>
-__device__ __forceinline__ void block_fast_batch(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
-                                                 const uint16_t *xb, int64_t ld_x, int nb, float (&acc)[8][NB],
-                                                 bool &bad) {
+// BF16 bits of an escaped element's true value (fp8: the e4m3 value, exact in BF16).
+template <int ELEM>
+__device__ __forceinline__ uint32_t esc_bf16(uint32_t bits) {
+    if (ELEM == 0) return bits & 0xFFFFu;
+    return __float_as_uint(elem_value<1>(bits >> 7, (bits >> 3) & 15u, bits & 7u)) >> 16;
+}
+
+// Interior block from its staged region, all vectors: d[0..3] receive the block's sums in the
+// m16n8k16 accumulator layout (vector lane/4 rows 2(lane%4), +1 in d0, d1; vector lane/4 + 8 in
+// d2, d3). x0/x1 = this thread's two vectors (from the block's first column), or null past nb.
+template <int ELEM>
+__device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
+                                          uint32_t tile, const uint16_t *x0, const uint16_t *x1, float (&d)[4],
+                                          bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
     const uint32_t lw = reg[lane];
     uint32_t incl = lw;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += o;
+    for (int dd = 1; dd < 32; dd <<= 1) {
+        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, dd);
+        if (lane >= dd) incl += o;
     }
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
@@ -888,48 +871,76 @@ __device__ __forceinline__ void block_fast_batch(const uint8_t *reg, uint32_t by
         asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
     }
     const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
+    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
+    const uint32_t slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
+    const uint32_t *list = reinterpret_cast<const uint32_t *>(reg + esc0);
+    const uint32_t gid = (uint32_t)lane >> 2, t = (uint32_t)lane & 3u;
+    // this thread's operand row in every group: row gid of lane 4j + t
+    const uint32_t brow = tile + gid * 256u;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
-        uint2 xq[NB];  // the group's four activations of each vector (BF16 pairs)
+        // A operands of the group's eight products: columns 4g..4g+3 of lane 4j + t, as BF16
+        // pairs (cols 0, 1 -> k = 2t, 2t + 1; cols 2, 3 -> k = 2t + 8, 2t + 9)
+        uint2 xa[8], xb8[8];
 #pragma unroll
-        for (int v = 0; v < NB; v++)
-            xq[v] = v < nb ? __ldg(reinterpret_cast<const uint2 *>(xb + (int64_t)v * ld_x + lane * kLaneCols) + g)
-                           : make_uint2(0u, 0u);
+        for (int j = 0; j < 8; j++) {
+            const int col = (4 * j + (int)t) * kLaneCols + 4 * g;
+            xa[j] = x0 ? __ldg(reinterpret_cast<const uint2 *>(x0 + col)) : make_uint2(0u, 0u);
+            xb8[j] = x1 ? __ldg(reinterpret_cast<const uint2 *>(x1 + col)) : make_uint2(0u, 0u);
+        }
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+        uint32_t w2[16];
 #pragma unroll
         for (int q = 0; q < 16; q++) {
-            const int pp = q & 3, c4 = q >> 2;
-            const uint32_t X = xpair<F>(mw, q);
-            float w0, w1;
-            const uint32_t w2 = pair_step<ELEM>(s, lutb, X, w0, w1);
-#pragma unroll
-            for (int v = 0; v < NB; v++) {
-                const uint32_t xw = c4 < 2 ? xq[v].x : xq[v].y;
-                if (ELEM == 0) {
-                    if (c4 & 1) fma_bf16x2_half<true>(w2, xw, acc[2 * pp][v], acc[2 * pp + 1][v]);
-                    else fma_bf16x2_half<false>(w2, xw, acc[2 * pp][v], acc[2 * pp + 1][v]);
-                } else {
-                    const float xc = __uint_as_float((c4 & 1) ? (xw & 0xFFFF0000u) : (xw << 16));
-                    const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
-                                                make_float2(acc[2 * pp][v], acc[2 * pp + 1][v]));
-                    acc[2 * pp][v] = r.x;
-                    acc[2 * pp + 1][v] = r.y;
-                }
-            }
+            float f0, f1;
+            w2[q] = pair_step<ELEM>(s, lutb, xpair<F>(mw, q), f0, f1);
+            if (ELEM == 1) w2[q] = pack_bf16x2(f0, f1);
         }
+        // rows 2pp (low halves) and 2pp + 1 (high halves) of columns 0..3 (w2[4 c + pp])
+#pragma unroll
+        for (int pp = 0; pp < 4; pp++) {
+            const uint32_t lo0 = __byte_perm(w2[pp], w2[4 + pp], 0x5410), lo1 = __byte_perm(w2[8 + pp], w2[12 + pp], 0x5410);
+            const uint32_t hi0 = __byte_perm(w2[pp], w2[4 + pp], 0x7632), hi1 = __byte_perm(w2[8 + pp], w2[12 + pp], 0x7632);
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tile + tile_off(2 * pp, lane)), "r"(lo0), "r"(lo1)
+                         : "memory");
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(tile + tile_off(2 * pp + 1, lane)), "r"(hi0),
+                         "r"(hi1)
+                         : "memory");
+        }
+        __syncwarp();
+        // escaped elements of this group: their true values over the placeholders
+        for (uint32_t j = (uint32_t)lane; j < slots; j += 32) {
+            const uint32_t e = list[j];
+            if (e == kEscPad) continue;
+            const uint32_t te = esc_t(e), c = te >> 3;
+            if ((c >> 2) != (uint32_t)g) continue;
+            const uint32_t a = tile + tile_off(te & 7u, esc_lane(e)) + 2u * (c & 3u);
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)esc_bf16<ELEM>(esc_bits(e))) : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            uint32_t b0, b1;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(b0), "=r"(b1)
+                         : "r"(brow + 8u * ((4u * (uint32_t)j + t) ^ (4u * gid)))
+                         : "memory");
+            mma_bf16(acc[j & 1], xa[j].x, xb8[j].x, xa[j].y, xb8[j].y, b0, b1);
+        }
+        __syncwarp();
     }
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
     bad |= inserted - valid > 32u * lw;
-    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
-    esc_correct_batch<ELEM, NB>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0,
-                                lane, xb, ld_x, nb, kRows, kCols, acc, bad);
+#pragma unroll
+    for (int i = 0; i < 4; i++) d[i] = acc[0][i] + acc[1][i];
 }
 
-template <int ELEM, int NB>
-__global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
+template <int ELEM>
+__global__ void __launch_bounds__(kBatchWarps * 32, 1)
     gemv_batch_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, int nb, float *__restrict__ y,
                       int64_t ld_y, float *partial, uint32_t *counters, uint64_t n_pad) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -938,11 +949,13 @@ __global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
     uint8_t *rexp = smem + kRexpOff;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16);
-    uint8_t *stage = smem + BatchCfg<NB>::kStageOff + warp * kStageBytes;
-    const uint64_t total_warps = (uint64_t)gridDim.x * BatchCfg<NB>::kWarps;
+    uint8_t *stage = smem + kBatchStageOff + warp * kStageBytes;
+    const uint32_t tile = smem_u32(smem + kBatchTileOff + warp * kTileBytes);
+    const uint64_t total_warps = (uint64_t)gridDim.x * kBatchWarps;
     uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
     uint32_t phase = 0;
     bool bad = false, timed_out = false;
+    const int gid = lane >> 2, t = lane & 3;
 
     auto region = [&](uint64_t bb, const uint8_t *&ptr, uint32_t &bytes) {
         uint32_t s0 = 0, s1 = 0;
@@ -964,6 +977,11 @@ __global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
             mbar_expect_tx(bar0, bytes);
             tma_load_1d(smem_u32(stage), src, bytes, bar0);
         }
+    };
+    // result of vector v, row `row` (< n) of column block cb
+    auto emit = [&](int v, uint64_t row, uint64_t cb, float val) {
+        if (m.cbs == 1) y[(int64_t)v * ld_y + (int64_t)row] = ELEM == 0 ? val : val * m.scales[row];
+        else partial[((uint64_t)v * m.cbs + cb) * n_pad + row] = val;
     };
 
     if (lane == 0) {
@@ -1002,49 +1020,45 @@ __global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
-        float acc[8][NB];
-#pragma unroll
-        for (int r = 0; r < 8; r++)
-#pragma unroll
-            for (int v = 0; v < NB; v++) acc[r][v] = 0.0f;
         if (interior && staged) {
-            block_fast_batch<ELEM, NB>(stage, bytes, lane, lut, x + cb * kCols, ld_x, nb, acc, bad);
+            const uint16_t *xc = x + cb * kCols;
+            const uint16_t *x0 = gid < nb ? xc + (int64_t)gid * ld_x : nullptr;
+            const uint16_t *x1 = gid + 8 < nb ? xc + (int64_t)(gid + 8) * ld_x : nullptr;
+            float d[4];
+            block_mma<ELEM>(stage, bytes, lane, lut, tile, x0, x1, d, bad);
+            const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;  // interior: both rows < n
+            if (gid < nb) {
+                emit(gid, r0, cb, d[0]);
+                emit(gid, r0 + 1, cb, d[1]);
+            }
+            if (gid + 8 < nb) {
+                emit(gid + 8, r0, cb, d[2]);
+                emit(gid + 8, r0 + 1, cb, d[3]);
+            }
         } else {
-            // edge blocks: the single-vector decoder once per vector
-#pragma unroll
-            for (int v = 0; v < NB; v++) {
-                if (v >= nb) break;
+            // edge blocks and regions too large to stage: the single-vector decoder per vector
+            const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
+            const uint64_t row = rb * kRows + (uint64_t)row_in;
+            for (int v = 0; v < nb; v++) {
                 float a1[8];
 #pragma unroll
                 for (int r = 0; r < 8; r++) a1[r] = 0.0f;
                 block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + (int64_t)v * ld_x + cb * kCols,
                                     a1, bad);
-#pragma unroll
-                for (int r = 0; r < 8; r++) acc[r][v] = a1[r];
-            }
-        }
-        const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
-        const uint64_t row = rb * kRows + (uint64_t)row_in;
-        const bool writer = (lane & 3) == 0 && row < m.n;
-#pragma unroll
-        for (int v = 0; v < NB; v++) {
-            float a1[8];
-#pragma unroll
-            for (int r = 0; r < 8; r++) a1[r] = acc[r][v];
-            const float sum = transpose_reduce(a1, lane);
-            if (v < nb && writer) {
-                if (m.cbs == 1) y[(int64_t)v * ld_y + (int64_t)row] = ELEM == 0 ? sum : sum * m.scales[row];
-                else partial[((uint64_t)v * m.cbs + cb) * n_pad + row] = sum;
+                const float sum = transpose_reduce(a1, lane);
+                if ((lane & 3) == 0 && row < m.n) emit(v, row, cb, sum);
             }
         }
         if (m.cbs > 1) {
             __syncwarp();
             uint32_t ticket = 0;
+            // release / acquire as in the single-vector GEMV
             if (lane == 0)
                 asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
             if (ticket == (uint32_t)m.cbs - 1) {
                 __syncwarp();
+                // row lane % 8; lane / 8 sums column blocks lane / 8, + 4, ...
                 const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
                 for (int v = 0; v < nb; v++) {
                     float sv = 0.0f;
@@ -1053,7 +1067,8 @@ __global__ void __launch_bounds__(BatchCfg<NB>::kWarps * 32, 1)
                             sv += __ldcg(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
                     sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 8);
                     sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 16);
-                    if (lane < kRows && r2 < m.n) y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
+                    if (lane < kRows && r2 < m.n)
+                        y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
                 }
                 if (lane == 0) counters[rb] = 0;
             }
@@ -1540,27 +1555,27 @@ namespace {
 // vectors serves every smaller count.
 uint64_t wsb_partial_off(const nwc_matrix &m) { return up16(4 * (uint64_t)m.row_blocks); }
 
-template <int ELEM, int NB>
+template <int ELEM>
 cudaError_t launch_batch(const Mat &m, const uint16_t *x, int64_t ld_x, int nb, float *y, int64_t ld_y, void *ws,
                          uint64_t n_pad, int grid, cudaStream_t s) {
     static bool smem_ok = false;
     static std::once_flag once;
-    std::call_once(once, [] { smem_ok = set_smem(gemv_batch_kernel<ELEM, NB>, BatchCfg<NB>::kSmem); });
+    std::call_once(once, [] { smem_ok = set_smem(gemv_batch_kernel<ELEM>, kBatchSmem); });
     if (!smem_ok) return cudaErrorInvalidConfiguration;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     uint32_t *counters = reinterpret_cast<uint32_t *>(w8);
     float *partial = reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(BatchCfg<NB>::kWarps * 32);
-    cfg.dynamicSmemBytes = BatchCfg<NB>::kSmem;
+    cfg.blockDim = dim3(kBatchWarps * 32);
+    cfg.dynamicSmemBytes = kBatchSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_batch_kernel<ELEM, NB>, m, x, ld_x, nb, y, ld_y, partial, counters, n_pad);
+    return cudaLaunchKernelEx(&cfg, gemv_batch_kernel<ELEM>, m, x, ld_x, nb, y, ld_y, partial, counters, n_pad);
 }
 }  // namespace
 
@@ -1591,15 +1606,8 @@ extern "C" nwc_status nwc_gemv_batch(const nwc_matrix *mp, const uint16_t *x, in
     const uint64_t n_pad = pad_rows(*mp);
     const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t rc;
-    if (m.elem == NWC_ELEM_BF16)
-        rc = nb <= 2 ? launch_batch<0, 2>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
-           : nb <= 4 ? launch_batch<0, 4>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
-                     : launch_batch<0, 8>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
-    else
-        rc = nb <= 2 ? launch_batch<1, 2>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
-           : nb <= 4 ? launch_batch<1, 4>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
-                     : launch_batch<1, 8>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
+    const cudaError_t rc = m.elem == NWC_ELEM_BF16 ? launch_batch<0>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
+                                                   : launch_batch<1>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 

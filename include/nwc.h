@@ -186,7 +186,7 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
 nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
 
 /* Largest vector count of one nwc_gemv_batch call. */
-#define NWC_GEMV_BATCH_MAX 8
+#define NWC_GEMV_BATCH_MAX 16
 
 /*
  * nwc_gemv_batch_workspace_bytes -- device scratch nwc_gemv_batch needs for m and nb vectors
@@ -204,16 +204,17 @@ nwc_status nwc_gemv_batch_prepare(const nwc_matrix *m, int nb, void *ws, size_t 
                                   nwc_stream stream);
 
 /*
- * nwc_gemv_batch -- Y = W X for nb activation vectors at once: nwc_gemv's fused kernel with
- * nb accumulators per row. The pages run only batch 1 fused (the NWC page, "How it works") and
- * send batch > 1 through a decode to BF16 and cuBLAS; this call covers the small batches in
- * between (a few tokens per step). Every weight is decoded once per call and multiplied into
- * all nb vectors, so the matrix bytes are read, and the codes decoded, once for the whole batch. x: BF16 [nb][ld_x], vector v at x + v*ld_x,
- * x 16-byte aligned, ld_x >= K and a multiple of 8. y: FP32 [nb][ld_y], ld_y >= N. Each
- * y[v] meets nwc_gemv's bound for its own vector (the sum order may differ from nwc_gemv's).
- * ws/ws_bytes: a workspace prepared by nwc_gemv_batch_prepare for this matrix and at least nb
- * vectors. nb outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. For nb == 1, nwc_gemv
- * is the faster call.
+ * nwc_gemv_batch -- Y = W X for nb activation vectors at once: nwc_gemv's decoder, with the
+ * products of each decoded 8 x 512 block and all nb vectors done on the tensor cores (BF16
+ * operands, FP32 accumulation; fp8 weights widened exactly to BF16). The pages run only batch 1
+ * fused (the NWC page, "How it works") and send batch > 1 through a decode to BF16 and cuBLAS;
+ * this call covers the small batches in between (a few tokens per step). Every weight is decoded
+ * once per call, so the matrix bytes are read, and the codes decoded, once for the whole batch,
+ * and any nb up to 16 costs about the same. x: BF16 [nb][ld_x], vector v at x + v*ld_x, x
+ * 16-byte aligned, ld_x >= K and a multiple of 8. y: FP32 [nb][ld_y], ld_y >= N. Each y[v]
+ * meets nwc_gemv's bound for its own vector (the sum order differs from nwc_gemv's). ws/ws_bytes:
+ * a workspace prepared by nwc_gemv_batch_prepare for this matrix and at least nb vectors. nb
+ * outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. For nb == 1, nwc_gemv is faster.
  */
 nwc_status nwc_gemv_batch(const nwc_matrix *m, const uint16_t *x, int64_t ld_x, int nb, float *y,
                           int64_t ld_y, void *ws, size_t ws_bytes, nwc_stream stream);

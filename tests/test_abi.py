@@ -187,12 +187,12 @@ def test_batch_gemv_workspace_and_argument_checks():
     mp = ctypes.byref(m)
     P = ctypes.c_void_p
     # 5 counters (32 B with padding) + nb x 3 column blocks x 40 padded rows x 4 B
-    for nb in range(1, 9):
+    for nb in range(1, 17):
         assert int(L.nwc_gemv_batch_workspace_bytes(mp, nb)) == 32 + nb * 3 * 40 * 4
     assert L.nwc_gemv_batch_workspace_bytes(mp, 0) == 0
-    assert L.nwc_gemv_batch_workspace_bytes(mp, 9) == 0
+    assert L.nwc_gemv_batch_workspace_bytes(mp, 17) == 0
     ws = int(L.nwc_gemv_batch_workspace_bytes(mp, 4))
-    assert L.nwc_gemv_batch(mp, P(0x20000), 1104, 9, P(0x30000), 40, P(0x40000), 10 ** 6, None) == 1  # nb > 8
+    assert L.nwc_gemv_batch(mp, P(0x20000), 1104, 17, P(0x30000), 40, P(0x40000), 10 ** 6, None) == 1  # nb > 16
     assert L.nwc_gemv_batch(mp, P(0x20000), 1104, 0, P(0x30000), 40, P(0x40000), ws, None) == 1     # nb < 1
     assert L.nwc_gemv_batch(mp, P(0x20000), 1100, 4, P(0x30000), 40, P(0x40000), ws, None) == 1     # ld_x % 8
     assert L.nwc_gemv_batch(mp, P(0x20000), 1096, 4, P(0x30000), 40, P(0x40000), ws, None) == 1     # ld_x < K
@@ -202,8 +202,9 @@ def test_batch_gemv_workspace_and_argument_checks():
     assert L.nwc_gemv_batch(mp, P(0x20000), 1104, 4, P(0x30000), 40, P(0x40000), ws - 16, None) == 1
     assert L.nwc_gemv_batch(mp, P(0x20000), 1104, 4, None, 40, P(0x40000), ws, None) == 1
     assert L.nwc_gemv_batch_prepare(mp, 4, P(0x40000), ws - 16, None) == 1
-    assert L.nwc_gemv_batch_prepare(mp, 9, P(0x40000), 10 ** 6, None) == 1
+    assert L.nwc_gemv_batch_prepare(mp, 17, P(0x40000), 10 ** 6, None) == 1
     assert L.nwc_gemv_batch_prepare(mp, 4, P(0x40008), ws, None) == 1
     # one column block: no partials, no counters, 16 bytes
     st, m1 = bind_host(nwc.encode(synth.normal_bf16((9, 500), 0.02, seed=4)))
-    assert st == 0 and L.nwc_gemv_batch_workspace_bytes(ctypes.byref(m1), 8) == 16
+    assert st == 0 and L.nwc_gemv_batch_workspace_bytes(ctypes.byref(m1), 16) == 16
+    assert nwc.BATCH_MAX == 16
