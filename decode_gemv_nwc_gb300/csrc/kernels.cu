@@ -664,6 +664,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     // Block b goes to CTA b % grid, so every SM gets within one block of the same count.
     const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
     uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
+    // b's row and column block, stepped by (dq, dr) = total_warps / cbs, % cbs without dividing
+    uint64_t rb = b / m.cbs, cb = b % m.cbs;
+    const uint64_t dq = total_warps / m.cbs, dr = total_warps % m.cbs;
     uint32_t phase = 0;  // bit i: parity of the next completion of stage i
     bool bad = false, timed_out = false;
 
@@ -726,7 +729,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         region(b, src, bytes);
         const uint8_t *reg = src;
         const bool staged = bytes <= (uint32_t)kStageBytes;
-        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         // the fast path's first activations, loaded while the region copy completes
@@ -784,6 +786,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
             if (nxt < m.nb) issue(nxt, 0, true);
         }
         b = nxt;
+        rb += dq;
+        cb += dr;
+        if (cb >= m.cbs) {
+            cb -= m.cbs;
+            rb += 1;
+        }
     }
     if (timed_out) {
         raise_error(kErrTimeout);
@@ -800,14 +808,28 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
 // vectors are a dense contraction per block ([vectors x 512] . [512 x 8 rows]), done by the
 // tensor cores. Per group of 4 columns the warp writes its decoded 8 x 128 tile to shared memory
 // and runs eight m16n8k16 BF16 products with FP32 accumulation; the vectors are the M side, so
-// any count up to 16 costs the same. Escaped elements are written into the tile with their true
-// values, so no correction is needed.
-constexpr int kBatchWarps = 16;
+// any count up to 16 costs about the same. Escaped elements are written into the tile with their
+// true values, so no correction is needed. Each CTA takes a contiguous range of blocks in
+// column-block-major order and stages the activations of its (at most two) column blocks in
+// shared memory once; 20 warps per SM with up to 102 registers.
+#ifndef NWC_BATCH_WARPS
+#define NWC_BATCH_WARPS 20
+#endif
+constexpr int kBatchWarps = NWC_BATCH_WARPS;
 constexpr int kTileBytes = 8 * 32 * 8;  // 8 rows x 32 lanes x 4 columns x BF16
 constexpr int kBatchStageOff = (kBarOff + kBatchWarps * 2 * 8 + 127) / 128 * 128;
 constexpr int kBatchTileOff = kBatchStageOff + kBatchWarps * kStageBytes;
-constexpr int kBatchSmem = kBatchTileOff + kBatchWarps * kTileBytes;
+constexpr int kBatchMax = 16;
+constexpr int kXSlice = kBatchMax * kCols * 2;  // one column block of every vector, BF16
+constexpr int kBatchXOff = kBatchTileOff + kBatchWarps * kTileBytes;
+constexpr int kBatchSmem = kBatchXOff + 2 * kXSlice;
 static_assert(kBatchSmem <= 232448, "shared memory per CTA");
+static_assert(kBatchMax == NWC_GEMV_BATCH_MAX, "vectors per call");
+
+// Byte offset in a staged activation slice of vector v, columns 4u..4u+3 of the column block
+// (u = 4 * lane + group): 8-byte unit u ^ (v & 3), so the operand loads of one product (vectors
+// gid, four lanes) fall in 16 distinct units per half-warp.
+__device__ __forceinline__ uint32_t xs_off(uint32_t v, uint32_t u) { return v * (uint32_t)(kCols * 2) + 8u * (u ^ (v & 3u)); }
 
 // Byte offset in a warp's tile of row r, lane L's 4 columns (8 bytes). The 8-byte unit is
 // L ^ 4r: a row's stores (32 lanes) and an mma operand load (rows 0..7, four consecutive lanes
@@ -840,11 +862,13 @@ __device__ __forceinline__ uint32_t esc_bf16(uint32_t bits) {
 
 // Interior block from its staged region, all vectors: d[0..3] receive the block's sums in the
 // m16n8k16 accumulator layout (vector lane/4 rows 2(lane%4), +1 in d0, d1; vector lane/4 + 8 in
-// d2, d3). x0/x1 = this thread's two vectors (from the block's first column), or null past nb.
+// d2, d3). The activations come from the CTA's staged slice at xs (shared address) when the
+// block's column block is staged, else from global memory at x0/x1 (this thread's two vectors
+// from the block's first column); v0/v1: those vectors exist (< nb).
 template <int ELEM>
 __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
-                                          uint32_t tile, const uint16_t *x0, const uint16_t *x1, float (&d)[4],
-                                          bool &bad) {
+                                          uint32_t tile, bool staged_x, uint32_t xs, const uint16_t *x0,
+                                          const uint16_t *x1, bool v0, bool v1, float (&d)[4], bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -880,15 +904,6 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
-        // A operands of the group's eight products: columns 4g..4g+3 of lane 4j + t, as BF16
-        // pairs (cols 0, 1 -> k = 2t, 2t + 1; cols 2, 3 -> k = 2t + 8, 2t + 9)
-        uint2 xa[8], xb8[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int col = (4 * j + (int)t) * kLaneCols + 4 * g;
-            xa[j] = x0 ? __ldg(reinterpret_cast<const uint2 *>(x0 + col)) : make_uint2(0u, 0u);
-            xb8[j] = x1 ? __ldg(reinterpret_cast<const uint2 *>(x1 + col)) : make_uint2(0u, 0u);
-        }
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
@@ -921,14 +936,28 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
             asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)esc_bf16<ELEM>(esc_bits(e))) : "memory");
         }
         __syncwarp();
+        // A operands: columns 4g..4g+3 of lane 4j + t as BF16 pairs (cols 0, 1 -> k = 2t, 2t + 1;
+        // cols 2, 3 -> k = 2t + 8, 2t + 9); B: the same columns of row gid, from the tile
 #pragma unroll
         for (int j = 0; j < 8; j++) {
+            const uint32_t L = 4u * (uint32_t)j + t;
             uint32_t b0, b1;
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                          : "=r"(b0), "=r"(b1)
-                         : "r"(brow + 8u * ((4u * (uint32_t)j + t) ^ (4u * gid)))
+                         : "r"(brow + 8u * (L ^ (4u * gid)))
                          : "memory");
-            mma_bf16(acc[j & 1], xa[j].x, xb8[j].x, xa[j].y, xb8[j].y, b0, b1);
+            uint2 a = make_uint2(0u, 0u), a8 = make_uint2(0u, 0u);
+            if (staged_x) {
+                const uint32_t u = 4u * L + (uint32_t)g;
+                if (v0) asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a.x), "=r"(a.y) : "r"(xs + xs_off(gid, u)) : "memory");
+                if (v1)
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a8.x), "=r"(a8.y) : "r"(xs + xs_off(gid + 8, u)) : "memory");
+            } else {
+                const int col = (int)L * kLaneCols + 4 * g;
+                if (v0) a = __ldg(reinterpret_cast<const uint2 *>(x0 + col));
+                if (v1) a8 = __ldg(reinterpret_cast<const uint2 *>(x1 + col));
+            }
+            mma_bf16(acc[j & 1], a.x, a8.x, a.y, a8.y, b0, b1);
         }
         __syncwarp();
     }
@@ -951,8 +980,25 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16);
     uint8_t *stage = smem + kBatchStageOff + warp * kStageBytes;
     const uint32_t tile = smem_u32(smem + kBatchTileOff + warp * kTileBytes);
-    const uint64_t total_warps = (uint64_t)gridDim.x * kBatchWarps;
-    uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
+    const uint32_t xs0 = smem_u32(smem + kBatchXOff);
+    // The CTA takes a contiguous range of positions p in column-block-major order (block
+    // (rb, cb) at p = cb * rbs + rb), so its warps mostly share one column block, whose
+    // activations it stages once in shared memory (two slices: the range may cross one
+    // boundary). Warp w takes positions start + w, start + w + warps, ...
+    const uint64_t per = (m.nb + gridDim.x - 1) / gridDim.x;
+    const uint64_t start = (uint64_t)blockIdx.x * per;
+    const uint64_t end = start + per < m.nb ? start + per : m.nb;
+    const uint64_t cb_first = start / m.rbs;
+    uint64_t p = start + (uint64_t)warp;
+    // (rb, cb) of position p, stepped without division; (rbn, cbn) of the next position
+    uint64_t cb = p / m.rbs, rb = p % m.rbs;
+    auto step = [&](uint64_t &r, uint64_t &c) {
+        r += kBatchWarps;
+        while (r >= m.rbs) {
+            r -= m.rbs;
+            c += 1;
+        }
+    };
     uint32_t phase = 0;
     bool bad = false, timed_out = false;
     const int gid = lane >> 2, t = lane & 3;
@@ -989,17 +1035,34 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    if (b < m.nb) issue(b, false);
+    if (p < end) issue(rb * m.cbs + cb, false);
     load_rank_table(m, rexp);
     build_lut<ELEM>(m, lut);
-    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // stage the activations of column blocks cb_first and cb_first + 1 (whole 16-byte pieces
+    // inside K; the rest of a slice is only read for interior blocks, which lie inside K)
+    for (uint32_t i = threadIdx.x; i < 2u * (uint32_t)nb * (kCols / 8); i += blockDim.x) {
+        const uint32_t slot = i / ((uint32_t)nb * (kCols / 8)), rem = i % ((uint32_t)nb * (kCols / 8));
+        const uint32_t v = rem / (kCols / 8), c8 = rem % (kCols / 8);  // columns 8 c8 .. 8 c8 + 7
+        const uint64_t col = (cb_first + slot) * kCols + 8 * (uint64_t)c8;
+        if (col + 8 > m.k) continue;
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)v * ld_x + (int64_t)col));
+        // columns 8 c8.. are lane c8 / 2, groups 2 (c8 & 1) and 2 (c8 & 1) + 1: units 2 c8, 2 c8 + 1
+        const uint32_t xs = xs0 + slot * (uint32_t)kXSlice;
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(xs + xs_off(v, 2 * c8)), "r"(q.x), "r"(q.y) : "memory");
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(xs + xs_off(v, 2 * c8 + 1)), "r"(q.z), "r"(q.w) : "memory");
+    }
+    __syncthreads();
 
-    while (b < m.nb) {
-        const uint64_t nxt = b + total_warps;
+    while (p < end) {
+        const uint64_t b = rb * m.cbs + cb;
+        const uint64_t pn = p + kBatchWarps;
+        uint64_t rbn = rb, cbn = cb;
+        step(rbn, cbn);
+        const uint64_t bn = rbn * m.cbs + cbn;
         __syncwarp();
-        if (nxt < m.nb && lane == 0) {
-            const uint32_t s0 = m.tab[nxt], s1 = m.tab[nxt + 1];
+        if (pn < end && lane == 0) {
+            const uint32_t s0 = m.tab[bn], s1 = m.tab[bn + 1];
             asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(m.data + 16 * (uint64_t)s0),
                          "r"(16 * (s1 - s0))
                          : "memory");
@@ -1017,21 +1080,23 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             phase ^= 1u;
             reg = stage;
         }
-        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         if (interior && staged) {
             const uint16_t *xc = x + cb * kCols;
-            const uint16_t *x0 = gid < nb ? xc + (int64_t)gid * ld_x : nullptr;
-            const uint16_t *x1 = gid + 8 < nb ? xc + (int64_t)(gid + 8) * ld_x : nullptr;
+            const bool v0 = gid < nb, v1 = gid + 8 < nb;
+            const uint16_t *x0 = xc + (int64_t)(v0 ? gid : 0) * ld_x;
+            const uint16_t *x1 = xc + (int64_t)(v1 ? gid + 8 : 0) * ld_x;
+            const bool staged_x = cb == cb_first || cb == cb_first + 1;
+            const uint32_t xs = xs0 + (cb == cb_first ? 0u : (uint32_t)kXSlice);
             float d[4];
-            block_mma<ELEM>(stage, bytes, lane, lut, tile, x0, x1, d, bad);
+            block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
             const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;  // interior: both rows < n
-            if (gid < nb) {
+            if (v0) {
                 emit(gid, r0, cb, d[0]);
                 emit(gid, r0 + 1, cb, d[1]);
             }
-            if (gid + 8 < nb) {
+            if (v1) {
                 emit(gid + 8, r0, cb, d[2]);
                 emit(gid + 8, r0 + 1, cb, d[3]);
             }
@@ -1058,24 +1123,59 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
             if (ticket == (uint32_t)m.cbs - 1) {
                 __syncwarp();
-                // row lane % 8; lane / 8 sums column blocks lane / 8, + 4, ...
-                const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
-                for (int v = 0; v < nb; v++) {
+                // (vector, row) pairs i, vector i / 8, row i % 8, summed over the column blocks in a
+                // fixed order with all loads in flight together. Up to 16 pairs (nb <= 2): lanes
+                // i + np * sub (np = 8 or 16) sum column blocks sub, sub + 32 / np, ... and two or
+                // one shuffle steps add those; more pairs: lane sums pairs lane + 32 k whole.
+                const int pairs = nb * kRows;
+                if (pairs <= 16) {
+                    const int np = pairs <= 8 ? 8 : 16, S = 32 / np;
+                    const int i = lane & (np - 1), sub = lane / np;
+                    const uint64_t r2 = rb * kRows + (uint64_t)(i & 7);
+                    const bool live = i < pairs && r2 < m.n;
+                    const float *pp = partial + (uint64_t)(i >> 3) * m.cbs * n_pad + r2;
                     float sv = 0.0f;
-                    if (r2 < m.n)
-                        for (uint64_t c2 = (uint64_t)(lane >> 3); c2 < m.cbs; c2 += 4)
-                            sv += __ldcg(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
-                    sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 8);
+#pragma unroll 4
+                    for (uint64_t c2 = (uint64_t)sub; c2 < m.cbs; c2 += (uint64_t)S)
+                        if (live) sv += __ldcg(pp + c2 * n_pad);
+                    if (S == 4) sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 8);
                     sv += __shfl_xor_sync(0xFFFFFFFFu, sv, 16);
-                    if (lane < kRows && r2 < m.n)
-                        y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
+                    if (sub == 0 && live)
+                        y[(int64_t)(i >> 3) * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
+                } else {
+                    float sv[kBatchMax * kRows / 32];
+                    bool live[kBatchMax * kRows / 32];
+                    const float *pp[kBatchMax * kRows / 32];
+#pragma unroll
+                    for (int k2 = 0; k2 < kBatchMax * kRows / 32; k2++) {
+                        const int i = lane + 32 * k2, v = i >> 3;
+                        const uint64_t r2 = rb * kRows + (uint64_t)(i & 7);
+                        live[k2] = v < nb && r2 < m.n;
+                        pp[k2] = partial + (uint64_t)v * m.cbs * n_pad + r2;
+                        sv[k2] = 0.0f;
+                    }
+#pragma unroll 4
+                    for (uint64_t c2 = 0; c2 < m.cbs; c2++) {
+#pragma unroll
+                        for (int k2 = 0; k2 < kBatchMax * kRows / 32; k2++)
+                            if (live[k2]) sv[k2] += __ldcg(pp[k2] + c2 * n_pad);
+                    }
+#pragma unroll
+                    for (int k2 = 0; k2 < kBatchMax * kRows / 32; k2++) {
+                        if (!live[k2]) continue;
+                        const int i = lane + 32 * k2, v = i >> 3;
+                        const uint64_t r2 = rb * kRows + (uint64_t)(i & 7);
+                        y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv[k2] : sv[k2] * m.scales[r2];
+                    }
                 }
                 if (lane == 0) counters[rb] = 0;
             }
         }
         __syncwarp();
-        if (nxt < m.nb) issue(nxt, true);
-        b = nxt;
+        if (pn < end) issue(bn, true);
+        p = pn;
+        rb = rbn;
+        cb = cbn;
     }
     if (timed_out) {
         raise_error(kErrTimeout);
