@@ -380,6 +380,35 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+def run_batch_only(args):
+    """Small-batch GEMV alone on the headline matrix (24 rotated copies, nb vectors): one JSON
+    line, not the benchmark contract's; used for profiling the batch kernel."""
+    import torch
+    import decode_gemv_nwc_gb300 as nwc
+    from decode_gemv_nwc_gb300 import build, synth
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    nb = args.only_batch
+    w = synth.normal_bf16((N_ROWS, K_COLS), 0.02, seed=0)
+    blob = nwc.encode(w)
+    host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+    mats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(COPIES)]
+    X = torch.from_numpy(np.stack([synth.activations_bf16(K_COLS, 1 + v) for v in range(nb)]).view(np.int16)).to(dev)
+    Y = torch.empty((nb, N_ROWS), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ms = time_graph(lambda: [m.gemv_batch(X, y=Y, stream=stream) for m in mats], stream, args.steps, args.warmup)
+    st, flags = nwc.check(stream)
+    assert st == 0, f"device error word {flags:#x}"
+    us = ms * 1e3 / COPIES
+    peak, peak_kind = peaks()
+    algo = len(blob) + 2 * K_COLS * nb + 4 * N_ROWS * nb
+    print(json.dumps({"workload": f"square {N_ROWS}x{K_COLS} BF16, {nb} vectors per GEMV, {COPIES} rotated copies",
+                      "nb": nb, "us_per_matrix": us, "us_per_matrix_vector": us / nb,
+                      "achieved_gbs": algo / (us * 1e-6) / 1e9, "frac_of_hbm": algo / (us * 1e-6) / 1e9 / peak,
+                      "peak_kind": peak_kind, "gpu_launches": args.steps * COPIES}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -388,9 +417,14 @@ def main():
     ap.add_argument("--impl", default="nwc", choices=["nwc", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--only-batch", type=int, default=0, metavar="NB",
+                    help="time only nwc_gemv_batch with NB vectors on the headline matrix")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only_batch:
+        run_batch_only(args)
+        return
 
     if args.impl == "reference":
         # the CPU oracle: rank 0 alone runs it (no GPU, no process group); other ranks exit

@@ -664,9 +664,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     // Block b goes to CTA b % grid, so every SM gets within one block of the same count.
     const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
     uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
-    // b's row and column block, stepped by (dq, dr) = total_warps / cbs, % cbs without dividing
-    uint64_t rb = b / m.cbs, cb = b % m.cbs;
-    const uint64_t dq = total_warps / m.cbs, dr = total_warps % m.cbs;
     uint32_t phase = 0;  // bit i: parity of the next completion of stage i
     bool bad = false, timed_out = false;
 
@@ -729,6 +726,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         region(b, src, bytes);
         const uint8_t *reg = src;
         const bool staged = bytes <= (uint32_t)kStageBytes;
+        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         // the fast path's first activations, loaded while the region copy completes
@@ -786,12 +784,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
             if (nxt < m.nb) issue(nxt, 0, true);
         }
         b = nxt;
-        rb += dq;
-        cb += dr;
-        if (cb >= m.cbs) {
-            cb -= m.cbs;
-            rb += 1;
-        }
     }
     if (timed_out) {
         raise_error(kErrTimeout);
