@@ -485,17 +485,11 @@ __device__ __forceinline__ void e4m3_pair_to_f32(uint32_t bf, float &w0, float &
         : "r"(codes));
 }
 
-// One row pair: two single-code lookups, assembly with the raw mantissas. No branch: an escape
-// yields its placeholder, corrected from the block's escape list. Returns the pair as packed
-// BF16 (row r in the low half; fp8: each half's high byte is the e4m3 code); fp8 also returns
-// the two values as FP32 in w0, w1.
+// Row pair from its two table entries and raw mantissas X (even t at bits 0.., odd t at 16..):
+// packed BF16 (row r in the low half; fp8: each half's high byte is the e4m3 code); fp8 also
+// returns the two values as FP32 in w0, w1.
 template <int ELEM>
-__device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
-    fs_refill(s);  // two codes take at most 24 bits; a refill leaves at least 33
-    const uint32_t e1 = lut_at(s, lutb);
-    fs_consume(s, e1);
-    const uint32_t e2 = lut_at(s, lutb);
-    fs_consume(s, e2);
+__device__ __forceinline__ uint32_t pair_bits(uint32_t e1, uint32_t e2, uint32_t X, float &w0, float &w1) {
     const uint32_t e = __byte_perm(e1, e2, 0x5410);
     uint32_t bf;
     if (ELEM == 0) {
@@ -505,6 +499,38 @@ __device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X
         e4m3_pair_to_f32(bf, w0, w1);
     }
     return bf;
+}
+
+// Four codes (two row pairs) on one refill: the refill leaves at least 33 valid bits, which four
+// codes (at most 12 bits each) exceed only rarely. No escape branch: an escape yields its
+// placeholder, corrected from the block's escape list. A lane that ran past its valid bits (the low seven
+// bits of V wrapped: bit 6 set) finds code 3's bit position from the words it inserted and the
+// valid count before code 3, reloads its window there from the staged stream and decodes codes 3
+// and 4 again. code = shared address of the lane's first code word.
+__device__ __forceinline__ void fs_quad(Fs32 &s, uint32_t lutb, uint32_t code, uint32_t (&e)[4]) {
+    fs_refill(s);
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        e[c] = lut_at(s, lutb);
+        fs_consume(s, e[c]);
+    }
+    if (__any_sync(0xFFFFFFFFu, (s.V & 64u) != 0u) && (s.V & 64u)) {
+        const uint32_t V2 = s.V + e[2] + e[3];  // V before code 3 (low seven bits)
+        const uint32_t pos = (s.pa - code) * 8u - ((V2 & 127u) + 1u);
+        const uint32_t a = code + 4u * (pos >> 5), o = pos & 31u;
+        uint32_t w0, w1;
+        asm("ld.shared.u32 %0, [%1];" : "=r"(w0) : "r"(a));
+        asm("ld.shared.u32 %0, [%1];" : "=r"(w1) : "r"(a + 4));
+        s.wh = __funnelshift_l(w1, w0, o);
+        s.wl = w1 << o;
+        s.V = 63u - o;  // 64 - o >= 33 valid bits
+        s.pa = a + 8;
+        asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
+        e[2] = lut_at(s, lutb);
+        fs_consume(s, e[2]);
+        e[3] = lut_at(s, lutb);
+        fs_consume(s, e[3]);
+    }
 }
 
 // acc0 += lo(w2) * x, acc1 += hi(w2) * x with BF16 operands and FP32 accumulation: the BF16
@@ -597,12 +623,14 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+        uint32_t e4[4];  // table entries of row pairs q, q + 1 (q even)
 #pragma unroll
         for (int q = 0; q < 16; q++) {
             const int pp = q & 3;
             const uint32_t X = xpair<F>(mw, q);
             float w0, w1;
-            const uint32_t w2 = pair_step<ELEM>(s, lutb, X, w0, w1);
+            if ((q & 1) == 0) fs_quad(s, lutb, code, e4);
+            const uint32_t w2 = pair_bits<ELEM>(e4[2 * (q & 1)], e4[2 * (q & 1) + 1], X, w0, w1);
             if (ELEM == 0) {
                 fma_bf16x2(w2, x16[q >> 2], acc[2 * pp], acc[2 * pp + 1]);
             } else {
@@ -899,11 +927,12 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
-        uint32_t w2[16];
+        uint32_t w2[16], e4[4];
 #pragma unroll
         for (int q = 0; q < 16; q++) {
             float f0, f1;
-            w2[q] = pair_step<ELEM>(s, lutb, xpair<F>(mw, q), f0, f1);
+            if ((q & 1) == 0) fs_quad(s, lutb, code, e4);
+            w2[q] = pair_bits<ELEM>(e4[2 * (q & 1)], e4[2 * (q & 1) + 1], xpair<F>(mw, q), f0, f1);
             if (ELEM == 1) w2[q] = pack_bf16x2(f0, f1);
         }
         // rows 2pp (low halves) and 2pp + 1 (high halves) of columns 0..3 (w2[4 c + pp])
