@@ -501,6 +501,18 @@ __device__ __forceinline__ uint32_t pair_bits(uint32_t e1, uint32_t e2, uint32_t
     return bf;
 }
 
+// One row pair: refill, two single-code lookups, assembly with the raw mantissas (the batch
+// GEMV's decoder; the single-vector GEMV decodes four codes per refill, below).
+template <int ELEM>
+__device__ __forceinline__ uint32_t pair_step(Fs32 &s, uint32_t lutb, uint32_t X, float &w0, float &w1) {
+    fs_refill(s);  // two codes take at most 24 bits; a refill leaves at least 33
+    const uint32_t e1 = lut_at(s, lutb);
+    fs_consume(s, e1);
+    const uint32_t e2 = lut_at(s, lutb);
+    fs_consume(s, e2);
+    return pair_bits<ELEM>(e1, e2, X, w0, w1);
+}
+
 // Four codes (two row pairs) on one refill: the refill leaves at least 33 valid bits, which four
 // codes (at most 12 bits each) exceed only rarely. No escape branch: an escape yields its
 // placeholder, corrected from the block's escape list. A lane that ran past its valid bits (the low seven
@@ -927,12 +939,11 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
-        uint32_t w2[16], e4[4];
+        uint32_t w2[16];
 #pragma unroll
         for (int q = 0; q < 16; q++) {
             float f0, f1;
-            if ((q & 1) == 0) fs_quad(s, lutb, code, e4);
-            w2[q] = pair_bits<ELEM>(e4[2 * (q & 1)], e4[2 * (q & 1) + 1], xpair<F>(mw, q), f0, f1);
+            w2[q] = pair_step<ELEM>(s, lutb, xpair<F>(mw, q), f0, f1);
             if (ELEM == 1) w2[q] = pack_bf16x2(f0, f1);
         }
         // rows 2pp (low halves) and 2pp + 1 (high halves) of columns 0..3 (w2[4 c + pp])
