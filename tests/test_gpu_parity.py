@@ -394,3 +394,13 @@ def test_gemv_batch_matches_single_vector_calls_in_tolerance_full_size():
         y1 = mat.gemv(dev_bits(xs[v])).cpu().numpy().astype(np.float64)
         bound = 2 * (TOL_REL * oracle.abs_dot(blob, xs[v], rows) + TOL_ABS)
         assert (np.abs(y1[rows] - y[v, rows]) <= bound).all()
+
+
+def test_gemv_batch_fp8_full_size_sampled():
+    """fp8 gate projection at full size, 16 vectors: sampled rows of every vector against the
+    oracle (row scales applied at the end)."""
+    w = synth.normal_bf16((9728, 2560), 0.02, seed=150)
+    blob = nwc.encode(w, elem=nwc.FP8)
+    xs = [synth.activations_bf16(2560, 500 + v) for v in range(16)]
+    rows = np.sort(np.random.default_rng(9).choice(9728, 256, False))
+    batch_check(blob, xs, rows=rows)
