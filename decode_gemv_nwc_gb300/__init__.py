@@ -191,7 +191,8 @@ class Matrix:
 
     def gemv_batch(self, x, y=None, stream=None):
         """Y (float32[nb, N]) = W x[v] for the nb <= 16 rows of x (BF16 [nb, K] as an int16/bfloat16
-        CUDA tensor, row stride a multiple of 8): one fused pass that decodes every weight once.
+        CUDA tensor, row stride a multiple of 8): one fused pass that decodes every weight once
+        (one vector: the single-vector kernel).
         The batch workspace (sized for 16 vectors) is allocated and prepared on first use."""
         import torch
         assert x.dim() == 2 and x.shape[1] == self.k and x.is_cuda and x.stride(1) == 1

@@ -1643,12 +1643,11 @@ extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws
     return cudaMemsetAsync(counters, 0, 4 * (size_t)mp->row_blocks, s) == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 
-extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
-                               nwc_stream stream) {
-    if (!mp || !x || !y || !ws) return NWC_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
-    if (ws_bytes < nwc_gemv_workspace_bytes(mp)) return NWC_ERR_INVALID_ARG;
-    const Mat m = to_mat(*mp);
+namespace {
+// The single-vector GEMV on `partial` (col_blocks x n_pad floats) and `counters` (row_blocks,
+// zero); arguments already checked.
+nwc_status launch_gemv(const Mat &m, const uint16_t *x, float *y, float *partial, uint32_t *counters,
+                       uint64_t n_pad, cudaStream_t stream) {
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
     static bool smem_ok[2] = {false, false};
@@ -1656,10 +1655,6 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     std::call_once(once[0], [] { smem_ok[0] = set_smem(gemv_kernel<0>, kGemvSmem); });
     std::call_once(once[1], [] { smem_ok[1] = set_smem(gemv_kernel<1>, kGemvSmem); });
     if (!smem_ok[m.elem]) return NWC_ERR_CUDA;
-    const uint64_t n_pad = pad_rows(*mp);
-    uint8_t *w8 = static_cast<uint8_t *>(ws);
-    float *partial = reinterpret_cast<float *>(w8);
-    uint32_t *counters = reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp));
     const uint64_t slots = (uint64_t)sms * kCtasPerSm;
     const int grid = (int)(m.nb < slots ? m.nb : slots);
     // Programmatic dependent launch: the kernel may start while the previous kernel on the stream
@@ -1668,7 +1663,7 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kGemvWarps * 32);
     cfg.dynamicSmemBytes = kGemvSmem;
-    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1678,6 +1673,18 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
                          ? cudaLaunchKernelEx(&cfg, gemv_kernel<0>, m, x, y, partial, counters, n_pad)
                          : cudaLaunchKernelEx(&cfg, gemv_kernel<1>, m, x, y, partial, counters, n_pad);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                               nwc_stream stream) {
+    if (!mp || !x || !y || !ws) return NWC_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
+    if (ws_bytes < nwc_gemv_workspace_bytes(mp)) return NWC_ERR_INVALID_ARG;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    return launch_gemv(to_mat(*mp), x, y, reinterpret_cast<float *>(w8),
+                       reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp)), pad_rows(*mp),
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- small-batch GEMV
@@ -1733,11 +1740,17 @@ extern "C" nwc_status nwc_gemv_batch(const nwc_matrix *mp, const uint16_t *x, in
     if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
     if (ws_bytes < nwc_gemv_batch_workspace_bytes(mp, nb)) return NWC_ERR_INVALID_ARG;
     const Mat m = to_mat(*mp);
+    const uint64_t n_pad = pad_rows(*mp);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (nb == 1) {
+        // one vector: the single-vector kernel, on the batch workspace's counters and partials
+        uint8_t *w8 = static_cast<uint8_t *>(ws);
+        return launch_gemv(m, x, y, reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0)),
+                           reinterpret_cast<uint32_t *>(w8), n_pad, s);
+    }
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
-    const uint64_t n_pad = pad_rows(*mp);
     const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const cudaError_t rc = m.elem == NWC_ELEM_BF16 ? launch_batch<0>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s)
                                                    : launch_batch<1>(m, x, ld_x, nb, y, ld_y, ws, n_pad, grid, s);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;

@@ -214,7 +214,8 @@ nwc_status nwc_gemv_batch_prepare(const nwc_matrix *m, int nb, void *ws, size_t 
  * 16-byte aligned, ld_x >= K and a multiple of 8. y: FP32 [nb][ld_y], ld_y >= N. Each y[v]
  * meets nwc_gemv's bound for its own vector (the sum order differs from nwc_gemv's). ws/ws_bytes:
  * a workspace prepared by nwc_gemv_batch_prepare for this matrix and at least nb vectors. nb
- * outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. For nb == 1, nwc_gemv is faster.
+ * outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. nb == 1 runs nwc_gemv's kernel (on
+ * this workspace), with nwc_gemv's result bit for bit.
  */
 nwc_status nwc_gemv_batch(const nwc_matrix *m, const uint16_t *x, int64_t ld_x, int nb, float *y,
                           int64_t ld_y, void *ws, size_t ws_bytes, nwc_stream stream);

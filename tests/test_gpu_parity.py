@@ -404,3 +404,16 @@ def test_gemv_batch_fp8_full_size_sampled():
     xs = [synth.activations_bf16(2560, 500 + v) for v in range(16)]
     rows = np.sort(np.random.default_rng(9).choice(9728, 256, False))
     batch_check(blob, xs, rows=rows)
+
+
+def test_gemv_batch_one_vector_equals_gemv_bitwise():
+    """nwc_gemv_batch with one vector runs the single-vector kernel on the batch workspace."""
+    w = synth.normal_bf16((300, 2600), 0.02, seed=88)
+    mat = nwc.Matrix(nwc.encode(w))
+    x = synth.activations_bf16(2600, 89)
+    xb = np.zeros((1, 2608), np.uint16)
+    xb[0, :2600] = x
+    yb = mat.gemv_batch(dev_bits(xb)[:, :2600]).cpu().numpy()
+    y1 = mat.gemv(dev_bits(x)).cpu().numpy()
+    assert_clean()
+    assert np.array_equal(yb[0].view(np.uint32), y1.view(np.uint32))
