@@ -310,6 +310,17 @@ static_assert(kGemvSmem <= 232448, "shared memory per CTA");
 constexpr int kCtasPerSm = (32 / kGemvWarps) < (233472 / (kGemvSmem + 1024)) ? (32 / kGemvWarps)
                                                                                : (233472 / (kGemvSmem + 1024));
 static_assert(kCtasPerSm >= 1, "one CTA per SM at least");
+// The GEMV kernel for NB vectors at once (1 or 2): two vectors need a second accumulator set, so
+// 24 warps per SM with up to 85 registers each and one stage per warp.
+template <int NB>
+struct GemvCfg {
+    static constexpr int kWarps = NB == 1 ? kGemvWarps : 24;
+    static constexpr int kStages = NB == 1 ? kStagesPerWarp : 1;
+    static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
+    static constexpr int kSmem = kStageOff + kWarps * kStages * kStageBytes;
+    static constexpr int kCtas = NB == 1 ? kCtasPerSm : 1;
+};
+static_assert(GemvCfg<2>::kSmem <= 232448, "shared memory per CTA");
 // Decode: 16 warps per SM with up to 128 registers each, so that a lane holds its whole 8x16
 // output tile and writes every 32-byte row segment with full-sector stores. Gather keeps one
 // row per lane and runs 32 warps.
@@ -594,9 +605,10 @@ __device__ __forceinline__ void esc_correct(const uint32_t *list, uint32_t slots
 
 // Interior block from its staged region (`bytes` long): 4 groups of 4 columns (16 row pairs
 // each); the group loop stays rolled so the hot loop fits the instruction cache.
-template <int ELEM>
+template <int ELEM, int NB>
 __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
-                                           const uint16_t *xb, uint2 xq, float (&acc)[8], bool &bad) {
+                                           const uint16_t *xb, int64_t ld_x, uint2 (&xq)[NB], float (&acc)[NB][8],
+                                           bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
     constexpr int MWG = MW / 4;              // words per group of 4 columns
@@ -624,14 +636,23 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
         asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
     }
     const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
-    const uint2 *xp = reinterpret_cast<const uint2 *>(xb + lane * kLaneCols);
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
-        const uint2 xn = __ldg(xp + (g < 3 ? g + 1 : 3));
-        // the group's four activations: BF16 bits (BF16 path) and FP32 (fp8 path)
-        const uint32_t x16[4] = {xq.x & 0xFFFFu, xq.x >> 16, xq.y & 0xFFFFu, xq.y >> 16};
-        const float xf[4] = {__uint_as_float(xq.x << 16), __uint_as_float(xq.x & 0xFFFF0000u),
-                             __uint_as_float(xq.y << 16), __uint_as_float(xq.y & 0xFFFF0000u)};
+        uint2 xn[NB];
+        uint32_t x16[NB][4];  // the group's four activations of each vector: BF16 bits (BF16 path)
+        float xf[NB][4];      // and FP32 (fp8 path)
+#pragma unroll
+        for (int v = 0; v < NB; v++) {
+            xn[v] = __ldg(reinterpret_cast<const uint2 *>(xb + v * ld_x + lane * kLaneCols) + (g < 3 ? g + 1 : 3));
+            x16[v][0] = xq[v].x & 0xFFFFu;
+            x16[v][1] = xq[v].x >> 16;
+            x16[v][2] = xq[v].y & 0xFFFFu;
+            x16[v][3] = xq[v].y >> 16;
+            xf[v][0] = __uint_as_float(xq[v].x << 16);
+            xf[v][1] = __uint_as_float(xq[v].x & 0xFFFF0000u);
+            xf[v][2] = __uint_as_float(xq[v].y << 16);
+            xf[v][3] = __uint_as_float(xq[v].y & 0xFFFF0000u);
+        }
         uint32_t mw[MWG];
 #pragma unroll
         for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
@@ -643,25 +664,31 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
             float w0, w1;
             if ((q & 1) == 0) fs_quad(s, lutb, code, e4);
             const uint32_t w2 = pair_bits<ELEM>(e4[2 * (q & 1)], e4[2 * (q & 1) + 1], X, w0, w1);
-            if (ELEM == 0) {
-                fma_bf16x2(w2, x16[q >> 2], acc[2 * pp], acc[2 * pp + 1]);
-            } else {
-                const float xc = xf[q >> 2];
-                const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
-                                            make_float2(acc[2 * pp], acc[2 * pp + 1]));
-                acc[2 * pp] = r.x;
-                acc[2 * pp + 1] = r.y;
+#pragma unroll
+            for (int v = 0; v < NB; v++) {
+                if (ELEM == 0) {
+                    fma_bf16x2(w2, x16[v][q >> 2], acc[v][2 * pp], acc[v][2 * pp + 1]);
+                } else {
+                    const float xc = xf[v][q >> 2];
+                    const float2 r = __ffma2_rn(make_float2(w0, w1), make_float2(xc, xc),
+                                                make_float2(acc[v][2 * pp], acc[v][2 * pp + 1]));
+                    acc[v][2 * pp] = r.x;
+                    acc[v][2 * pp + 1] = r.y;
+                }
             }
         }
-        xq = xn;
+#pragma unroll
+        for (int v = 0; v < NB; v++) xq[v] = xn[v];
     }
     // consumed bits = 32 * words inserted - valid bits
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
     bad |= inserted - valid > 32u * lw;
     const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
-    esc_correct<ELEM>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0, lane,
-                      xb, kRows, kCols, acc, bad);
+#pragma unroll
+    for (int v = 0; v < NB; v++)
+        esc_correct<ELEM>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0, lane,
+                          xb + v * ld_x, kRows, kCols, acc[v], bad);
 }
 
 // Any block (edge, or a region too large to stage) from shared or global memory; escaped
@@ -686,10 +713,13 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes
     bad |= ls.overrun();
 }
 
-template <int ELEM>
-__global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
-    gemv_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, float *partial, uint32_t *counters,
-                uint64_t n_pad) {
+// y[v] = W x[v] for NB vectors (1 or 2; vector v at x + v ld_x, its result at y + v ld_y, its
+// partial sums at partial + v col_blocks n_pad).
+template <int ELEM, int NB>
+__global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
+    gemv_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, float *__restrict__ y, int64_t ld_y,
+                float *partial, uint32_t *counters, uint64_t n_pad) {
+    using C = GemvCfg<NB>;
     // A kernel launched after this one with programmatic stream serialization may start as soon
     // as SMs free up; it waits (griddepcontrol.wait) before touching anything this one writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -698,11 +728,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     uint8_t *rexp = smem + kRexpOff;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t bar0 = smem_u32(smem + kBarOff + warp * 16), bar1 = bar0 + 8;
-    uint8_t *stage0 = smem + kStageOff + warp * kStagesPerWarp * kStageBytes,
-            *stage1 = stage0 + (kStagesPerWarp - 1) * kStageBytes;
+    uint8_t *stage0 = smem + C::kStageOff + warp * C::kStages * kStageBytes,
+            *stage1 = stage0 + (C::kStages - 1) * kStageBytes;
 
     // Block b goes to CTA b % grid, so every SM gets within one block of the same count.
-    const uint64_t total_warps = (uint64_t)gridDim.x * kGemvWarps;
+    const uint64_t total_warps = (uint64_t)gridDim.x * C::kWarps;
     uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
     uint32_t phase = 0;  // bit i: parity of the next completion of stage i
     bool bad = false, timed_out = false;
@@ -748,10 +778,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
     // belong to the kernel before this one on the stream: wait for it to complete.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int it = 0; b < m.nb; it++) {
-        const int cur = kStagesPerWarp == 2 ? (it & 1) : 0;
+        const int cur = C::kStages == 2 ? (it & 1) : 0;
         const uint64_t nxt = b + total_warps;
         __syncwarp();
-        if (kStagesPerWarp == 2) {
+        if (C::kStages == 2) {
             if (nxt < m.nb) issue(nxt, cur ^ 1, it > 0);
         } else if (nxt < m.nb && lane == 0) {
             const uint8_t *nsrc;
@@ -770,8 +800,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         const int rows = real_rows(m.n, rb);
         const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
         // the fast path's first activations, loaded while the region copy completes
-        uint2 xq0 = make_uint2(0u, 0u);
-        if (interior && staged) xq0 = __ldg(reinterpret_cast<const uint2 *>(x + cb * kCols + lane * kLaneCols));
+        uint2 xq0[NB];
+#pragma unroll
+        for (int v = 0; v < NB; v++) {
+            xq0[v] = make_uint2(0u, 0u);
+            if (interior && staged)
+                xq0[v] = __ldg(reinterpret_cast<const uint2 *>(x + v * ld_x + cb * kCols + lane * kLaneCols));
+        }
         if (staged) {
             const uint32_t bar = cur ? bar1 : bar0;
             if (!mbar_wait(bar, (phase >> cur) & 1u)) {
@@ -781,22 +816,32 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
             phase ^= 1u << cur;
             reg = cur ? stage1 : stage0;
         }
-        float acc[8];
+        float acc[NB][8];
 #pragma unroll
-        for (int r = 0; r < 8; r++) acc[r] = 0.0f;
+        for (int v = 0; v < NB; v++)
+#pragma unroll
+            for (int r = 0; r < 8; r++) acc[v][r] = 0.0f;
         if (interior && staged) {
-            block_fast<ELEM>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, xq0, acc, bad);
+            block_fast<ELEM, NB>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad);
         } else {
-            block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + cb * kCols, acc, bad);
+#pragma unroll
+            for (int v = 0; v < NB; v++)
+                block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + v * ld_x + cb * kCols, acc[v],
+                                    bad);
         }
-        const float sum = transpose_reduce(acc, lane);
         const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
         const uint64_t row = rb * kRows + (uint64_t)row_in;
         const bool writer = (lane & 3) == 0 && row < m.n;
-        if (m.cbs == 1) {
-            if (writer) y[row] = ELEM == 0 ? sum : sum * m.scales[row];
-        } else {
-            if (writer) partial[cb * n_pad + row] = sum;
+#pragma unroll
+        for (int v = 0; v < NB; v++) {
+            const float sum = transpose_reduce(acc[v], lane);
+            if (m.cbs == 1) {
+                if (writer) y[v * ld_y + (int64_t)row] = ELEM == 0 ? sum : sum * m.scales[row];
+            } else {
+                if (writer) partial[(v * m.cbs + cb) * n_pad + row] = sum;
+            }
+        }
+        if (m.cbs > 1) {
             __syncwarp();
             uint32_t ticket = 0;
             // Release: the warp's partial sums (ordered before lane 0 by the warp barrier) are
@@ -810,16 +855,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
                 // row lane % 8; lane / 8 sums column blocks lane / 8, + 4, ... (loads in
                 // parallel across the warp), then a fixed shuffle order adds the four
                 const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
-                float s = 0.0f;
-                if (r2 < m.n)
-                    for (uint64_t c2 = (uint64_t)(lane >> 3); c2 < m.cbs; c2 += 4) s += __ldcg(partial + c2 * n_pad + r2);
-                s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
-                s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
-                if (lane < kRows && r2 < m.n) y[r2] = ELEM == 0 ? s : s * m.scales[r2];
+#pragma unroll
+                for (int v = 0; v < NB; v++) {
+                    const float *pv = partial + (uint64_t)v * m.cbs * n_pad;
+                    float s = 0.0f;
+                    if (r2 < m.n)
+                        for (uint64_t c2 = (uint64_t)(lane >> 3); c2 < m.cbs; c2 += 4) s += __ldcg(pv + c2 * n_pad + r2);
+                    s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
+                    s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
+                    if (lane < kRows && r2 < m.n) y[v * ld_y + (int64_t)r2] = ELEM == 0 ? s : s * m.scales[r2];
+                }
                 if (lane == 0) counters[rb] = 0;
             }
         }
-        if (kStagesPerWarp == 1) {
+        if (C::kStages == 1) {
             __syncwarp();
             if (nxt < m.nb) issue(nxt, 0, true);
         }
@@ -829,7 +878,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, kCtasPerSm)
         raise_error(kErrTimeout);
         // let this warp's own copies land before the CTA's shared memory goes away
         mbar_wait(bar0, phase & 1u);
-        if (kStagesPerWarp == 2) mbar_wait(bar1, (phase >> 1) & 1u);
+        if (C::kStages == 2) mbar_wait(bar1, (phase >> 1) & 1u);
     }
     if (bad) raise_error(kErrFormat);
 }
@@ -1644,34 +1693,44 @@ extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws
 }
 
 namespace {
-// The single-vector GEMV on `partial` (col_blocks x n_pad floats) and `counters` (row_blocks,
-// zero); arguments already checked.
-nwc_status launch_gemv(const Mat &m, const uint16_t *x, float *y, float *partial, uint32_t *counters,
-                       uint64_t n_pad, cudaStream_t stream) {
-    const int sms = sm_count();
-    if (sms <= 0) return NWC_ERR_CUDA;
-    static bool smem_ok[2] = {false, false};
-    static std::once_flag once[2];
-    std::call_once(once[0], [] { smem_ok[0] = set_smem(gemv_kernel<0>, kGemvSmem); });
-    std::call_once(once[1], [] { smem_ok[1] = set_smem(gemv_kernel<1>, kGemvSmem); });
-    if (!smem_ok[m.elem]) return NWC_ERR_CUDA;
-    const uint64_t slots = (uint64_t)sms * kCtasPerSm;
+template <int ELEM, int NB>
+cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, float *partial,
+                           uint32_t *counters, uint64_t n_pad, int sms, cudaStream_t stream) {
+    using C = GemvCfg<NB>;
+    static bool smem_ok = false;
+    static std::once_flag once;
+    std::call_once(once, [] { smem_ok = set_smem(gemv_kernel<ELEM, NB>, C::kSmem); });
+    if (!smem_ok) return cudaErrorInvalidConfiguration;
+    const uint64_t slots = (uint64_t)sms * C::kCtas;
     const int grid = (int)(m.nb < slots ? m.nb : slots);
     // Programmatic dependent launch: the kernel may start while the previous kernel on the stream
     // finishes; it streams its first block regions and builds its decode table meanwhile.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kGemvWarps * 32);
-    cfg.dynamicSmemBytes = kGemvSmem;
+    cfg.blockDim = dim3(C::kWarps * 32);
+    cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t rc = m.elem == NWC_ELEM_BF16
-                         ? cudaLaunchKernelEx(&cfg, gemv_kernel<0>, m, x, y, partial, counters, n_pad)
-                         : cudaLaunchKernelEx(&cfg, gemv_kernel<1>, m, x, y, partial, counters, n_pad);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<ELEM, NB>, m, x, ld_x, y, ld_y, partial, counters, n_pad);
+}
+
+// The GEMV for nb = 1 or 2 vectors on `partial` (nb x col_blocks x n_pad floats) and `counters`
+// (row_blocks, zero); arguments already checked.
+nwc_status launch_gemv(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, int nb, float *partial,
+                       uint32_t *counters, uint64_t n_pad, cudaStream_t stream) {
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    cudaError_t rc;
+    if (nb == 1)
+        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream)
+                                     : launch_gemv_nb<1, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream);
+    else
+        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream)
+                                     : launch_gemv_nb<1, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 }  // namespace
@@ -1682,7 +1741,7 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
     if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
     if (ws_bytes < nwc_gemv_workspace_bytes(mp)) return NWC_ERR_INVALID_ARG;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    return launch_gemv(to_mat(*mp), x, y, reinterpret_cast<float *>(w8),
+    return launch_gemv(to_mat(*mp), x, 0, y, 0, 1, reinterpret_cast<float *>(w8),
                        reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp)), pad_rows(*mp),
                        reinterpret_cast<cudaStream_t>(stream));
 }
@@ -1742,10 +1801,11 @@ extern "C" nwc_status nwc_gemv_batch(const nwc_matrix *mp, const uint16_t *x, in
     const Mat m = to_mat(*mp);
     const uint64_t n_pad = pad_rows(*mp);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (nb == 1) {
-        // one vector: the single-vector kernel, on the batch workspace's counters and partials
+    if (nb <= 2) {
+        // one or two vectors: the GEMV kernel (FMA per vector), on the batch workspace's counters
+        // and partials
         uint8_t *w8 = static_cast<uint8_t *>(ws);
-        return launch_gemv(m, x, y, reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0)),
+        return launch_gemv(m, x, ld_x, y, ld_y, nb, reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0)),
                            reinterpret_cast<uint32_t *>(w8), n_pad, s);
     }
     const int sms = sm_count();

@@ -215,7 +215,8 @@ nwc_status nwc_gemv_batch_prepare(const nwc_matrix *m, int nb, void *ws, size_t 
  * meets nwc_gemv's bound for its own vector (the sum order differs from nwc_gemv's). ws/ws_bytes:
  * a workspace prepared by nwc_gemv_batch_prepare for this matrix and at least nb vectors. nb
  * outside [1, NWC_GEMV_BATCH_MAX] is NWC_ERR_INVALID_ARG. nb == 1 runs nwc_gemv's kernel (on
- * this workspace), with nwc_gemv's result bit for bit.
+ * this workspace), with nwc_gemv's result bit for bit; nb == 2 runs it with a second accumulator
+ * set (FMAs per vector), which is faster than the tensor-core path for two vectors.
  */
 nwc_status nwc_gemv_batch(const nwc_matrix *m, const uint16_t *x, int64_t ld_x, int nb, float *y,
                           int64_t ld_y, void *ws, size_t ws_bytes, nwc_stream stream);
