@@ -1,5 +1,5 @@
 // kernels.cu -- sm_103a kernels and C-ABI launchers: decode to BF16/e4m3, embedding gather,
-// and the fused decode-GEMV.
+// the fused decode-GEMV (one or two vectors) and the small-batch GEMV (up to 16 vectors).
 //
 // "NWC -- Neural Weight Compression", section "How it works":
 //   * each lane decodes its own bit stream for a block of 8 rows x 512 columns (16 columns
@@ -21,13 +21,17 @@
 // b % grid); each warp streams whole block regions (counts, code streams, mantissas, escape
 // list) from HBM into its own shared-memory stage with one TMA bulk copy (cp.async.bulk,
 // completion on an mbarrier, bounded waits) and prefetches its next region into L2; every CTA
-// builds the 4096-entry table in shared memory while its first copies are in flight; the LUT
+// builds the 4096-entry table in shared memory while its first copies are in flight; a lane
+// decodes four codes per window refill (the table yields one code per peek: a second code from
+// the same peek would be incomplete too often for a SIMT warp); the LUT
 // entry carries the code as a BF16 high half so that one LOP3 merges a row pair's two raw
 // mantissas (stored 16 bits apart) into a BF16x2, which feeds FMAs with BF16 operands and FP32
 // accumulators (fp8: packed FP32 FMA). Cross-column-block sums are done by the last warp to
 // finish a row block (one counter per row block, reset by that warp), in a fixed order. The
 // kernel is launched with programmatic stream serialization: it may start while the previous
 // kernel on the stream drains and waits for it before touching x, the workspace or y.
+// The small-batch GEMV keeps the decoder and moves the products with three or more vectors to
+// the tensor cores (mma.sync on decoded tiles staged in shared memory).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
