@@ -208,3 +208,42 @@ def test_batch_gemv_workspace_and_argument_checks():
     st, m1 = bind_host(nwc.encode(synth.normal_bf16((9, 500), 0.02, seed=4)))
     assert st == 0 and L.nwc_gemv_batch_workspace_bytes(ctypes.byref(m1), 16) == 16
     assert nwc.BATCH_MAX == 16
+
+
+def flip_code_bits(blob, seed, blocks=6, flips=3):
+    """The blob with `flips` random bits flipped in the code streams of `blocks` random blocks:
+    the structure (header, tables, region sizes, escape lists) is unchanged, so host validation
+    still accepts it; only decoding can tell."""
+    b = bytearray(blob)
+    a = np.frombuffer(bytes(blob), np.uint8)
+    nb = int(a[24:32].view(np.uint64)[0])
+    off_data = int(a[48:56].view(np.uint64)[0])
+    tab = a[80:80 + 4 * (nb + 1)].view(np.uint32)
+    rng = np.random.default_rng(seed)
+    for i in rng.choice(nb, min(blocks, nb), replace=False):
+        start = off_data + 16 * int(tab[i])
+        code_bytes = 4 * int(a[start:start + 32].astype(np.int64).sum())
+        for bit in rng.choice(8 * code_bytes, min(flips, 8 * code_bytes), replace=False):
+            b[start + 32 + bit // 8] ^= 1 << (bit % 8)
+    return bytes(b)
+
+
+@pytest.mark.parametrize("elem", [0, 1])
+def test_code_bit_flips_pass_validation_and_the_oracle_never_crashes(elem):
+    """Flipped code bits keep the blob structurally valid; the oracle decoder then either
+    reports a malformed blob or decodes some other matrix of the same shape."""
+    from oracle import decode as oracle_decode
+    w = synth.normal_bf16((64, 1100), 0.02, seed=31)
+    blob = nwc.encode(w, elem=elem)
+    outcomes = set()
+    for seed in range(12):
+        bad = flip_code_bits(blob, seed)
+        assert bad != blob
+        assert nwc.lib().nwc_validate(np.frombuffer(bad, np.uint8).ctypes.data_as(ctypes.c_void_p), len(bad)) == 0
+        try:
+            q = oracle_decode(bad)[0]
+            assert q.shape == w.shape
+            outcomes.add("decoded")
+        except ValueError:
+            outcomes.add("rejected")
+    assert "rejected" in outcomes  # most flips break a lane's bit count or escape pattern
