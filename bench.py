@@ -68,48 +68,73 @@ def recorded_traffic(workload_key):
 
 
 class ClockSampler:
-    """SM clocks and throttle reasons sampled every 100 ms (nvidia-smi loop mode) while running."""
+    """SM clocks and throttle reasons from nvidia-smi's loop mode (every 20 ms, timestamped),
+    read by a thread. start() returns once the first sample arrived (or after 5 s); summary()
+    keeps the samples taken inside a wall-clock window (the timed region)."""
 
-    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Q = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.samples = []
+        self.samples = []  # (epoch seconds, [sm, max, hw, hw_thermal, sw_thermal, sw_power])
+        self.thread = None
 
-    def __enter__(self):
+    def _read(self):
+        import datetime
+        for line in self.proc.stdout:
+            vals = [v.strip() for v in line.split(",")]
+            if len(vals) != 7:
+                continue
+            try:
+                ts = datetime.datetime.strptime(vals[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            self.samples.append((ts, vals[1:]))
+
+    def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t_end = time.time() + 5.0
+        while not self.samples and time.time() < t_end:
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *a):
+    def stop(self):
         if self.proc is None:
             return
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=10)
+            self.proc.wait(timeout=10)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        for line in out.splitlines():
-            vals = [v.strip() for v in line.split(",")]
-            if len(vals) == 6:
-                self.samples.append(vals)
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        if not self.samples:
+    def summary(self, t0, t1):
+        inside = [v for ts, v in self.samples if t0 - 0.005 <= ts <= t1 + 0.005]
+        where = "timed region"
+        if not inside and self.samples:  # region shorter than the interval: the nearest sample
+            inside = [min(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[1]]
+            where = "nearest sample"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        sm = [float(v[0]) for v in inside if v[0].replace(".", "").isdigit()]
+        mx = [float(v[1]) for v in inside if v[1].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[2 + i].lower() == "active"})
+        reasons = sorted({names[i] for v in inside for i in range(4) if v[2 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+                "reasons": reasons, "samples": len(inside), "interval_ms": self.INTERVAL_MS, "window": where}
 
 
 def dist_setup(gpus):
@@ -457,6 +482,7 @@ def main():
     with torch.cuda.graph(graph, stream=stream):
         for i, m in enumerate(mats):
             m.gemv(xd, y=ys[i], stream=stream)
+    clocks = ClockSampler(local).start()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -466,13 +492,16 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            ev1.record(stream)
-        ev1.synchronize()
+    t_on = time.time()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    t_off = time.time()
+    time.sleep(2.5 * ClockSampler.INTERVAL_MS / 1000)  # the sample covering the region's end
+    clocks.stop()
     torch.cuda.synchronize()
     barrier(world)
     ms_local = ev0.elapsed_time(ev1)
@@ -554,7 +583,7 @@ def main():
                "sample": f"{n} runs of decode + FP64 matvec of one 4096x4096 blob (single-threaded C)"}
 
     traffic = recorded_traffic("square4096")
-    clk = clocks.summary()
+    clk = clocks.summary(t_on, t_off)
     # the pages' decoder metric: SM clocks spent per 64 decoded weights, all SMs together
     f_sm = (clk.get("sm_mhz") or clk.get("sm_max_mhz") or 0) * 1e6
     clocks_per_64w = us_per_launch * 1e-6 * f_sm * nwc.sm_count() / (N_ROWS * K_COLS / 64) if f_sm else None
