@@ -434,6 +434,56 @@ def run_batch_only(args):
                       "peak_kind": peak_kind, "gpu_launches": args.steps * COPIES}))
 
 
+def run_only(args):
+    """One workload of the pages' configurations alone (few launches, for profiling): the
+    lm_head GEMV of the 151936x2560 table, the gather of 4096 ids from it, or the fp8 gate /
+    down GEMV (12 rotated copies). One JSON line, not the benchmark contract's."""
+    import torch
+    import decode_gemv_nwc_gb300 as nwc
+    from decode_gemv_nwc_gb300 import build, synth
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    peak, peak_kind = peaks()
+    name = args.only
+    if name in ("lm_head", "gather"):
+        w = synth.normal_bf16((synth.VOCAB, synth.HIDDEN), 0.02, 7, device=dev)
+        blob = encode_on_host(w)
+        del w
+        m = nwc.Matrix(blob, device=dev)
+        if name == "lm_head":
+            x = torch.from_numpy(synth.activations_bf16(synth.HIDDEN, 9).view(np.int16)).to(dev)
+            y = torch.empty(synth.VOCAB, dtype=torch.float32, device=dev)
+            ms = time_graph(lambda: m.gemv(x, y=y, stream=stream), stream, args.steps, args.warmup)
+            gbs = len(blob) / (ms * 1e-3) / 1e9
+            out = {"workload": "lm_head GEMV 151936x2560", "us": ms * 1e3, "compressed_gbs": gbs,
+                   "frac_of_hbm": gbs / peak}
+        else:
+            ids = torch.from_numpy(synth.token_ids(4096, synth.VOCAB, seed=8)).to(dev)
+            g = torch.empty((4096, synth.HIDDEN), dtype=torch.int16, device=dev)
+            ms = time_graph(lambda: m.gather(ids, out=g, stream=stream), stream, args.steps, args.warmup)
+            out = {"workload": "gather 4096 ids from the 151936x2560 table", "us": ms * 1e3,
+                   "rows_per_s": 4096 / (ms * 1e-3)}
+    else:
+        n, k = (9728, 2560) if name == "fp8_gate" else (2560, 9728)
+        w = synth.normal_bf16((n, k), 0.02, 50 + n, device=dev)
+        blob = encode_on_host(w, elem=1)
+        host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+        mats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(12)]
+        x = torch.from_numpy(synth.activations_bf16(k, 77).view(np.int16)).to(dev)
+        y = torch.empty(n, dtype=torch.float32, device=dev)
+        ms = time_graph(lambda: [mm.gemv(x, y=y, stream=stream) for mm in mats], stream, args.steps,
+                        args.warmup) / len(mats)
+        gbs = len(blob) / (ms * 1e-3) / 1e9
+        out = {"workload": f"fp8 e4m3 {name[4:]} {n}x{k}, 12 rotated copies", "us": ms * 1e3,
+               "compressed_gbs": gbs, "frac_of_hbm": gbs / peak}
+    st, flags = nwc.check(stream)
+    assert st == 0, f"device error word {flags:#x}"
+    out["peak_kind"] = peak_kind
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,11 +494,16 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--only-batch", type=int, default=0, metavar="NB",
                     help="time only nwc_gemv_batch with NB vectors on the headline matrix")
+    ap.add_argument("--only", choices=["lm_head", "gather", "fp8_gate", "fp8_down"],
+                    help="time only this workload (few launches; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.only_batch:
         run_batch_only(args)
+        return
+    if args.only:
+        run_only(args)
         return
 
     if args.impl == "reference":
