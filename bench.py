@@ -654,6 +654,7 @@ def main():
                        "graph": True, "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
+                         "frac_of_nominal_7900": achieved / 7900.0,
                          "traffic": traffic, "algorithmic_bytes_per_launch": algo_bytes,
                          "us_per_launch": us_per_launch},
             "decompressed_gbs": 2 * N_ROWS * K_COLS / (us_per_launch * 1e-6) / 1e9,
