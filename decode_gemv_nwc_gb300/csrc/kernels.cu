@@ -901,7 +901,8 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
 #define NWC_BATCH_WARPS 20
 #endif
 constexpr int kBatchWarps = NWC_BATCH_WARPS;
-constexpr int kTileBytes = 8 * 32 * 8;  // 8 rows x 32 lanes x 4 columns x BF16
+constexpr int kTileRow = 32 * 8 + 32;  // 32 lanes x 4 columns x BF16, padded by 32 bytes
+constexpr int kTileBytes = 8 * kTileRow;
 constexpr int kBatchStageOff = (kBarOff + kBatchWarps * 2 * 8 + 127) / 128 * 128;
 constexpr int kBatchTileOff = kBatchStageOff + kBatchWarps * kStageBytes;
 constexpr int kBatchMax = 16;
@@ -916,10 +917,11 @@ static_assert(kBatchMax == NWC_GEMV_BATCH_MAX, "vectors per call");
 // gid, four lanes) fall in 16 distinct units per half-warp.
 __device__ __forceinline__ uint32_t xs_off(uint32_t v, uint32_t u) { return v * (uint32_t)(kCols * 2) + 8u * (u ^ (v & 3u)); }
 
-// Byte offset in a warp's tile of row r, lane L's 4 columns (8 bytes). The 8-byte unit is
-// L ^ 4r: a row's stores (32 lanes) and an mma operand load (rows 0..7, four consecutive lanes
-// per row) each touch 16 distinct units per half-warp, so neither has bank conflicts.
-__device__ __forceinline__ uint32_t tile_off(uint32_t r, uint32_t L) { return r * 256u + 8u * (L ^ (4u * r)); }
+// Byte offset in a warp's tile of row r, lane L's 4 columns (8 bytes). Rows are 288 bytes apart
+// (36 8-byte units, 4 mod 16): a row's stores (32 consecutive units) and an mma operand load
+// (rows 0..3 or 4..7 of a half-warp, four consecutive lanes each) both touch 16 distinct bank
+// pairs per half-warp, and the operand of product j sits 32 j bytes after that of product 0.
+__device__ __forceinline__ uint32_t tile_off(uint32_t r, uint32_t L) { return r * (uint32_t)kTileRow + 8u * L; }
 
 // d += A . B for one m16n8k16 tile: a0..a3 and b0, b1 in the PTX fragment layout (BF16 pairs),
 // FP32 accumulators.
@@ -984,8 +986,8 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     const uint32_t slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
     const uint32_t *list = reinterpret_cast<const uint32_t *>(reg + esc0);
     const uint32_t gid = (uint32_t)lane >> 2, t = (uint32_t)lane & 3u;
-    // this thread's operand row in every group: row gid of lane 4j + t
-    const uint32_t brow = tile + gid * 256u;
+    // this thread's B operand of product j in every group: row gid, lane 4j + t (32 j bytes on)
+    const uint32_t bbase = tile + tile_off(gid, t);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
@@ -1022,21 +1024,27 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
         }
         __syncwarp();
         // A operands: columns 4g..4g+3 of lane 4j + t as BF16 pairs (cols 0, 1 -> k = 2t, 2t + 1;
-        // cols 2, 3 -> k = 2t + 8, 2t + 9); B: the same columns of row gid, from the tile
+        // cols 2, 3 -> k = 2t + 8, 2t + 9); B: the same columns of row gid, from the tile. In the
+        // staged slice these are units 16 j + 4 t + g, whose swizzle (^ (gid & 3)) touches only the
+        // low two bits: product j's A operand sits 128 j bytes after product 0's.
+        const uint32_t abase = xs + xs_off(gid, 4u * t + (uint32_t)g);
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             const uint32_t L = 4u * (uint32_t)j + t;
             uint32_t b0, b1;
             asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
                          : "=r"(b0), "=r"(b1)
-                         : "r"(brow + 8u * (L ^ (4u * gid)))
+                         : "r"(bbase + 32u * (uint32_t)j)
                          : "memory");
             uint2 a = make_uint2(0u, 0u), a8 = make_uint2(0u, 0u);
             if (staged_x) {
-                const uint32_t u = 4u * L + (uint32_t)g;
-                if (v0) asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a.x), "=r"(a.y) : "r"(xs + xs_off(gid, u)) : "memory");
+                const uint32_t aj = abase + 128u * (uint32_t)j;
+                if (v0) asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a.x), "=r"(a.y) : "r"(aj) : "memory");
                 if (v1)
-                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a8.x), "=r"(a8.y) : "r"(xs + xs_off(gid + 8, u)) : "memory");
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                                 : "=r"(a8.x), "=r"(a8.y)
+                                 : "r"(aj + 8u * (uint32_t)kCols * 2u)
+                                 : "memory");
             } else {
                 const int col = (int)L * kLaneCols + 4 * g;
                 if (v0) a = __ldg(reinterpret_cast<const uint2 *>(x0 + col));
