@@ -1,6 +1,6 @@
 /*
- * nwc.h -- C ABI of the GB300 (sm_103a) library for batch-1 matrix-vector products over
- * losslessly entropy-coded BF16 (and fp8 e4m3) weight matrices.
+ * nwc.h -- C ABI of the GB300 (sm_103a) library for batch-1 (and small-batch) matrix-vector
+ * products over losslessly entropy-coded BF16 (and fp8 e4m3) weight matrices.
  *
  * What the calls compute is defined by two pages:
  *   "NWC -- Neural Weight Compression" (PyPI project page, v0.9.0), section "How it works":
@@ -27,6 +27,9 @@
  *   - Matrices are row-major: element (n, k) of an N x K matrix is at index n*ld + k.
  *     N = output features (rows), K = input features (columns), ld >= K.
  *   - BF16 values are passed as their 16-bit patterns (uint16_t); x is BF16, y is FP32.
+ *   - Any call may come from any host thread. Calls that share a workspace (or the one
+ *     scratch array of nwc_gemv_noalloc) must not overlap on the GPU; order them on one
+ *     stream or with events. The device error word is per device, shared by all streams.
  */
 #ifndef NWC_H
 #define NWC_H
