@@ -1310,23 +1310,30 @@ __device__ __forceinline__ uint2 row_words(uint32_t a, uint32_t b, uint32_t c, u
     return make_uint2(__byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410), 0u);
 }
 
-// One lane's 16-column row segment (BF16: 8 words, fp8: 4 words) to out[at ..]: two (one)
-// 16-byte stores when vec (out and the row stride keep 16-byte alignment), else element-wise.
+// One lane's 16-column row segment (BF16: 8 words, fp8: 4 words) to out[at ..]: with vec = 2
+// (out and the row stride keep 16-byte alignment) two (one) 16-byte stores, with vec = 1 (8-byte
+// alignment) four (two) 8-byte stores, else element-wise.
 template <int ELEM>
-__device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32_t (&w)[8], bool vec) {
+__device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32_t (&w)[8], int vec) {
     if (ELEM == 0) {
         uint16_t *o = static_cast<uint16_t *>(out) + at;
-        if (vec) {
+        if (vec == 2) {
             reinterpret_cast<uint4 *>(o)[0] = make_uint4(w[0], w[1], w[2], w[3]);
             reinterpret_cast<uint4 *>(o)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else if (vec == 1) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) reinterpret_cast<uint2 *>(o)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; i++) o[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
         }
     } else {
         uint8_t *o = static_cast<uint8_t *>(out) + at;
-        if (vec) {
+        if (vec == 2) {
             *reinterpret_cast<uint4 *>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if (vec == 1) {
+            reinterpret_cast<uint2 *>(o)[0] = make_uint2(w[0], w[1]);
+            reinterpret_cast<uint2 *>(o)[1] = make_uint2(w[2], w[3]);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; i++) o[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
@@ -1339,7 +1346,7 @@ __device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32
 template <int ELEM, int MODE>
 __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                             void *out, int64_t ld_out, uint64_t row0, uint64_t col0, int want,
-                                            bool vec, bool &bad) {
+                                            int vec, bool &bad) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -1580,7 +1587,7 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
             const int rows = real_rows(m.n, rb);
             const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
             if (interior && staged)
-                unpack_fast<ELEM, MODE>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec != 0, bad);
+                unpack_fast<ELEM, MODE>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad);
             else
                 unpack_generic<ELEM, MODE>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, out, ld_out, orow, col0, want,
                                            bad);
@@ -1645,10 +1652,13 @@ nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, voi
 }
 
 // A lane's 16-column row segment is stored with 16-byte stores when every row start keeps that
-// alignment.
+// alignment (2), with 8-byte stores when rows keep 8-byte alignment (1), else element by element.
 int vec_ok(const void *out, int64_t ld_out, int elem) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(out);
-    return elem == NWC_ELEM_BF16 ? ((a % 16) == 0 && (ld_out % 8) == 0) : ((a % 16) == 0 && (ld_out % 16) == 0);
+    const int64_t per16 = elem == NWC_ELEM_BF16 ? 8 : 16;  // elements in 16 bytes
+    if ((a % 16) == 0 && (ld_out % per16) == 0) return 2;
+    if ((a % 8) == 0 && (ld_out % (per16 / 2)) == 0) return 1;
+    return 0;
 }
 
 }  // namespace

@@ -483,3 +483,29 @@ def test_tiny_shape_sweep_decode_gemv_batch():
             assert np.array_equal(mat.decode().cpu().numpy().view(np.uint16), w), (n, k)
             gemv_check(blob, synth.activations_bf16(k, n + k), mat=mat)
             batch_check(blob, [synth.activations_bf16(k, n + k + v) for v in range(3)], mat=mat)
+
+
+def test_decode_and_gather_8_byte_aligned_rows():
+    """Row strides that keep 8-byte but not 16-byte alignment (BF16 K + 4, fp8 K + 8) take the
+    8-byte store path; the padding columns keep their sentinel."""
+    n, k = 40, 2600
+    w = _escape_heavy((n, k), 41)
+    mat = nwc.Matrix(nwc.encode(w))
+    big = torch.full((n, k + 4), -7, dtype=torch.int16, device="cuda")
+    mat.decode(out=big[:, :k])
+    assert_clean()
+    got = big.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, :k], w) and (got[:, k:] == np.uint16(0xFFF9)).all()
+    ids = np.array([39, 0, 17, 17, 8, 33], np.int32)
+    gbig = torch.full((len(ids), k + 4), -7, dtype=torch.int16, device="cuda")
+    mat.gather(torch.from_numpy(ids).cuda(), out=gbig[:, :k])
+    assert_clean()
+    g = gbig.cpu().numpy().view(np.uint16)
+    assert np.array_equal(g[:, :k], w[ids]) and (g[:, k:] == np.uint16(0xFFF9)).all()
+    q, sc = oracle.quantize_fp8(w)
+    m8 = nwc.Matrix(nwc.encode_fp8(q, sc))
+    out8 = torch.full((n, k + 8), 0xAB, dtype=torch.uint8, device="cuda")
+    m8.decode(out=out8[:, :k])
+    assert_clean()
+    o = out8.cpu().numpy()
+    assert np.array_equal(o[:, :k], q) and (o[:, k:] == 0xAB).all()
