@@ -607,12 +607,26 @@ __device__ __forceinline__ void esc_correct(const uint32_t *list, uint32_t slots
     }
 }
 
-// Interior block from its staged region (`bytes` long): 4 groups of 4 columns (16 row pairs
-// each); the group loop stays rolled so the hot loop fits the instruction cache.
-template <int ELEM, int NB>
+// Four activations (columns c0 .. c0 + 3 of a column block starting at xv) as BF16 pairs;
+// columns at or past kc (the block's real columns) read as 0.
+__device__ __forceinline__ uint2 x4_load(const uint16_t *xv, int c0, int kc) {
+    if (c0 + 4 <= kc) return __ldg(reinterpret_cast<const uint2 *>(xv + c0));
+    uint32_t e[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) e[j] = c0 + j < kc ? (uint32_t)__ldg(xv + c0 + j) : 0u;
+    return make_uint2(e[0] | e[1] << 16, e[2] | e[3] << 16);
+}
+
+// Block from its staged region (`bytes` long), all 8 rows real: 4 groups of 4 columns (16 row
+// pairs each); the group loop stays rolled so the hot loop fits the instruction cache.
+// EDGE: the block's last real column is kc - 1 < 511 (K ragged). Every lane still holds 128
+// codes (fillers for columns past K), and the real columns' mantissa fields sit where they sit in
+// a full block, but the lanes' mantissa regions follow one another unless all have the same word
+// count; activations past K read as 0, so the fillers add nothing.
+template <int ELEM, int NB, bool EDGE = false>
 __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                            const uint16_t *xb, int64_t ld_x, uint2 (&xq)[NB], float (&acc)[NB][8],
-                                           bool &bad) {
+                                           bool &bad, int kc = kCols) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
     constexpr int MWG = MW / 4;              // words per group of 4 columns
@@ -626,8 +640,27 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
     const uint32_t code = regs + 32 + 4 * (incl - lw);
-    // interior block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
-    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
+    // full block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
+    const uint32_t man0 = (uint32_t)up16(32 + 4 * (uint64_t)total);
+    uint32_t man = regs + man0 + (uint32_t)lane * 4, mstride = 4 * kLanes, esc0 = man0 + kLanes * MW * 4;
+    uint32_t mwords = MW;  // this lane's mantissa words (EDGE: only these are read)
+    if (EDGE) {
+        const int cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
+        const uint32_t mw = man_words(kRows, cols, F);
+        mwords = mw;
+        uint32_t mincl = mw;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            uint32_t o = __shfl_up_sync(0xFFFFFFFFu, mincl, d);
+            if (lane >= d) mincl += o;
+        }
+        const bool uniform = __all_sync(0xFFFFFFFFu, mw == __shfl_sync(0xFFFFFFFFu, mw, 0));
+        if (!uniform) {
+            man = regs + man0 + 4 * (mincl - mw);
+            mstride = 4;
+        }
+        esc0 = man0 + 4 * __shfl_sync(0xFFFFFFFFu, mincl, 31);
+    }
     Fs32 s;
     {
         uint32_t w0 = 0, w1 = 0;
@@ -647,7 +680,8 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
         float xf[NB][4];      // and FP32 (fp8 path)
 #pragma unroll
         for (int v = 0; v < NB; v++) {
-            xn[v] = __ldg(reinterpret_cast<const uint2 *>(xb + v * ld_x + lane * kLaneCols) + (g < 3 ? g + 1 : 3));
+            if (EDGE) xn[v] = x4_load(xb + v * ld_x, lane * kLaneCols + 4 * (g < 3 ? g + 1 : 3), kc);
+            else xn[v] = __ldg(reinterpret_cast<const uint2 *>(xb + v * ld_x + lane * kLaneCols) + (g < 3 ? g + 1 : 3));
             x16[v][0] = xq[v].x & 0xFFFFu;
             x16[v][1] = xq[v].x >> 16;
             x16[v][2] = xq[v].y & 0xFFFFu;
@@ -659,7 +693,12 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
         }
         uint32_t mw[MWG];
 #pragma unroll
-        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+        for (int i = 0; i < MWG; i++) {
+            const uint32_t kw = (uint32_t)(MWG * g + i);
+            mw[i] = 0;
+            if (!EDGE || kw < mwords)
+                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+        }
         uint32_t e4[4];  // table entries of row pairs q, q + 1 (q even)
 #pragma unroll
         for (int q = 0; q < 16; q++) {
@@ -688,11 +727,10 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
     bad |= inserted - valid > 32u * lw;
-    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
 #pragma unroll
     for (int v = 0; v < NB; v++)
         esc_correct<ELEM>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0, lane,
-                          xb + v * ld_x, kRows, kCols, acc[v], bad);
+                          xb + v * ld_x, kRows, kc, acc[v], bad);
 }
 
 // Any block (edge, or a region too large to stage) from shared or global memory; escaped
@@ -802,14 +840,17 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
         const bool staged = bytes <= (uint32_t)kStageBytes;
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
-        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
+        const uint64_t kc64 = m.k - cb * kCols;
+        const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
+        // full rows: the fast decoder (for a ragged K only when filler codes, which decode to
+        // rank 0 with a garbage mantissa, cannot be Inf or NaN, so that times 0 they add 0)
+        const bool fast = rows == kRows && staged && (kc == kCols || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu));
         // the fast path's first activations, loaded while the region copy completes
         uint2 xq0[NB];
 #pragma unroll
         for (int v = 0; v < NB; v++) {
             xq0[v] = make_uint2(0u, 0u);
-            if (interior && staged)
-                xq0[v] = __ldg(reinterpret_cast<const uint2 *>(x + v * ld_x + cb * kCols + lane * kLaneCols));
+            if (fast) xq0[v] = x4_load(x + v * ld_x + cb * kCols, lane * kLaneCols, kc);
         }
         if (staged) {
             const uint32_t bar = cur ? bar1 : bar0;
@@ -825,8 +866,10 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
         for (int v = 0; v < NB; v++)
 #pragma unroll
             for (int r = 0; r < 8; r++) acc[v][r] = 0.0f;
-        if (interior && staged) {
+        if (fast && kc == kCols) {
             block_fast<ELEM, NB>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad);
+        } else if (fast) {
+            block_fast<ELEM, NB, true>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad, kc);
         } else {
 #pragma unroll
             for (int v = 0; v < NB; v++)
