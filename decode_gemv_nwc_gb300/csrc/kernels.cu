@@ -1384,12 +1384,25 @@ __device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32
     }
 }
 
-// Interior block from its staged region. Decode writes rows row0 .. row0 + 7; gather writes
-// row `want` of the block to output row row0. col0 = the lane's first column.
-template <int ELEM, int MODE>
+// The first `cols` columns (< 16) of a lane's row segment, element by element.
+template <int ELEM>
+__device__ __forceinline__ void store_row_part(void *out, uint64_t at, const uint32_t (&w)[8], int cols) {
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        if (i >= cols) break;
+        if (ELEM == 0) static_cast<uint16_t *>(out)[at + i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
+        else static_cast<uint8_t *>(out)[at + i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
+    }
+}
+
+// Block from its staged region, all 8 rows real. Decode writes rows row0 .. row0 + 7; gather
+// writes row `want` of the block to output row row0. col0 = the lane's first column. EDGE: the
+// block's real columns end at kc < 512 (ragged K): lane-contiguous mantissa regions unless all
+// lanes have the same word count, and only the real columns are written.
+template <int ELEM, int MODE, bool EDGE = false>
 __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                             void *out, int64_t ld_out, uint64_t row0, uint64_t col0, int want,
-                                            int vec, bool &bad) {
+                                            int vec, bool &bad, int kc = kCols) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -1403,8 +1416,28 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
     const uint32_t code = regs + 32 + 4 * (incl - lw);
-    // interior block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
-    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
+    // full block: every lane has MW mantissa words, interleaved (word k of lane l at 32k + l)
+    const uint32_t man0 = (uint32_t)up16(32 + 4 * (uint64_t)total);
+    uint32_t man = regs + man0 + (uint32_t)lane * 4, mstride = 4 * kLanes, esc0e = 0;
+    uint32_t mwords = MW;
+    int cols = kLaneCols;
+    if (EDGE) {
+        cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
+        const uint32_t mw = man_words(kRows, cols, F);
+        mwords = mw;
+        uint32_t mincl = mw;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            uint32_t o = __shfl_up_sync(0xFFFFFFFFu, mincl, d);
+            if (lane >= d) mincl += o;
+        }
+        const bool uniform = __all_sync(0xFFFFFFFFu, mw == __shfl_sync(0xFFFFFFFFu, mw, 0));
+        if (!uniform) {
+            man = regs + man0 + 4 * (mincl - mw);
+            mstride = 4;
+        }
+        esc0e = man0 + 4 * __shfl_sync(0xFFFFFFFFu, mincl, 31);
+    }
     Fs32 s;
     {
         uint32_t w0 = 0, w1 = 0;
@@ -1425,7 +1458,12 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     auto group = [&](int g) {
         uint32_t mw[MWG];
 #pragma unroll
-        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+        for (int i = 0; i < MWG; i++) {
+            const uint32_t kw = (uint32_t)(MWG * g + i);
+            mw[i] = 0;
+            if (!EDGE || kw < mwords)
+                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+        }
         uint32_t p[16];  // p[c4 * 4 + pp]: rows (2pp, 2pp + 1) at column 4g + c4
 #pragma unroll
         for (int q = 0; q < 16; q++) p[q] = unpack_pair<ELEM>(s, lutb, xpair<F>(mw, q), flags);
@@ -1469,24 +1507,33 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
 #pragma unroll 1
         for (int g = 0; g < 4; g++) group(g);
     }
-    if (MODE == 0) {
+    if (!EDGE || cols == kLaneCols) {
+        if (MODE == 0) {
 #pragma unroll
-        for (int r = 0; r < 8; r++) store_row16<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], vec);
-    } else {
-        store_row16<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], vec);
+            for (int r = 0; r < 8; r++) store_row16<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], vec);
+        } else {
+            store_row16<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], vec);
+        }
+    } else if (cols > 0) {
+        if (MODE == 0) {
+#pragma unroll
+            for (int r = 0; r < 8; r++) store_row_part<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], cols);
+        } else {
+            store_row_part<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], cols);
+        }
     }
     const uint32_t valid = (s.V & 127u) + 1u;
     const uint32_t inserted = (s.pa - code) * 8u;
     bad |= inserted - valid > 32u * lw;
     // escaped elements over their placeholders: this lane's slice of the list
     LaneRegion lr;
-    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
+    const uint32_t esc0 = EDGE ? esc0e : (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
     lr.esc = reinterpret_cast<const uint32_t *>(reg + esc0);
     lr.slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
     const uint32_t n_esc = flags >> 24;
     const uint32_t start = esc_slice(lr, n_esc, lane, bad);
     const uint64_t lane_col = col0;
-    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, kRows, kLaneCols, MODE == 0 ? -1 : want, out, ld_out,
+    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, kRows, cols, MODE == 0 ? -1 : want, out, ld_out,
                          MODE == 0 ? (int64_t)row0 : (int64_t)row0 - want, lane_col))
         bad = true;
 }
@@ -1516,7 +1563,7 @@ __device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t byte
         bad = true;
 }
 
-template <int ELEM, int MODE>
+template <int ELEM, int MODE, bool EDGEK = false>
 __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
     unpack_kernel(Mat m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1628,10 +1675,23 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
             }
             const uint64_t rb = b / m.cbs;
             const int rows = real_rows(m.n, rb);
-            const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
-            if (interior && staged)
+            const uint64_t kc64 = m.k - cb * kCols;
+            const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
+            bool done = false;
+            if (rows == kRows && staged && kc == kCols) {
                 unpack_fast<ELEM, MODE>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad);
-            else
+                done = true;
+            }
+            // blocks of a ragged K with full rows: the fast decoder, in a kernel of their own
+            // (EDGEK) so that the regular decode keeps its registers; gather (64 registers) and
+            // fp8 decode take the generic path for them
+            if constexpr (EDGEK && MODE == 0 && ELEM == 0) {
+                if (!done && rows == kRows && staged) {
+                    unpack_fast<ELEM, MODE, true>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad, kc);
+                    done = true;
+                }
+            }
+            if (!done)
                 unpack_generic<ELEM, MODE>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, out, ld_out, orow, col0, want,
                                            bad);
         }
@@ -1679,7 +1739,7 @@ uint64_t pad_rows(const nwc_matrix &m) { return (uint64_t)m.row_blocks * kRows; 
 extern "C" int nwc_sm_count(void) { return sm_count(); }
 
 namespace {
-template <int ELEM, int MODE>
+template <int ELEM, int MODE, bool EDGEK = false>
 nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, void *out, int64_t ld_out, int vec,
                          cudaStream_t s) {
     const int sms = sm_count();
@@ -1687,10 +1747,10 @@ nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, voi
     static bool smem_ok = false;
     static std::once_flag once;
     using C = UnpackCfg<MODE>;
-    std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE>, C::kSmem); });
+    std::call_once(once, [] { smem_ok = set_smem(unpack_kernel<ELEM, MODE, EDGEK>, C::kSmem); });
     if (!smem_ok) return NWC_ERR_CUDA;
     const int grid = (int)(n_items < (uint64_t)sms ? n_items : (uint64_t)sms);
-    unpack_kernel<ELEM, MODE><<<grid, C::kWarps * 32, C::kSmem, s>>>(m, ids, n_items, out, ld_out, vec);
+    unpack_kernel<ELEM, MODE, EDGEK><<<grid, C::kWarps * 32, C::kSmem, s>>>(m, ids, n_items, out, ld_out, vec);
     return launched();
 }
 
@@ -1711,8 +1771,10 @@ extern "C" nwc_status nwc_decode(const nwc_matrix *mp, void *out, int64_t ld_out
     const Mat m = to_mat(*mp);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vec = vec_ok(out, ld_out, m.elem);
-    const nwc_status st = m.elem == NWC_ELEM_BF16 ? launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s)
-                                                  : launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
+    const bool k_rag = (m.k % kCols) != 0;
+    const nwc_status st = m.elem != NWC_ELEM_BF16 ? launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s)
+                          : k_rag                 ? launch_unpack<0, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
+                                                  : launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
     if (st != NWC_OK) return st;
     if (m.elem == NWC_ELEM_FP8_E4M3 && scales_out) {
         if (cudaMemcpyAsync(scales_out, m.scales, 4 * m.n, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
