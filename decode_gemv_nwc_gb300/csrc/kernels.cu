@@ -995,10 +995,14 @@ __device__ __forceinline__ uint32_t esc_bf16(uint32_t bits) {
 // d2, d3). The activations come from the CTA's staged slice at xs (shared address) when the
 // block's column block is staged, else from global memory at x0/x1 (this thread's two vectors
 // from the block's first column); v0/v1: those vectors exist (< nb).
-template <int ELEM>
+// EDGE: the block's real columns end at kc < 512 (ragged K; all 8 rows real): lane-contiguous
+// mantissa regions unless all lanes have the same word count, and activations past K are 0 (the
+// staged slice is zero-filled there, global loads are masked), so filler codes add nothing.
+template <int ELEM, bool EDGE = false>
 __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                           uint32_t tile, bool staged_x, uint32_t xs, const uint16_t *x0,
-                                          const uint16_t *x1, bool v0, bool v1, float (&d)[4], bool &bad) {
+                                          const uint16_t *x1, bool v0, bool v1, float (&d)[4], bool &bad,
+                                          int kc = kCols) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -1012,7 +1016,26 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const uint32_t regs = (uint32_t)__cvta_generic_to_shared(reg);
     const uint32_t code = regs + 32 + 4 * (incl - lw);
-    const uint32_t man = regs + (uint32_t)up16(32 + 4 * (uint64_t)total) + (uint32_t)lane * 4;
+    const uint32_t man0 = (uint32_t)up16(32 + 4 * (uint64_t)total);
+    uint32_t man = regs + man0 + (uint32_t)lane * 4, mstride = 4 * kLanes, mwords = MW;
+    uint32_t esc0 = man0 + kLanes * MW * 4;
+    if (EDGE) {
+        const int cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
+        const uint32_t mw = man_words(kRows, cols, F);
+        mwords = mw;
+        uint32_t mincl = mw;
+#pragma unroll
+        for (int dd = 1; dd < 32; dd <<= 1) {
+            uint32_t o = __shfl_up_sync(0xFFFFFFFFu, mincl, dd);
+            if (lane >= dd) mincl += o;
+        }
+        const bool uniform = __all_sync(0xFFFFFFFFu, mw == __shfl_sync(0xFFFFFFFFu, mw, 0));
+        if (!uniform) {
+            man = regs + man0 + 4 * (mincl - mw);
+            mstride = 4;
+        }
+        esc0 = man0 + 4 * __shfl_sync(0xFFFFFFFFu, mincl, 31);
+    }
     Fs32 s;
     {
         uint32_t w0 = 0, w1 = 0;
@@ -1025,7 +1048,6 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
         asm("ld.shared.u32 %0, [%1];" : "=r"(s.nw) : "r"(s.pa));
     }
     const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(lut);
-    const uint32_t esc0 = (uint32_t)up16(32 + 4 * (uint64_t)total) + kLanes * MW * 4;
     const uint32_t slots = esc0 <= bytes ? (bytes - esc0) / 4 : 0;
     const uint32_t *list = reinterpret_cast<const uint32_t *>(reg + esc0);
     const uint32_t gid = (uint32_t)lane >> 2, t = (uint32_t)lane & 3u;
@@ -1036,7 +1058,12 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     for (int g = 0; g < 4; g++) {
         uint32_t mw[MWG];
 #pragma unroll
-        for (int i = 0; i < MWG; i++) asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + 4 * kLanes * (MWG * g + i)));
+        for (int i = 0; i < MWG; i++) {
+            const uint32_t kw = (uint32_t)(MWG * g + i);
+            mw[i] = 0;
+            if (!EDGE || kw < mwords)
+                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+        }
         uint32_t w2[16];
 #pragma unroll
         for (int q = 0; q < 16; q++) {
@@ -1090,8 +1117,8 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
                                  : "memory");
             } else {
                 const int col = (int)L * kLaneCols + 4 * g;
-                if (v0) a = __ldg(reinterpret_cast<const uint2 *>(x0 + col));
-                if (v1) a8 = __ldg(reinterpret_cast<const uint2 *>(x1 + col));
+                if (v0) a = EDGE ? x4_load(x0, col, kc) : __ldg(reinterpret_cast<const uint2 *>(x0 + col));
+                if (v1) a8 = EDGE ? x4_load(x1, col, kc) : __ldg(reinterpret_cast<const uint2 *>(x1 + col));
             }
             mma_bf16(acc[j & 1], a.x, a8.x, a.y, a8.y, b0, b1);
         }
@@ -1181,8 +1208,15 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
         const uint32_t slot = i / ((uint32_t)nb * (kCols / 8)), rem = i % ((uint32_t)nb * (kCols / 8));
         const uint32_t v = rem / (kCols / 8), c8 = rem % (kCols / 8);  // columns 8 c8 .. 8 c8 + 7
         const uint64_t col = (cb_first + slot) * kCols + 8 * (uint64_t)c8;
-        if (col + 8 > m.k) continue;
-        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)v * ld_x + (int64_t)col));
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);  // past K: zeros (the fillers of a ragged K meet them)
+        if (col + 8 <= m.k) {
+            q = __ldg(reinterpret_cast<const uint4 *>(x + (int64_t)v * ld_x + (int64_t)col));
+        } else if (col < m.k) {
+            uint32_t e[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) e[j] = col + j < m.k ? (uint32_t)__ldg(x + (int64_t)v * ld_x + (int64_t)(col + j)) : 0u;
+            q = make_uint4(e[0] | e[1] << 16, e[2] | e[3] << 16, e[4] | e[5] << 16, e[6] | e[7] << 16);
+        }
         // columns 8 c8.. are lane c8 / 2, groups 2 (c8 & 1) and 2 (c8 & 1) + 1: units 2 c8, 2 c8 + 1
         const uint32_t xs = xs0 + slot * (uint32_t)kXSlice;
         asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(xs + xs_off(v, 2 * c8)), "r"(q.x), "r"(q.y) : "memory");
@@ -1217,8 +1251,11 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             reg = stage;
         }
         const int rows = real_rows(m.n, rb);
-        const bool interior = rows == kRows && (cb + 1) * kCols <= m.k;
-        if (interior && staged) {
+        const uint64_t kc64 = m.k - cb * kCols;
+        const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
+        // full rows: the tensor-core path (for a ragged K only when filler codes cannot decode
+        // to Inf or NaN, so that times 0 they add 0)
+        if (rows == kRows && staged && (kc == kCols || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu))) {
             const uint16_t *xc = x + cb * kCols;
             const bool v0 = gid < nb, v1 = gid + 8 < nb;
             const uint16_t *x0 = xc + (int64_t)(v0 ? gid : 0) * ld_x;
@@ -1226,7 +1263,8 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             const bool staged_x = cb == cb_first || cb == cb_first + 1;
             const uint32_t xs = xs0 + (cb == cb_first ? 0u : (uint32_t)kXSlice);
             float d[4];
-            block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
+            if (kc == kCols) block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
+            else block_mma<ELEM, true>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad, kc);
             const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;  // interior: both rows < n
             if (v0) {
                 emit(gid, r0, cb, d[0]);
