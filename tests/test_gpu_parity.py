@@ -509,3 +509,18 @@ def test_decode_and_gather_8_byte_aligned_rows():
     assert_clean()
     o = out8.cpu().numpy()
     assert np.array_equal(o[:, :k], q) and (o[:, k:] == 0xAB).all()
+
+
+def test_ragged_k_11008_gemv_batch_and_decode():
+    """K = 11008 (21.5 column blocks): the ragged last column block of every row block takes the
+    fast decoders (single vector, two vectors, 16 vectors on the tensor cores, decode)."""
+    n, k = 512, 11008
+    w = synth.normal_bf16((n, k), 0.02, seed=110)
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    assert np.array_equal(mat.decode().cpu().numpy().view(np.uint16), w)
+    assert_clean()
+    rows = np.sort(np.random.default_rng(11).choice(n, 192, False))
+    gemv_check(blob, synth.activations_bf16(k, 12), rows=rows, mat=mat)
+    for nb in (2, 16):
+        batch_check(blob, [synth.activations_bf16(k, 20 + v) for v in range(nb)], rows=rows, mat=mat)
