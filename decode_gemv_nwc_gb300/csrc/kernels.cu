@@ -147,6 +147,10 @@ __device__ __forceinline__ bool decode_one(S &ls, int nr, const uint8_t *rexp, u
     return esc;
 }
 
+__device__ __forceinline__ bool stream_decode(LaneStream &ls, int nr, const uint8_t *rexp, uint32_t &s, uint32_t &v) {
+    return decode_one(ls, nr, rexp, s, v);
+}
+
 // Field j of the even (odd = 0) or odd (odd = 1) mantissa half-stream of a lane region whose
 // word k is man[k * stride] (stride 32 when the block's lane regions are interleaved).
 template <int F>
@@ -182,8 +186,8 @@ __device__ __forceinline__ uint32_t elem_bits(uint32_t s, uint32_t v, uint32_t m
 // Generic decode of one lane of one block, column loop rolled and rows unrolled: calls
 // fn(c, r, s, v, m, esc) for each real element (column c, row r of the lane). rows/cols are the
 // lane's real extent. Returns the number of escape codes in the lane's 128 codes.
-template <int ELEM, class Fn>
-__device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *man, uint32_t stride, int rows,
+template <int ELEM, class S, class Fn>
+__device__ __forceinline__ uint32_t lane_rolled(S &ls, const uint32_t *man, uint32_t stride, int rows,
                                                 int cols, int nr,
                                                 const uint8_t *rexp, Fn &&fn) {
     constexpr int F = ELEM == 0 ? 7 : 3;
@@ -193,7 +197,7 @@ __device__ __forceinline__ uint32_t lane_rolled(LaneStream &ls, const uint32_t *
 #pragma unroll
         for (int r = 0; r < kRows; r++) {
             uint32_t s, v;
-            const bool esc = decode_one(ls, nr, rexp, s, v);
+            const bool esc = stream_decode(ls, nr, rexp, s, v);
             n_esc += esc;
             if (r < rows && c < cols) {
                 uint32_t m;
@@ -486,6 +490,56 @@ __device__ __forceinline__ uint32_t lut_at(const Fs32 &s, uint32_t lutb) {
     return e;
 }
 
+// The generic decoder's stream over a staged region: the fast path's window and table, one
+// lookup per code. It serves malformed streams too, so every word read is checked against
+// `limit` (the last word of the warp's stage); past it the stream reads zeros.
+template <int ELEM>
+struct LutStream {
+    Fs32 f;
+    uint32_t code, lw, lutb, limit;
+    __device__ __forceinline__ uint32_t word(uint32_t a) const {
+        uint32_t w = 0;
+        if (a <= limit) asm("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(a));
+        return w;
+    }
+    __device__ __forceinline__ void init(uint32_t code_, uint32_t lw_, uint32_t lutb_, uint32_t limit_) {
+        code = code_;
+        lw = lw_;
+        lutb = lutb_;
+        limit = limit_;
+        f.wh = lw > 0 ? word(code) : 0u;
+        f.wl = lw > 1 ? word(code + 4) : 0u;
+        f.pa = code + 8;
+        f.V = 63u;
+        f.nw = word(f.pa);
+    }
+    // at most 32 valid bits: the preloaded word goes right below them (as fs_refill)
+    __device__ __forceinline__ void refill() {
+        const uint32_t t = f.V & 127u;  // valid bits - 1
+        if (t < 32u) {
+            f.wl += f.nw << (31u - t);
+            f.wh += t == 31u ? 0u : f.nw >> (t + 1u);
+            f.pa += 4;
+            f.V += 32;
+            f.nw = word(f.pa);
+        }
+    }
+    __device__ __forceinline__ bool overrun() const {
+        const uint32_t valid = (f.V & 127u) + 1u, inserted = (f.pa - code) * 8u;
+        return inserted - valid > 32u * lw;
+    }
+};
+
+template <int ELEM>
+__device__ __forceinline__ bool stream_decode(LutStream<ELEM> &ls, int, const uint8_t *, uint32_t &s, uint32_t &v) {
+    ls.refill();  // a refill leaves at least 33 valid bits; a code takes at most 12
+    const uint32_t e = lut_at(ls.f, ls.lutb);
+    fs_consume(ls.f, e);
+    s = (e >> 15) & 1u;
+    v = ELEM == 0 ? (e >> 7) & 0xFFu : (e >> 11) & 0xFu;
+    return (e >> 24) & 1u;
+}
+
 // fp8: the row pair's two e4m3 codes (the high bytes of the halves) widened exactly to FP32
 // through the hardware e4m3x2 -> f16x2 conversion (subnormals included).
 __device__ __forceinline__ void e4m3_pair_to_f32(uint32_t bf, float &w0, float &w1) {
@@ -739,20 +793,29 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
 template <int ELEM>
 __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes, int lane, const uint8_t *rexp,
                                               int nr, int rows, uint64_t k, uint64_t cb, const uint16_t *xb,
-                                              float (&acc)[8], bool &bad) {
+                                              float (&acc)[8], bool &bad, bool staged = false, uint32_t lutb = 0) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     const int cols = real_cols(k, cb, lane);
     LaneRegion lr = lane_region(reg, bytes, lane, rows, k, cb, F);
     const uint64_t kc = k - cb * kCols;
     esc_correct<ELEM>(lr.esc, lr.slots, lane, xb, rows, kc < (uint64_t)kCols ? (int)kc : kCols, acc, bad);
     const uint16_t *xl = xb + lane * kLaneCols;
-    LaneStream ls;
-    ls.init(lr.code, lr.nwords);
-    lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, [&](int c, int r, uint32_t s, uint32_t v, uint32_t mm, bool esc) {
+    auto fma_elem = [&](int c, int r, uint32_t s, uint32_t v, uint32_t mm, bool esc) {
         const float w = esc ? esc_placeholder<ELEM>(elem_bits<ELEM>(s, 0, mm)) : elem_value<ELEM>(s, v, mm);
         acc[r] = fmaf(w, __uint_as_float((uint32_t)__ldg(xl + c) << 16), acc[r]);
-    });
-    bad |= ls.overrun();
+    };
+    if (staged) {  // codes through the shared table
+        LutStream<ELEM> ls;
+        ls.init((uint32_t)__cvta_generic_to_shared(lr.code), lr.nwords, lutb,
+                (uint32_t)__cvta_generic_to_shared(reg) + kStageBytes - 4);
+        lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, fma_elem);
+        bad |= ls.overrun();
+    } else {
+        LaneStream ls;
+        ls.init(lr.code, lr.nwords);
+        lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, fma_elem);
+        bad |= ls.overrun();
+    }
 }
 
 // y[v] = W x[v] for NB vectors (1 or 2; vector v at x + v ld_x, its result at y + v ld_y, its
@@ -874,7 +937,7 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
 #pragma unroll
             for (int v = 0; v < NB; v++)
                 block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + v * ld_x + cb * kCols, acc[v],
-                                    bad);
+                                    bad, staged, smem_u32(lut));
         }
         const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
         const uint64_t row = rb * kRows + (uint64_t)row_in;
@@ -1283,7 +1346,7 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
 #pragma unroll
                 for (int r = 0; r < 8; r++) a1[r] = 0.0f;
                 block_generic<ELEM>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, x + (int64_t)v * ld_x + cb * kCols,
-                                    a1, bad);
+                                    a1, bad, staged, smem_u32(lut));
                 const float sum = transpose_reduce(a1, lane);
                 if ((lane & 3) == 0 && row < m.n) emit(v, row, cb, sum);
             }
@@ -1580,21 +1643,31 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
 template <int ELEM, int MODE>
 __device__ __forceinline__ void unpack_generic(const uint8_t *reg, uint32_t bytes, int lane, const uint8_t *rexp,
                                                int nr, int rows, uint64_t k, uint64_t cb, void *out, int64_t ld_out,
-                                               uint64_t row0, uint64_t col0, int want, bool &bad) {
+                                               uint64_t row0, uint64_t col0, int want, bool &bad, bool staged = false,
+                                               uint32_t lutb = 0) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     const int cols = real_cols(k, cb, lane);
     LaneRegion lr = lane_region(reg, bytes, lane, rows, k, cb, F);
-    LaneStream ls;
-    ls.init(lr.code, lr.nwords);
-    const uint32_t n_esc =
-        lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, [&](int c, int r, uint32_t sg, uint32_t v, uint32_t mm, bool esc) {
-            if (MODE == 1 && r != want) return;
-            const uint64_t row = MODE == 0 ? row0 + (uint64_t)r : row0;
-            const uint32_t e = elem_bits<ELEM>(sg, esc ? 0u : v, mm);
-            if (ELEM == 0) static_cast<uint16_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint16_t)e;
-            else static_cast<uint8_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint8_t)e;
-        });
-    bad |= ls.overrun();
+    auto put = [&](int c, int r, uint32_t sg, uint32_t v, uint32_t mm, bool esc) {
+        if (MODE == 1 && r != want) return;
+        const uint64_t row = MODE == 0 ? row0 + (uint64_t)r : row0;
+        const uint32_t e = elem_bits<ELEM>(sg, esc ? 0u : v, mm);
+        if (ELEM == 0) static_cast<uint16_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint16_t)e;
+        else static_cast<uint8_t *>(out)[row * (uint64_t)ld_out + col0 + (uint64_t)c] = (uint8_t)e;
+    };
+    uint32_t n_esc;
+    if (staged) {  // codes through the shared table
+        LutStream<ELEM> ls;
+        ls.init((uint32_t)__cvta_generic_to_shared(lr.code), lr.nwords, lutb,
+                (uint32_t)__cvta_generic_to_shared(reg) + kStageBytes - 4);
+        n_esc = lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, put);
+        bad |= ls.overrun();
+    } else {
+        LaneStream ls;
+        ls.init(lr.code, lr.nwords);
+        n_esc = lane_rolled<ELEM>(ls, lr.man, lr.man_stride, rows, cols, nr, rexp, put);
+        bad |= ls.overrun();
+    }
     const uint32_t start = esc_slice(lr, n_esc, lane, bad);
     if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, rows, cols, MODE == 0 ? -1 : want, out, ld_out,
                          MODE == 0 ? (int64_t)row0 : (int64_t)row0 - want, col0))
@@ -1731,7 +1804,7 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
             }
             if (!done)
                 unpack_generic<ELEM, MODE>(reg, bytes, lane, rexp, m.nr, rows, m.k, cb, out, ld_out, orow, col0, want,
-                                           bad);
+                                           bad, staged, smem_u32(lut));
         }
         __syncwarp();
         if (nxt < n_items && nok) issue(nb_);
