@@ -416,6 +416,48 @@ __device__ __forceinline__ uint32_t xpair(const uint32_t *mw, int q) {
     return ((mw[k] >> o) & M) | ((mw[k + 1] << (16 - o)) & ~M);
 }
 
+// Row-ragged block (only the first `rows` < 8 rows real): the region stores mantissa fields of
+// real elements only, he = (rows + 1) / 2 per column in the even half-stream and ho = rows / 2 in
+// the odd one, where a full block has 4 and 4. Column c's fields start at field c he (c ho), and
+// the 4 F bits from there hold its real fields followed by the next column's: taken whole into
+// the column's place in the full-block layout, the real fields land where the full-block decoder
+// reads them and the rest fall on rows past N, whose values are never stored. Reads stay inside
+// the lane's nw mantissa words (word k at man + k mstride bytes); missing bits read as 0.
+template <int F>
+__device__ __forceinline__ uint32_t col_fields(uint32_t man, uint32_t mstride, uint32_t nw, int odd, uint32_t first) {
+    const uint32_t bit = (uint32_t)F * first, k = bit >> 4, o = bit & 15u;
+    uint64_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 3; i++) {  // o + 4 F <= 43 bits
+        uint32_t w = 0;
+        if (k + i < nw) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(man + (k + i) * mstride));
+        v |= (uint64_t)(odd ? w >> 16 : w & 0xFFFFu) << (16 * i);
+    }
+    return (uint32_t)(v >> o) & ((1u << (4 * F)) - 1u);
+}
+
+// Group g (columns 4g .. 4g + 3) of a row-ragged block in the full-block word layout: word i =
+// even half-word F g + i | odd half-word F g + i << 16.
+template <int F>
+__device__ __forceinline__ void group_fields_ragged(uint32_t man, uint32_t mstride, uint32_t nw, int g, int rows,
+                                                    uint32_t (&mw)[F]) {
+    const uint32_t he = (uint32_t)(rows + 1) >> 1, ho = (uint32_t)rows >> 1;
+#pragma unroll
+    for (int i = 0; i < F; i++) mw[i] = 0;
+#pragma unroll
+    for (int cl = 0; cl < 4; cl++) {
+        const uint32_t c = 4u * (uint32_t)g + (uint32_t)cl;
+        const int P = 4 * F * cl, k = P >> 4, o = P & 15;  // the column's place in the group (static)
+#pragma unroll
+        for (int odd = 0; odd < 2; odd++) {
+            const uint64_t v = (uint64_t)col_fields<F>(man, mstride, nw, odd, c * (odd ? ho : he)) << o;
+#pragma unroll
+            for (int h = 0; h < 3; h++)
+                if (k + h < F) mw[k + h] |= ((uint32_t)(v >> (16 * h)) & 0xFFFFu) << (16 * odd);
+        }
+    }
+}
+
 // Transposed reduction of acc[8] over the 32 lanes: afterwards lanes with (lane & 3) == 0
 // hold the sum of row rowsel(lane) = bit4<<2 | bit3<<1 | bit2 of the lane id.
 __device__ __forceinline__ float transpose_reduce(float (&acc)[8], int lane) {
@@ -673,14 +715,16 @@ __device__ __forceinline__ uint2 x4_load(const uint16_t *xv, int c0, int kc) {
 
 // Block from its staged region (`bytes` long), all 8 rows real: 4 groups of 4 columns (16 row
 // pairs each); the group loop stays rolled so the hot loop fits the instruction cache.
-// EDGE: the block's last real column is kc - 1 < 511 (K ragged). Every lane still holds 128
-// codes (fillers for columns past K), and the real columns' mantissa fields sit where they sit in
-// a full block, but the lanes' mantissa regions follow one another unless all have the same word
-// count; activations past K read as 0, so the fillers add nothing.
+// EDGE: the block's real extent is kc <= 512 columns and rows <= 8 rows, not both full. Every
+// lane still holds 128 codes (fillers for elements past K or N). Past K: the real columns'
+// mantissa fields sit where they sit in a full block, but the lanes' mantissa regions follow one
+// another unless all have the same word count; activations past K read as 0, so the fillers add
+// nothing. Past N: each group's fields are gathered into the full-block layout first; the rows
+// past N accumulate filler values that are never stored.
 template <int ELEM, int NB, bool EDGE = false>
 __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                            const uint16_t *xb, int64_t ld_x, uint2 (&xq)[NB], float (&acc)[NB][8],
-                                           bool &bad, int kc = kCols) {
+                                           bool &bad, int kc = kCols, int rows = kRows) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;  // words of a full lane's mantissa region
     constexpr int MWG = MW / 4;              // words per group of 4 columns
@@ -700,7 +744,7 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
     uint32_t mwords = MW;  // this lane's mantissa words (EDGE: only these are read)
     if (EDGE) {
         const int cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
-        const uint32_t mw = man_words(kRows, cols, F);
+        const uint32_t mw = man_words(rows, cols, F);
         mwords = mw;
         uint32_t mincl = mw;
 #pragma unroll
@@ -746,12 +790,16 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
             xf[v][3] = __uint_as_float(xq[v].y & 0xFFFF0000u);
         }
         uint32_t mw[MWG];
+        if (EDGE && rows < kRows) {
+            group_fields_ragged<F>(man, mstride, mwords, g, rows, mw);
+        } else {
 #pragma unroll
-        for (int i = 0; i < MWG; i++) {
-            const uint32_t kw = (uint32_t)(MWG * g + i);
-            mw[i] = 0;
-            if (!EDGE || kw < mwords)
-                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            for (int i = 0; i < MWG; i++) {
+                const uint32_t kw = (uint32_t)(MWG * g + i);
+                mw[i] = 0;
+                if (!EDGE || kw < mwords)
+                    asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            }
         }
         uint32_t e4[4];  // table entries of row pairs q, q + 1 (q even)
 #pragma unroll
@@ -784,7 +832,7 @@ __device__ __forceinline__ void block_fast(const uint8_t *reg, uint32_t bytes, i
 #pragma unroll
     for (int v = 0; v < NB; v++)
         esc_correct<ELEM>(reinterpret_cast<const uint32_t *>(reg + esc0), esc0 <= bytes ? (bytes - esc0) / 4 : 0, lane,
-                          xb + v * ld_x, kRows, kc, acc[v], bad);
+                          xb + v * ld_x, rows, kc, acc[v], bad);
 }
 
 // Any block (edge, or a region too large to stage) from shared or global memory; escaped
@@ -819,8 +867,10 @@ __device__ __forceinline__ void block_generic(const uint8_t *reg, uint32_t bytes
 }
 
 // y[v] = W x[v] for NB vectors (1 or 2; vector v at x + v ld_x, its result at y + v ld_y, its
-// partial sums at partial + v col_blocks n_pad).
-template <int ELEM, int NB>
+// partial sums at partial + v col_blocks n_pad). RAG: N % 8 != 0, and the blocks of the last row
+// block take the fast decoder too, in a kernel of their own so that the others keep their
+// registers.
+template <int ELEM, int NB, bool RAG = false>
 __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
     gemv_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, float *__restrict__ y, int64_t ld_y,
                 float *partial, uint32_t *counters, uint64_t n_pad) {
@@ -905,9 +955,10 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
         const int rows = real_rows(m.n, rb);
         const uint64_t kc64 = m.k - cb * kCols;
         const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
-        // full rows: the fast decoder (for a ragged K only when filler codes, which decode to
-        // rank 0 with a garbage mantissa, cannot be Inf or NaN, so that times 0 they add 0)
-        const bool fast = rows == kRows && staged && (kc == kCols || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu));
+        // the fast decoder; for a block past K or N only when filler codes, which decode to rank
+        // 0 with a garbage mantissa, cannot be Inf or NaN (times a zero activation they add 0)
+        const bool full = rows == kRows && kc == kCols;
+        const bool fast = staged && (RAG || rows == kRows) && (full || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu));
         // the fast path's first activations, loaded while the region copy completes
         uint2 xq0[NB];
 #pragma unroll
@@ -929,10 +980,11 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, GemvCfg<NB>::kCtas)
         for (int v = 0; v < NB; v++)
 #pragma unroll
             for (int r = 0; r < 8; r++) acc[v][r] = 0.0f;
-        if (fast && kc == kCols) {
+        if (fast && full) {
             block_fast<ELEM, NB>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad);
         } else if (fast) {
-            block_fast<ELEM, NB, true>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad, kc);
+            block_fast<ELEM, NB, true>(cur ? stage1 : stage0, bytes, lane, lut, x + cb * kCols, ld_x, xq0, acc, bad, kc,
+                                       RAG ? rows : kRows);
         } else {
 #pragma unroll
             for (int v = 0; v < NB; v++)
@@ -1058,14 +1110,16 @@ __device__ __forceinline__ uint32_t esc_bf16(uint32_t bits) {
 // d2, d3). The activations come from the CTA's staged slice at xs (shared address) when the
 // block's column block is staged, else from global memory at x0/x1 (this thread's two vectors
 // from the block's first column); v0/v1: those vectors exist (< nb).
-// EDGE: the block's real columns end at kc < 512 (ragged K; all 8 rows real): lane-contiguous
-// mantissa regions unless all lanes have the same word count, and activations past K are 0 (the
-// staged slice is zero-filled there, global loads are masked), so filler codes add nothing.
+// EDGE: the block's real extent is kc <= 512 columns and rows <= 8 rows, not both full. Past K:
+// lane-contiguous mantissa regions unless all lanes have the same word count, and activations
+// past K are 0 (the staged slice is zero-filled there, global loads are masked), so filler codes
+// add nothing. Past N: each group's fields are gathered into the full-block layout first; the
+// tile rows past N hold filler values whose products are never stored.
 template <int ELEM, bool EDGE = false>
 __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                           uint32_t tile, bool staged_x, uint32_t xs, const uint16_t *x0,
                                           const uint16_t *x1, bool v0, bool v1, float (&d)[4], bool &bad,
-                                          int kc = kCols) {
+                                          int kc = kCols, int rows = kRows) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -1084,7 +1138,7 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     uint32_t esc0 = man0 + kLanes * MW * 4;
     if (EDGE) {
         const int cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
-        const uint32_t mw = man_words(kRows, cols, F);
+        const uint32_t mw = man_words(rows, cols, F);
         mwords = mw;
         uint32_t mincl = mw;
 #pragma unroll
@@ -1120,12 +1174,16 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
 #pragma unroll 1
     for (int g = 0; g < 4; g++) {
         uint32_t mw[MWG];
+        if (EDGE && rows < kRows) {
+            group_fields_ragged<F>(man, mstride, mwords, g, rows, mw);
+        } else {
 #pragma unroll
-        for (int i = 0; i < MWG; i++) {
-            const uint32_t kw = (uint32_t)(MWG * g + i);
-            mw[i] = 0;
-            if (!EDGE || kw < mwords)
-                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            for (int i = 0; i < MWG; i++) {
+                const uint32_t kw = (uint32_t)(MWG * g + i);
+                mw[i] = 0;
+                if (!EDGE || kw < mwords)
+                    asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            }
         }
         uint32_t w2[16];
 #pragma unroll
@@ -1152,6 +1210,10 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
             if (e == kEscPad) continue;
             const uint32_t te = esc_t(e), c = te >> 3;
             if ((c >> 2) != (uint32_t)g) continue;
+            if (EDGE && ((int)(te & 7u) >= rows || (int)(esc_lane(e) * kLaneCols + c) >= kc)) {
+                bad = true;
+                continue;
+            }
             const uint32_t a = tile + tile_off(te & 7u, esc_lane(e)) + 2u * (c & 3u);
             asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)esc_bf16<ELEM>(esc_bits(e))) : "memory");
         }
@@ -1316,9 +1378,10 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
         const int rows = real_rows(m.n, rb);
         const uint64_t kc64 = m.k - cb * kCols;
         const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
-        // full rows: the tensor-core path (for a ragged K only when filler codes cannot decode
-        // to Inf or NaN, so that times 0 they add 0)
-        if (rows == kRows && staged && (kc == kCols || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu))) {
+        // the tensor-core path; for a block past K or N only when filler codes cannot decode to
+        // Inf or NaN (times a zero activation they add 0)
+        const bool full = rows == kRows && kc == kCols;
+        if (staged && (full || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu))) {
             const uint16_t *xc = x + cb * kCols;
             const bool v0 = gid < nb, v1 = gid + 8 < nb;
             const uint16_t *x0 = xc + (int64_t)(v0 ? gid : 0) * ld_x;
@@ -1326,19 +1389,21 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             const bool staged_x = cb == cb_first || cb == cb_first + 1;
             const uint32_t xs = xs0 + (cb == cb_first ? 0u : (uint32_t)kXSlice);
             float d[4];
-            if (kc == kCols) block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
-            else block_mma<ELEM, true>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad, kc);
-            const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;  // interior: both rows < n
+            if (full) block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
+            else block_mma<ELEM, true>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad, kc, rows);
+            const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;
+            const bool in0 = r0 < m.n, in1 = r0 + 1 < m.n;
             if (v0) {
-                emit(gid, r0, cb, d[0]);
-                emit(gid, r0 + 1, cb, d[1]);
+                if (in0) emit(gid, r0, cb, d[0]);
+                if (in1) emit(gid, r0 + 1, cb, d[1]);
             }
             if (v1) {
-                emit(gid + 8, r0, cb, d[2]);
-                emit(gid + 8, r0 + 1, cb, d[3]);
+                if (in0) emit(gid + 8, r0, cb, d[2]);
+                if (in1) emit(gid + 8, r0 + 1, cb, d[3]);
             }
         } else {
-            // edge blocks and regions too large to stage: the single-vector decoder per vector
+            // regions too large to stage, and edge blocks whose fillers could decode to Inf or NaN:
+            // the single-vector decoder per vector
             const int row_in = ((lane >> 4) & 1) << 2 | ((lane >> 3) & 1) << 1 | ((lane >> 2) & 1);
             const uint64_t row = rb * kRows + (uint64_t)row_in;
             for (int v = 0; v < nb; v++) {
@@ -1498,12 +1563,13 @@ __device__ __forceinline__ void store_row_part(void *out, uint64_t at, const uin
 
 // Block from its staged region, all 8 rows real. Decode writes rows row0 .. row0 + 7; gather
 // writes row `want` of the block to output row row0. col0 = the lane's first column. EDGE: the
-// block's real columns end at kc < 512 (ragged K): lane-contiguous mantissa regions unless all
-// lanes have the same word count, and only the real columns are written.
+// block's real extent is kc <= 512 columns and rows <= 8 rows, not both full: lane-contiguous
+// mantissa regions unless all lanes have the same word count, the fields of a row-ragged block
+// gathered into the full-block layout per group, and only real elements written.
 template <int ELEM, int MODE, bool EDGE = false>
 __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, int lane, const uint32_t *lut,
                                             void *out, int64_t ld_out, uint64_t row0, uint64_t col0, int want,
-                                            int vec, bool &bad, int kc = kCols) {
+                                            int vec, bool &bad, int kc = kCols, int rows = kRows) {
     constexpr int F = ELEM == 0 ? 7 : 3;
     constexpr int MW = ELEM == 0 ? 28 : 12;
     constexpr int MWG = MW / 4;
@@ -1524,7 +1590,7 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     int cols = kLaneCols;
     if (EDGE) {
         cols = kc - lane * kLaneCols < 0 ? 0 : (kc - lane * kLaneCols > kLaneCols ? kLaneCols : kc - lane * kLaneCols);
-        const uint32_t mw = man_words(kRows, cols, F);
+        const uint32_t mw = man_words(rows, cols, F);
         mwords = mw;
         uint32_t mincl = mw;
 #pragma unroll
@@ -1558,12 +1624,16 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     uint32_t o[MODE == 0 ? 8 : 1][8];
     auto group = [&](int g) {
         uint32_t mw[MWG];
+        if (EDGE && rows < kRows) {
+            group_fields_ragged<F>(man, mstride, mwords, g, rows, mw);
+        } else {
 #pragma unroll
-        for (int i = 0; i < MWG; i++) {
-            const uint32_t kw = (uint32_t)(MWG * g + i);
-            mw[i] = 0;
-            if (!EDGE || kw < mwords)
-                asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            for (int i = 0; i < MWG; i++) {
+                const uint32_t kw = (uint32_t)(MWG * g + i);
+                mw[i] = 0;
+                if (!EDGE || kw < mwords)
+                    asm("ld.shared.u32 %0, [%1];" : "=r"(mw[i]) : "r"(man + (EDGE ? mstride : 4 * kLanes) * kw));
+            }
         }
         uint32_t p[16];  // p[c4 * 4 + pp]: rows (2pp, 2pp + 1) at column 4g + c4
 #pragma unroll
@@ -1611,14 +1681,16 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     if (!EDGE || cols == kLaneCols) {
         if (MODE == 0) {
 #pragma unroll
-            for (int r = 0; r < 8; r++) store_row16<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], vec);
+            for (int r = 0; r < 8; r++)
+                if (!EDGE || r < rows) store_row16<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], vec);
         } else {
             store_row16<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], vec);
         }
     } else if (cols > 0) {
         if (MODE == 0) {
 #pragma unroll
-            for (int r = 0; r < 8; r++) store_row_part<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], cols);
+            for (int r = 0; r < 8; r++)
+                if (r < rows) store_row_part<ELEM>(out, (row0 + (uint64_t)r) * (uint64_t)ld_out + col0, o[r], cols);
         } else {
             store_row_part<ELEM>(out, row0 * (uint64_t)ld_out + col0, o[0], cols);
         }
@@ -1634,7 +1706,7 @@ __device__ __forceinline__ void unpack_fast(const uint8_t *reg, uint32_t bytes, 
     const uint32_t n_esc = flags >> 24;
     const uint32_t start = esc_slice(lr, n_esc, lane, bad);
     const uint64_t lane_col = col0;
-    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, kRows, cols, MODE == 0 ? -1 : want, out, ld_out,
+    if (!esc_patch<ELEM>(lr.esc, lr.slots, start, n_esc, lane, rows, cols, MODE == 0 ? -1 : want, out, ld_out,
                          MODE == 0 ? (int64_t)row0 : (int64_t)row0 - want, lane_col))
         bad = true;
 }
@@ -1793,12 +1865,13 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
                 unpack_fast<ELEM, MODE>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad);
                 done = true;
             }
-            // blocks of a ragged K with full rows: the fast decoder, in a kernel of their own
-            // (EDGEK) so that the regular decode keeps its registers; gather (64 registers) and
-            // fp8 decode take the generic path for them
+            // blocks past K or N: the fast decoder, in a kernel of their own (EDGEK) so that the
+            // regular decode keeps its registers; gather (64 registers) and fp8 decode take the
+            // generic path for them
             if constexpr (EDGEK && MODE == 0 && ELEM == 0) {
-                if (!done && rows == kRows && staged) {
-                    unpack_fast<ELEM, MODE, true>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad, kc);
+                if (!done && staged) {
+                    unpack_fast<ELEM, MODE, true>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad, kc,
+                                                  rows);
                     done = true;
                 }
             }
@@ -1882,9 +1955,9 @@ extern "C" nwc_status nwc_decode(const nwc_matrix *mp, void *out, int64_t ld_out
     const Mat m = to_mat(*mp);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vec = vec_ok(out, ld_out, m.elem);
-    const bool k_rag = (m.k % kCols) != 0;
+    const bool ragged = (m.k % kCols) != 0 || (m.n % kRows) != 0;
     const nwc_status st = m.elem != NWC_ELEM_BF16 ? launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s)
-                          : k_rag                 ? launch_unpack<0, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
+                          : ragged                ? launch_unpack<0, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
                                                   : launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
     if (st != NWC_OK) return st;
     if (m.elem == NWC_ELEM_FP8_E4M3 && scales_out) {
@@ -1937,7 +2010,9 @@ cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float 
     using C = GemvCfg<NB>;
     static bool smem_ok = false;
     static std::once_flag once;
-    std::call_once(once, [] { smem_ok = set_smem(gemv_kernel<ELEM, NB>, C::kSmem); });
+    std::call_once(once, [] {
+        smem_ok = set_smem(gemv_kernel<ELEM, NB>, C::kSmem) && set_smem(gemv_kernel<ELEM, NB, true>, C::kSmem);
+    });
     if (!smem_ok) return cudaErrorInvalidConfiguration;
     const uint64_t slots = (uint64_t)sms * C::kCtas;
     const int grid = (int)(m.nb < slots ? m.nb : slots);
@@ -1953,6 +2028,8 @@ cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (m.n % kRows != 0)
+        return cudaLaunchKernelEx(&cfg, gemv_kernel<ELEM, NB, true>, m, x, ld_x, y, ld_y, partial, counters, n_pad);
     return cudaLaunchKernelEx(&cfg, gemv_kernel<ELEM, NB>, m, x, ld_x, y, ld_y, partial, counters, n_pad);
 }
 

@@ -524,3 +524,58 @@ def test_ragged_k_11008_gemv_batch_and_decode():
     gemv_check(blob, synth.activations_bf16(k, 12), rows=rows, mat=mat)
     for nb in (2, 16):
         batch_check(blob, [synth.activations_bf16(k, 20 + v) for v in range(nb)], rows=rows, mat=mat)
+
+
+def test_row_ragged_last_row_block_every_height():
+    """N = 8 q + r for r = 1..7 (the last row block has r real rows), K full and ragged:
+    decode bit-exact; GEMV for one and two vectors and the batch GEMV for 3 and 16 vectors
+    within tolerance; BF16 with escapes in the ragged rows, and fp8."""
+    for r in range(1, 8):
+        for k in (1024, 1000):
+            n = 24 + r
+            w = _escape_heavy((n, k), 60 + 8 * r + k % 7)
+            blob = nwc.encode(w)
+            mat = nwc.Matrix(blob)
+            assert np.array_equal(mat.decode().cpu().numpy().view(np.uint16), w), (r, k)
+            assert_clean()
+            gemv_check(blob, synth.activations_bf16(k, 300 + r), mat=mat)
+            for nb in (2, 3, 16):
+                batch_check(blob, [synth.activations_bf16(k, 310 + r + v) for v in range(nb)], mat=mat)
+            q, sc = oracle.quantize_fp8(w)
+            b8 = nwc.encode_fp8(q, sc)
+            m8 = nwc.Matrix(b8)
+            qd, sd = m8.decode()
+            assert_clean()
+            assert np.array_equal(qd.cpu().numpy(), q) and np.array_equal(sd.cpu().numpy(), sc), (r, k)
+            gemv_check(b8, synth.activations_bf16(k, 320 + r), mat=m8)
+            for nb in (2, 5):
+                batch_check(b8, [synth.activations_bf16(k, 330 + r + v) for v in range(nb)], mat=m8)
+
+
+def test_infinite_rank0_exponent_keeps_fillers_out_of_real_rows():
+    """The most frequent exponent is 0xFF (most elements +-Inf), so filler codes would decode to
+    Inf and Inf * 0 would put NaN into real rows: blocks past K or N must skip their fillers.
+    Row 0 is finite and must match the oracle; the other rows are non-finite on both sides."""
+    rng = np.random.default_rng(91)
+    n, k = 13, 1100
+    w = np.where(rng.random((n, k)) < 0.5, 0x7F80, 0xFF80).astype(np.uint16)
+    w[0] = synth.normal_bf16((1, k), 0.02, seed=92)[0]
+    blob = nwc.encode(w)
+    mat = nwc.Matrix(blob)
+    assert np.array_equal(mat.decode().cpu().numpy().view(np.uint16), w)
+    x = synth.activations_bf16(k, 93)
+    y = mat.gemv(dev_bits(x)).cpu().numpy().astype(np.float64)
+    assert_clean()
+    ref = oracle.gemv(blob, x, np.array([0]))
+    assert abs(y[0] - ref[0]) <= TOL_REL * oracle.abs_dot(blob, x, np.array([0]))[0] + TOL_ABS
+    assert not np.isfinite(y[1:]).any()
+    xs = [synth.activations_bf16(k, 94 + v) for v in range(3)]
+    xb = np.zeros((3, (k + 7) // 8 * 8), np.uint16)
+    for v in range(3):
+        xb[v, :k] = xs[v]
+    yb = mat.gemv_batch(dev_bits(xb)[:, :k]).cpu().numpy().astype(np.float64)
+    assert_clean()
+    for v in range(3):
+        rv = oracle.gemv(blob, xs[v], np.array([0]))
+        assert abs(yb[v, 0] - rv[0]) <= TOL_REL * oracle.abs_dot(blob, xs[v], np.array([0]))[0] + TOL_ABS
+        assert not np.isfinite(yb[v, 1:]).any()
