@@ -310,7 +310,12 @@ constexpr int kLutBytes = kLutEntries * 4;
 constexpr int kRexpOff = kLutBytes;
 constexpr int kBarOff = kRexpOff + 16;
 constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
-constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes;
+// A lane's fast decoder reads at most about 208 bytes past its first code word whatever the code
+// bits (128 codes of at most 12 bits, a 64-bit window, one word of lookahead), and validation
+// caps a lane at 48 words, so the last lane of a staged region can read up to 6196 bytes past
+// the stage's start: the slack after the last stage keeps those reads inside the allocation.
+constexpr int kStageSlack = 256;
+constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes + kStageSlack;
 static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
 static_assert(kGemvSmem <= 232448, "shared memory per CTA");
 // CTAs per SM: 32 warps at 64 registers, and what 228 KB of shared memory holds (1 KB of it
@@ -325,7 +330,7 @@ struct GemvCfg {
     static constexpr int kWarps = NB == 1 ? kGemvWarps : 24;
     static constexpr int kStages = NB == 1 ? kStagesPerWarp : 1;
     static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
-    static constexpr int kSmem = kStageOff + kWarps * kStages * kStageBytes;
+    static constexpr int kSmem = kStageOff + kWarps * kStages * kStageBytes + kStageSlack;
     static constexpr int kCtas = NB == 1 ? kCtasPerSm : 1;
 };
 static_assert(GemvCfg<2>::kSmem <= 232448, "shared memory per CTA");
@@ -336,7 +341,7 @@ template <int MODE>
 struct UnpackCfg {
     static constexpr int kWarps = MODE == 0 ? 16 : kGemvWarps;
     static constexpr int kStageOff = (kBarOff + kWarps * 2 * 8 + 127) / 128 * 128;
-    static constexpr int kSmem = kStageOff + kWarps * kStageBytes;
+    static constexpr int kSmem = kStageOff + kWarps * kStageBytes + kStageSlack;
 };
 static_assert(UnpackCfg<0>::kSmem <= 232448 && UnpackCfg<1>::kSmem <= 232448, "shared memory per CTA");
 

@@ -247,3 +247,19 @@ def test_code_bit_flips_pass_validation_and_the_oracle_never_crashes(elem):
         except ValueError:
             outcomes.add("rejected")
     assert "rejected" in outcomes  # most flips break a lane's bit count or escape pattern
+
+
+def test_inflated_code_streams_pass_validation_and_the_oracle_rejects_them():
+    """A block region whose lane streams are rewritten to the 48-word maximum (all ones, so every
+    code is 12 bits long) with one short last lane: structurally valid, so host validation takes
+    it and only decoding can tell; the oracle rejects it."""
+    import blob_edit
+    from oracle import decode as oracle_decode
+    w = synth.normal_bf16((64, 513), 0.02, seed=5)
+    blob = nwc.encode(w)
+    bad = blob_edit.replace_code_streams(blob, 3, [48] * 31 + [8])
+    start, end = blob_edit.region_bounds(bad, 3)
+    assert end - start <= 6144  # still fits a decoder's shared-memory stage
+    assert nwc.validate(bad) == 0
+    with pytest.raises(ValueError):
+        oracle_decode(bad)

@@ -579,3 +579,43 @@ def test_infinite_rank0_exponent_keeps_fillers_out_of_real_rows():
         rv = oracle.gemv(blob, xs[v], np.array([0]))
         assert abs(yb[v, 0] - rv[0]) <= TOL_REL * oracle.abs_dot(blob, xs[v], np.array([0]))[0] + TOL_ABS
         assert not np.isfinite(yb[v, 1:]).any()
+
+
+def test_inflated_code_streams_in_the_last_stage_are_flagged_not_faulted():
+    """Blocks of a ragged K whose lane streams are rewritten to the 48-word maximum with a short
+    last lane (valid to the host, every code 12 bits long), placed where the last warp of each
+    CTA stages them (GEMV: warp 31, decode: warp 15): the last lane's decoder reads past its words
+    up to the end of the stage and beyond it into the slack that follows the last stage. Every
+    kernel finishes, the device error word reports the malformed blocks, and the context stays
+    usable."""
+    import blob_edit
+    sms = nwc.sm_count()
+    n, k = 8 * 2400, 513  # two column blocks; block 2 rb + 1 is the ragged one
+    w = synth.normal_bf16((n, k), 0.02, seed=150)
+    blob = nwc.encode(w)
+    targets = sorted({(31 * sms) | 1, (15 * sms) | 1})
+    bad = blob
+    for b in targets:
+        assert b < 2 * (n // 8) and b % 2 == 1
+        bad = blob_edit.replace_code_streams(bad, b, [48] * 31 + [8])
+        start, end = blob_edit.region_bounds(bad, b)
+        assert end - start <= 6144
+    assert nwc.validate(bad) == 0
+    mat = nwc.Matrix(bad)
+    x = synth.activations_bf16(k, 151)
+    mat.gemv(dev_bits(x))
+    st, flags = nwc.check()
+    assert st == 5 and flags & 1, (st, flags)
+    xb = np.zeros((3, 520), np.uint16)
+    for v in range(3):
+        xb[v, :k] = synth.activations_bf16(k, 152 + v)
+    mat.gemv_batch(dev_bits(xb)[:, :k])
+    st, flags = nwc.check()
+    assert st == 5 and flags & 1, (st, flags)
+    mat.decode()
+    st, flags = nwc.check()
+    assert st == 5 and flags & 1, (st, flags)
+    assert_clean()
+    # the rest of the matrix is untouched: rows outside the two rewritten row blocks still match
+    good_rows = np.array([r for r in range(0, n, 97) if r // 8 not in {b // 2 for b in targets}])
+    gemv_check(blob, x, rows=good_rows, mat=nwc.Matrix(blob))
