@@ -310,10 +310,11 @@ constexpr int kLutBytes = kLutEntries * 4;
 constexpr int kRexpOff = kLutBytes;
 constexpr int kBarOff = kRexpOff + 16;
 constexpr int kStageOff = (kBarOff + kGemvWarps * 2 * 8 + 127) / 128 * 128;
-// A lane's fast decoder reads at most about 208 bytes past its first code word whatever the code
-// bits (128 codes of at most 12 bits, a 64-bit window, one word of lookahead), and validation
-// caps a lane at 48 words, so the last lane of a staged region can read up to 6196 bytes past
-// the stage's start: the slack after the last stage keeps those reads inside the allocation.
+// A lane's fast decoder reads at most about 200 bytes past its first code word whatever the code
+// bits (128 codes of at most 12 bits through a 64-bit window with one word of lookahead), and
+// validation caps a lane at 48 words, so the last lane of a staged region can read up to
+// 32 + 31 * 48 * 4 + 200 = 6184 bytes past the stage's start (a stage holds 6144): the slack
+// after the last stage keeps those reads inside the allocation.
 constexpr int kStageSlack = 256;
 constexpr int kGemvSmem = kStageOff + kGemvWarps * kStagesPerWarp * kStageBytes + kStageSlack;
 static_assert(kStagesPerWarp == 1 || kStagesPerWarp == 2, "stages");
