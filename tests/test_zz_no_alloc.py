@@ -33,7 +33,8 @@ def _noalloc(mat, x_dev, y_dev):
 def test_noalloc_matches_gemv_on_two_calls_in_a_row():
     torch.cuda.init()
     cases = []
-    for shape, seed in (((520, 2600), 31), ((64, 512), 5)):  # multi- and single-column-block
+    # multi- and single-column-block, and a last row block of 5 rows (the row-ragged kernel)
+    for shape, seed in (((520, 2600), 31), ((64, 512), 5), ((517, 1500), 7)):
         w = synth.normal_bf16(shape, 0.03, seed)
         x = synth.activations_bf16(shape[1], seed + 1)
         cases.append((nwc.encode(w), x))
