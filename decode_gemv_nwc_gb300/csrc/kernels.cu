@@ -1525,34 +1525,29 @@ __device__ __forceinline__ uint2 row_words(uint32_t a, uint32_t b, uint32_t c, u
     return make_uint2(__byte_perm(__byte_perm(a, b, sel), __byte_perm(c, d, sel), 0x5410), 0u);
 }
 
-// One lane's 16-column row segment (BF16: 8 words, fp8: 4 words) to out[at ..]: with vec = 2
-// (out and the row stride keep 16-byte alignment) two (one) 16-byte stores, with vec = 1 (8-byte
-// alignment) four (two) 8-byte stores, else element-wise.
+// One lane's 16-column row segment (BF16: 8 words, fp8: 4 words) to out[at ..] with stores of
+// vec bytes (16, 8 or 4: out and the row stride keep that alignment), else element-wise.
 template <int ELEM>
 __device__ __forceinline__ void store_row16(void *out, uint64_t at, const uint32_t (&w)[8], int vec) {
-    if (ELEM == 0) {
-        uint16_t *o = static_cast<uint16_t *>(out) + at;
-        if (vec == 2) {
-            reinterpret_cast<uint4 *>(o)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            reinterpret_cast<uint4 *>(o)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        } else if (vec == 1) {
+    constexpr int NW = ELEM == 0 ? 8 : 4;  // words in the segment
+    void *o = ELEM == 0 ? static_cast<void *>(static_cast<uint16_t *>(out) + at)
+                        : static_cast<void *>(static_cast<uint8_t *>(out) + at);
+    if (vec == 16) {
 #pragma unroll
-            for (int i = 0; i < 4; i++) reinterpret_cast<uint2 *>(o)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
-        } else {
+        for (int i = 0; i < NW / 4; i++)
+            reinterpret_cast<uint4 *>(o)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if (vec == 8) {
 #pragma unroll
-            for (int i = 0; i < 16; i++) o[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
-        }
+        for (int i = 0; i < NW / 2; i++) reinterpret_cast<uint2 *>(o)[i] = make_uint2(w[2 * i], w[2 * i + 1]);
+    } else if (vec == 4) {
+#pragma unroll
+        for (int i = 0; i < NW; i++) reinterpret_cast<uint32_t *>(o)[i] = w[i];
+    } else if (ELEM == 0) {
+#pragma unroll
+        for (int i = 0; i < 16; i++) static_cast<uint16_t *>(o)[i] = (uint16_t)(w[i >> 1] >> (16 * (i & 1)));
     } else {
-        uint8_t *o = static_cast<uint8_t *>(out) + at;
-        if (vec == 2) {
-            *reinterpret_cast<uint4 *>(o) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else if (vec == 1) {
-            reinterpret_cast<uint2 *>(o)[0] = make_uint2(w[0], w[1]);
-            reinterpret_cast<uint2 *>(o)[1] = make_uint2(w[2], w[3]);
-        } else {
 #pragma unroll
-            for (int i = 0; i < 16; i++) o[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
-        }
+        for (int i = 0; i < 16; i++) static_cast<uint8_t *>(o)[i] = (uint8_t)(w[i >> 2] >> (8 * (i & 3)));
     }
 }
 
@@ -1872,9 +1867,8 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
                 done = true;
             }
             // blocks past K or N: the fast decoder, in a kernel of their own (EDGEK) so that the
-            // regular decode keeps its registers; gather (64 registers) and fp8 decode take the
-            // generic path for them
-            if constexpr (EDGEK && MODE == 0 && ELEM == 0) {
+            // regular decode and gather keep their registers
+            if constexpr (EDGEK) {
                 if (!done && staged) {
                     unpack_fast<ELEM, MODE, true>(stage, bytes, lane, lut, out, ld_out, orow, col0, want, vec, bad, kc,
                                                   rows);
@@ -1946,11 +1940,13 @@ nwc_status launch_unpack(const Mat &m, const int32_t *ids, uint64_t n_items, voi
 
 // A lane's 16-column row segment is stored with 16-byte stores when every row start keeps that
 // alignment (2), with 8-byte stores when rows keep 8-byte alignment (1), else element by element.
+// Widest store (16, 8 or 4 bytes; 0: element-wise) that every 16-column row segment of out allows:
+// segments start at out + (r ld_out + 16 j) elements.
 int vec_ok(const void *out, int64_t ld_out, int elem) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(out);
-    const int64_t per16 = elem == NWC_ELEM_BF16 ? 8 : 16;  // elements in 16 bytes
-    if ((a % 16) == 0 && (ld_out % per16) == 0) return 2;
-    if ((a % 8) == 0 && (ld_out % (per16 / 2)) == 0) return 1;
+    const int64_t esz = elem == NWC_ELEM_BF16 ? 2 : 1;
+    for (int v = 16; v >= 4; v /= 2)
+        if ((a % v) == 0 && ((ld_out * esz) % v) == 0) return v;
     return 0;
 }
 
@@ -1962,9 +1958,13 @@ extern "C" nwc_status nwc_decode(const nwc_matrix *mp, void *out, int64_t ld_out
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vec = vec_ok(out, ld_out, m.elem);
     const bool ragged = (m.k % kCols) != 0 || (m.n % kRows) != 0;
-    const nwc_status st = m.elem != NWC_ELEM_BF16 ? launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s)
-                          : ragged                ? launch_unpack<0, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
-                                                  : launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
+    nwc_status st;
+    if (m.elem == NWC_ELEM_BF16)
+        st = ragged ? launch_unpack<0, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
+                    : launch_unpack<0, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
+    else
+        st = ragged ? launch_unpack<1, 0, true>(m, nullptr, m.nb, out, ld_out, vec, s)
+                    : launch_unpack<1, 0>(m, nullptr, m.nb, out, ld_out, vec, s);
     if (st != NWC_OK) return st;
     if (m.elem == NWC_ELEM_FP8_E4M3 && scales_out) {
         if (cudaMemcpyAsync(scales_out, m.scales, 4 * m.n, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
@@ -1982,8 +1982,12 @@ extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vec = vec_ok(out, ld_out, m.elem);
     const uint64_t items = (uint64_t)n_ids * m.cbs;
-    return m.elem == NWC_ELEM_BF16 ? launch_unpack<0, 1>(m, ids, items, out, ld_out, vec, s)
-                                   : launch_unpack<1, 1>(m, ids, items, out, ld_out, vec, s);
+    const bool ragged = (m.k % kCols) != 0 || (m.n % kRows) != 0;
+    if (m.elem == NWC_ELEM_BF16)
+        return ragged ? launch_unpack<0, 1, true>(m, ids, items, out, ld_out, vec, s)
+                      : launch_unpack<0, 1>(m, ids, items, out, ld_out, vec, s);
+    return ragged ? launch_unpack<1, 1, true>(m, ids, items, out, ld_out, vec, s)
+                  : launch_unpack<1, 1>(m, ids, items, out, ld_out, vec, s);
 }
 
 namespace {

@@ -136,10 +136,9 @@ nwc_status nwc_bind(const void *blob_host, size_t bytes, const void *blob_dev, n
  * nwc_decode -- dequantization to the stored elements, bit-exact (the NWC page, "How it
  * works": decoding is lossless): BF16 blobs write uint16 out[n*ld_out + k]; fp8 blobs write the e4m3 bytes
  * (uint8) to out and the row scales to scales_out (fp32[N], may be NULL). ld_out >= K.
- * Rows are written 16 columns at a time: with 16-byte stores when out is 16-byte aligned and
- * ld_out is a multiple of 8 (BF16) or 16 (fp8), with 8-byte stores when out is 8-byte aligned
- * and ld_out a multiple of 4 (BF16) or 8 (fp8); any other out or ld_out is written element by
- * element (correct, slower).
+ * Rows are written 16 columns at a time with the widest store of 16, 8 or 4 bytes to which both
+ * out and the row stride in bytes (ld_out x element size) are aligned; any other out or ld_out
+ * is written element by element (correct, slower).
  */
 nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *scales_out,
                       nwc_stream stream);

@@ -511,6 +511,37 @@ def test_decode_and_gather_8_byte_aligned_rows():
     assert np.array_equal(o[:, :k], q) and (o[:, k:] == 0xAB).all()
 
 
+def test_decode_and_gather_4_byte_aligned_rows():
+    """Row strides that keep 4-byte but not 8-byte alignment (BF16 K + 2, fp8 K + 4) take the
+    4-byte store path; the padding columns keep their sentinel."""
+    n, k = 40, 2600
+    w = _escape_heavy((n, k), 43)
+    mat = nwc.Matrix(nwc.encode(w))
+    big = torch.full((n, k + 2), -7, dtype=torch.int16, device="cuda")
+    mat.decode(out=big[:, :k])
+    assert_clean()
+    got = big.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, :k], w) and (got[:, k:] == np.uint16(0xFFF9)).all()
+    ids = np.array([39, 0, 17, 17, 8, 33], np.int32)
+    gbig = torch.full((len(ids), k + 2), -7, dtype=torch.int16, device="cuda")
+    mat.gather(torch.from_numpy(ids).cuda(), out=gbig[:, :k])
+    assert_clean()
+    g = gbig.cpu().numpy().view(np.uint16)
+    assert np.array_equal(g[:, :k], w[ids]) and (g[:, k:] == np.uint16(0xFFF9)).all()
+    q, sc = oracle.quantize_fp8(w)
+    m8 = nwc.Matrix(nwc.encode_fp8(q, sc))
+    out8 = torch.full((n, k + 4), 0xAB, dtype=torch.uint8, device="cuda")
+    m8.decode(out=out8[:, :k])
+    assert_clean()
+    o = out8.cpu().numpy()
+    assert np.array_equal(o[:, :k], q) and (o[:, k:] == 0xAB).all()
+    g8 = torch.full((len(ids), k + 4), 0xAB, dtype=torch.uint8, device="cuda")
+    m8.gather(torch.from_numpy(ids).cuda(), out=g8[:, :k])
+    assert_clean()
+    o = g8.cpu().numpy()
+    assert np.array_equal(o[:, :k], q[ids]) and (o[:, k:] == 0xAB).all()
+
+
 def test_ragged_k_11008_gemv_batch_and_decode():
     """K = 11008 (21.5 column blocks): the ragged last column block of every row block takes the
     fast decoders (single vector, two vectors, 16 vectors on the tensor cores, decode)."""
