@@ -32,6 +32,9 @@
 // kernel on the stream drains and waits for it before touching x, the workspace or y.
 // The small-batch GEMV keeps the decoder and moves the products with three or more vectors to
 // the tensor cores (mma.sync on decoded tiles staged in shared memory).
+// Blocks that reach past K or N (filler codes, mantissas of real elements only) take the same
+// decoders, in kernel instantiations of their own; a generic one-code-at-a-time decoder serves
+// regions too large for a stage and blocks whose fillers could decode to Inf or NaN.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
