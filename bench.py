@@ -226,6 +226,29 @@ def extra_workloads(dev, stream, steps):
     out = {}
     peak, _ = peaks()
 
+    # The odd shape of the square workload: 4095x4100 (a ragged last row block and column block),
+    # 24 rotated copies as for the headline, then its decode; cuBLAS on the BF16 weights beside it.
+    w = synth.normal_bf16((4095, 4100), 0.02, 1, device=dev)
+    blob = encode_on_host(w)
+    host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+    omats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(COPIES)]
+    xo = torch.from_numpy(synth.activations_bf16(4100, 1001).view(np.int16)).to(dev)
+    yo = torch.empty(4095, dtype=torch.float32, device=dev)
+    odd_ms = time_graph(lambda: [m.gemv(xo, y=yo, stream=stream) for m in omats], stream, max(3, steps // 2))
+    dec_o = torch.empty((4095, 4100), dtype=torch.int16, device=dev)
+    odd_dec_ms = time_graph(lambda: omats[0].decode(out=dec_o, stream=stream), stream, steps)
+    wo = [w.view(torch.bfloat16).clone() for _ in range(COPIES)]
+    ybo = torch.empty(4095, dtype=torch.bfloat16, device=dev)
+    odd_bf16_ms = time_graph(lambda: [torch.mv(wc, xo.view(torch.bfloat16), out=ybo) for wc in wo], stream,
+                             max(3, steps // 2))
+    out["odd_4095x4100"] = {
+        "workload": "4095x4100 BF16 batch-1 GEMV (ragged last row and column blocks), 24 rotated copies; decode",
+        "us": odd_ms * 1e3 / COPIES, "compressed_bytes": len(blob),
+        "frac_of_measured_hbm": (len(blob) + 2 * 4100 + 4 * 4095) / (odd_ms * 1e-3 / COPIES) / 1e9 / peak,
+        "decode_us": odd_dec_ms * 1e3, "bf16_cublas_us": odd_bf16_ms * 1e3 / COPIES}
+    del omats, wo, host, w
+    torch.cuda.empty_cache()
+
     # 36-layer decoder stack, one token = one GEMV per matrix (252), as one CUDA graph
     t0 = time.time()
     mats, xs, ys, wbf = [], {}, [], []
