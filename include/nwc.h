@@ -21,9 +21,10 @@
  *   - GPU calls are asynchronous on the given stream (NULL = the legacy default stream).
  *     A launch failure returns NWC_ERR_CUDA. Data errors found on the device (a lane
  *     stream that runs past its words, an escape list that does not match the stream's
- *     escape codes, a gather id out of range) do not fault: the kernel
- *     skips the bad access, writes zeros and raises the device error word, which
- *     nwc_check() reads and clears.
+ *     escape codes, a gather id out of range) do not fault: every read stays inside the
+ *     block's staged region (or the lane's own words), the outputs of a malformed block are
+ *     unspecified (a bad gather id writes a zero row), and the kernel raises the device
+ *     error word, which nwc_check() reads and clears.
  *   - Matrices are row-major: element (n, k) of an N x K matrix is at index n*ld + k.
  *     N = output features (rows), K = input features (columns), ld >= K.
  *   - BF16 values are passed as their 16-bit patterns (uint16_t); x is BF16, y is FP32.
