@@ -1265,7 +1265,9 @@ __device__ __forceinline__ void block_mma(const uint8_t *reg, uint32_t bytes, in
     for (int i = 0; i < 4; i++) d[i] = acc[0][i] + acc[1][i];
 }
 
-template <int ELEM>
+// RAG: N % 8 != 0, and the blocks of the last row block take the tensor-core path too, in a kernel
+// of their own so that the others keep the regular kernel's code.
+template <int ELEM, bool RAG = false>
 __global__ void __launch_bounds__(kBatchWarps * 32, 1)
     gemv_batch_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, int nb, float *__restrict__ y,
                       int64_t ld_y, float *partial, uint32_t *counters, uint64_t n_pad) {
@@ -1390,7 +1392,7 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
         // the tensor-core path; for a block past K or N only when filler codes cannot decode to
         // Inf or NaN (times a zero activation they add 0)
         const bool full = rows == kRows && kc == kCols;
-        if (staged && (full || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu))) {
+        if (staged && (RAG || rows == kRows) && (full || m.rank_exp[0] != (ELEM == 0 ? 0xFFu : 0xFu))) {
             const uint16_t *xc = x + cb * kCols;
             const bool v0 = gid < nb, v1 = gid + 8 < nb;
             const uint16_t *x0 = xc + (int64_t)(v0 ? gid : 0) * ld_x;
@@ -1399,9 +1401,10 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             const uint32_t xs = xs0 + (cb == cb_first ? 0u : (uint32_t)kXSlice);
             float d[4];
             if (full) block_mma<ELEM>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad);
-            else block_mma<ELEM, true>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad, kc, rows);
+            else block_mma<ELEM, true>(stage, bytes, lane, lut, tile, staged_x, xs, x0, x1, v0, v1, d, bad, kc,
+                                       RAG ? rows : kRows);
             const uint64_t r0 = rb * kRows + 2 * (uint64_t)t;
-            const bool in0 = r0 < m.n, in1 = r0 + 1 < m.n;
+            const bool in0 = !RAG || r0 < m.n, in1 = !RAG || r0 + 1 < m.n;
             if (v0) {
                 if (in0) emit(gid, r0, cb, d[0]);
                 if (in1) emit(gid, r0 + 1, cb, d[1]);
@@ -2086,7 +2089,9 @@ cudaError_t launch_batch(const Mat &m, const uint16_t *x, int64_t ld_x, int nb, 
                          uint64_t n_pad, int grid, cudaStream_t s) {
     static bool smem_ok = false;
     static std::once_flag once;
-    std::call_once(once, [] { smem_ok = set_smem(gemv_batch_kernel<ELEM>, kBatchSmem); });
+    std::call_once(once, [] {
+        smem_ok = set_smem(gemv_batch_kernel<ELEM>, kBatchSmem) && set_smem(gemv_batch_kernel<ELEM, true>, kBatchSmem);
+    });
     if (!smem_ok) return cudaErrorInvalidConfiguration;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     uint32_t *counters = reinterpret_cast<uint32_t *>(w8);
@@ -2101,6 +2106,9 @@ cudaError_t launch_batch(const Mat &m, const uint16_t *x, int64_t ld_x, int nb, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (m.n % kRows != 0)
+        return cudaLaunchKernelEx(&cfg, gemv_batch_kernel<ELEM, true>, m, x, ld_x, nb, y, ld_y, partial, counters,
+                                  n_pad);
     return cudaLaunchKernelEx(&cfg, gemv_batch_kernel<ELEM>, m, x, ld_x, nb, y, ld_y, partial, counters, n_pad);
 }
 }  // namespace
