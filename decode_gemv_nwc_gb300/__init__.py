@@ -63,6 +63,7 @@ def lib():
     L.nwc_validate.argtypes = [p, sz]
     L.nwc_bind.argtypes = [p, sz, p, ctypes.POINTER(NwcMatrix)]
     L.nwc_decode.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, p]
+    L.nwc_dequantize_fp8.argtypes = [p, i64, p, i64, i64, p, i64, p]
     L.nwc_gemv_workspace_bytes.argtypes = [ctypes.POINTER(NwcMatrix)]
     L.nwc_gemv_workspace_bytes.restype = sz
     L.nwc_gemv_prepare.argtypes = [ctypes.POINTER(NwcMatrix), p, sz, p]
@@ -224,18 +225,39 @@ class Matrix:
                              ctypes.c_void_p(scales.data_ptr()), _stream_ptr(stream)), "nwc_decode")
         return out, scales
 
+    def dequantize(self, out=None, stream=None):
+        """fp8 matrices: BF16 weights [N, K] (int16 bits), each the BF16 nearest to e4m3(q) * s_n
+        (nwc_decode to e4m3 bytes and scales, then nwc_dequantize_fp8)."""
+        import torch
+        assert self.elem == FP8, "dequantize serves fp8 matrices"
+        dev = self.device_blob.device
+        if getattr(self, "_q8", None) is None:  # kept: the kernels may still read it after return
+            self._q8 = torch.empty((self.n, self.k), dtype=torch.uint8, device=dev)
+            self._s8 = torch.empty(self.n, dtype=torch.float32, device=dev)
+        q, scales = self._q8, self._s8
+        _ok(lib().nwc_decode(ctypes.byref(self.m), ctypes.c_void_p(q.data_ptr()), q.stride(0),
+                             ctypes.c_void_p(scales.data_ptr()), _stream_ptr(stream)), "nwc_decode")
+        out = out if out is not None else torch.empty((self.n, self.k), dtype=torch.int16, device=dev)
+        _ok(lib().nwc_dequantize_fp8(ctypes.c_void_p(q.data_ptr()), q.stride(0), ctypes.c_void_p(scales.data_ptr()),
+                                     self.n, self.k, ctypes.c_void_p(out.data_ptr()), out.stride(0),
+                                     _stream_ptr(stream)), "nwc_dequantize_fp8")
+        return out
+
     def matmul(self, x, scratch=None, stream=None):
         """Batch > 1 (prefill): Y[B, N] = X[B, K] W^T in BF16. The matrix is decoded into a BF16
-        scratch (allocated once and kept unless given) and multiplied by cuBLAS through torch,
-        as the NWC page describes for prefill ("dequantizes to BF16 and calls cuBLAS")."""
+        scratch (allocated once and kept unless given; fp8 matrices are dequantized into it) and
+        multiplied by cuBLAS through torch: the pages' prefill (weights back to BF16, then a BF16
+        GEMM)."""
         import torch
-        assert self.elem == BF16, "matmul serves BF16 matrices"
         if scratch is None:
             scratch = getattr(self, "_scratch", None)
             if scratch is None:
                 scratch = torch.empty((self.n, self.k), dtype=torch.int16, device=self.device_blob.device)
                 self._scratch = scratch
-        self.decode(out=scratch, stream=stream)
+        if self.elem == BF16:
+            self.decode(out=scratch, stream=stream)
+        else:
+            self.dequantize(out=scratch, stream=stream)
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s):
             return torch.nn.functional.linear(x.view(torch.bfloat16), scratch.view(torch.bfloat16))

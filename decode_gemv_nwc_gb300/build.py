@@ -17,7 +17,7 @@ LIB = os.path.join(OUT, "libnwc.so")
 INCLUDE = os.path.join(ROOT, "include")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU = ["kernels.cu"]
+CU = ["kernels.cu", "dequant.cu"]
 CPP = ["encoder.cpp", "bind.cpp"]
 
 

@@ -145,6 +145,18 @@ nwc_status nwc_decode(const nwc_matrix *m, void *out, int64_t ld_out, float *sca
                       nwc_stream stream);
 
 /*
+ * nwc_dequantize_fp8 -- BF16 weights for prefill from fp8 rows (the "Qwen3-4B-NWC-fp8" model
+ * card: prefill dequantizes the weights to BF16 and calls cuBLAS): out[n*ld_out + k] = the BF16
+ * nearest (ties to even) to the FP32 product e4m3(q[n*ld_q + k]) * scales[n]; a NaN code (or
+ * product) gives 0x7FC0. q and scales are what nwc_decode writes for an fp8 blob. Device
+ * pointers, N x K, ld_q >= K, ld_out >= K; 8-byte loads and 16-byte stores when q, out and the
+ * strides keep that alignment, else element by element. Asynchronous on the stream; N or K = 0
+ * is a no-op.
+ */
+nwc_status nwc_dequantize_fp8(const uint8_t *q, int64_t ld_q, const float *scales, int64_t n, int64_t k,
+                              uint16_t *out, int64_t ld_out, nwc_stream stream);
+
+/*
  * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 bytes): FP32
  * partial sums per (row, 512-column block) and one counter per 8-row block (both only when
  * K > 512). The 4096-entry decode table (the NWC page: a 16 KB shared-memory table indexed by

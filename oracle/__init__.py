@@ -42,6 +42,7 @@ def _L():
         lib.orc_info.argtypes = [p, u64, p, p]
         lib.orc_decode.argtypes = [p, u64, p, p]
         lib.orc_quantize_fp8.argtypes = [p, u64, u64, p, p]
+        lib.orc_dequantize_fp8.argtypes = [p, p, u64, u64, p]
         lib.orc_e4m3_from_f32.argtypes = [ctypes.c_float]
         lib.orc_e4m3_from_f32.restype = ctypes.c_uint8
         lib.orc_gemv_rows.argtypes = [p, u64, p, p, u64, p]
@@ -108,6 +109,16 @@ def quantize_fp8(w_bits: np.ndarray):
     if _L().orc_quantize_fp8(_ptr(w), n, k, _ptr(q), _ptr(s)) != 0:
         raise ValueError("non-finite weight")
     return q, s
+
+
+def dequantize_fp8(q: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """BF16 bits (uint16 (N, K)) of the FP32 products e4m3(q) * s_n, rounded to nearest even."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.float32)
+    n, k = q.shape
+    out = np.zeros((n, k), np.uint16)
+    _L().orc_dequantize_fp8(_ptr(q), _ptr(s), n, k, _ptr(out))
+    return out
 
 
 def e4m3_from_f32(x: float) -> int:

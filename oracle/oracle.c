@@ -77,6 +77,9 @@
  *
  *   Matrix-vector product (the plain definition): y_n = sum_k w[n,k] * x[k] with
  *   every product and the sum taken in FP64 (FP8: y_n = s_n * sum_k q[n,k] x[k]).
+ *
+ *   FP8 dequantization for prefill (READING of [P2]): BF16 nearest (ties to even) to the FP32
+ *   product e4m3(q[n,k]) * s_n; NaN codes give 0x7FC0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -532,6 +535,29 @@ int orc_quantize_fp8(const uint16_t *w, uint64_t N, uint64_t K, uint8_t *q, floa
         }
     }
     return 0;
+}
+
+/* BF16 nearest to a float, ties to even; every NaN gives the quiet NaN 0x7FC0. */
+static uint16_t bf16_nearest(float f) {
+    if (isnan(f)) return 0x7FC0;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    uint32_t low = u & 0xFFFFu, high = u >> 16;
+    if (low > 0x8000u || (low == 0x8000u && (high & 1u))) high += 1; /* carries into the exponent */
+    return (uint16_t)high;
+}
+
+/* Dequantization of fp8 rows to BF16 for prefill (READING of [P2], whose prefill turns the
+ * weights back into BF16 for a BF16 GEMM):
+ * out[n,k] = the BF16 nearest (ties to even) to the FP32 product of the e4m3 value (exact in
+ * FP32) and s_n; a NaN code gives 0x7FC0. */
+void orc_dequantize_fp8(const uint8_t *q, const float *scale, uint64_t N, uint64_t K, uint16_t *out) {
+    for (uint64_t n = 0; n < N; n++)
+        for (uint64_t k = 0; k < K; k++) {
+            float v = (float)e4m3_value(q[n * K + k]);
+            float p = v * scale[n];
+            out[n * K + k] = bf16_nearest(p);
+        }
 }
 
 /* y[i] = sum_k value(W[rows[i], k]) * x[k] in FP64 (times s_n for fp8), for the

@@ -292,3 +292,16 @@ def test_validate_and_oracle_survive_random_byte_mutations():
                 except ValueError:
                     pass
     assert accepted > 0  # edits inside code words and mantissas keep the structure valid
+
+
+def test_dequantize_fp8_argument_checks_before_any_launch():
+    L = nwc.lib()
+    P = ctypes.c_void_p
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, P(0x2000), 0, 16, P(0x3000), 16, None) == 0  # no rows: no-op
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, P(0x2000), 4, 0, P(0x3000), 16, None) == 0   # no columns
+    assert L.nwc_dequantize_fp8(P(0x1000), 8, P(0x2000), 4, 16, P(0x3000), 16, None) == 1   # ld_q < K
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, P(0x2000), 4, 16, P(0x3000), 8, None) == 1   # ld_out < K
+    assert L.nwc_dequantize_fp8(None, 16, P(0x2000), 4, 16, P(0x3000), 16, None) == 1
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, None, 4, 16, P(0x3000), 16, None) == 1
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, P(0x2000), 4, 16, None, 16, None) == 1
+    assert L.nwc_dequantize_fp8(P(0x1000), 16, P(0x2000), -1, 16, P(0x3000), 16, None) == 1

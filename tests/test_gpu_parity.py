@@ -650,3 +650,48 @@ def test_inflated_code_streams_in_the_last_stage_are_flagged_not_faulted():
     # the rest of the matrix is untouched: rows outside the two rewritten row blocks still match
     good_rows = np.array([r for r in range(0, n, 97) if r // 8 not in {b // 2 for b in targets}])
     gemv_check(blob, x, rows=good_rows, mat=nwc.Matrix(blob))
+
+
+def test_fp8_dequantize_bit_exact_and_prefill():
+    """fp8 prefill: nwc_dequantize_fp8 equals the oracle bit for bit (every byte value, NaN codes
+    included; aligned rows on the vector path, ragged and strided rows element by element), and
+    Matrix.matmul on an fp8 matrix meets the BF16 GEMM bound against FP64 products of the oracle's
+    BF16 weights."""
+    import ctypes
+    rng = np.random.default_rng(404)
+    # every byte value, random row scales; 8-aligned rows (vector path) and a ragged width
+    for n, k in ((64, 512), (33, 1001)):
+        q = rng.integers(0, 256, (n, k)).astype(np.uint8)
+        s = rng.uniform(1e-3, 2.0, n).astype(np.float32)
+        qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
+        out = torch.full((n, k), -7, dtype=torch.int16, device="cuda")
+        assert nwc.lib().nwc_dequantize_fp8(ctypes.c_void_p(qd.data_ptr()), k, ctypes.c_void_p(sd.data_ptr()), n, k,
+                                            ctypes.c_void_p(out.data_ptr()), k, None) == 0
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), oracle.dequantize_fp8(q, s)), (n, k)
+    # strided output rows with sentinels past K
+    q = rng.integers(0, 256, (20, 1000)).astype(np.uint8)
+    s = rng.uniform(0.01, 1.0, 20).astype(np.float32)
+    qpad = torch.zeros((20, 1008), dtype=torch.uint8, device="cuda")
+    qpad[:, :1000] = torch.from_numpy(q).cuda()
+    big = torch.full((20, 1016), -7, dtype=torch.int16, device="cuda")
+    assert nwc.lib().nwc_dequantize_fp8(ctypes.c_void_p(qpad.data_ptr()), 1008,
+                                        ctypes.c_void_p(torch.from_numpy(s).cuda().data_ptr()), 20, 1000,
+                                        ctypes.c_void_p(big.data_ptr()), 1016, None) == 0
+    torch.cuda.synchronize()
+    got = big.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got[:, :1000], oracle.dequantize_fp8(q, s)) and (got[:, 1000:] == 0xFFF9).all()
+    # through the matrix: decode + dequantize, then prefill on cuBLAS
+    w = synth.normal_bf16((300, 2600), 0.02, seed=405)
+    qm, sm = oracle.quantize_fp8(w)
+    mat = nwc.Matrix(nwc.encode_fp8(qm, sm))
+    wq = oracle.dequantize_fp8(qm, sm)
+    assert np.array_equal(mat.dequantize().cpu().numpy().view(np.uint16), wq)
+    X = np.stack([synth.activations_bf16(2600, 406 + b) for b in range(6)])
+    Y = mat.matmul(torch.from_numpy(X.view(np.int16)).cuda()).float().cpu().numpy().astype(np.float64)
+    assert_clean()
+    Wf = synth.bf16_bits_to_f32(wq).astype(np.float64)
+    Xf = synth.bf16_bits_to_f32(X).astype(np.float64)
+    ref = Xf @ Wf.T
+    bound = 2.0 ** -7 * (np.abs(Xf) @ np.abs(Wf).T) + 1e-6
+    assert (np.abs(Y - ref) <= bound).all()

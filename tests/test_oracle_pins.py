@@ -355,3 +355,29 @@ def test_zero_row_fp8_scale_is_one():
     q, s = oracle.quantize_fp8(w)
     assert s[0] == 1.0 and (q[0] == 0).all()
     assert q[1, 3] == 0x7E
+
+
+def test_fp8_dequantize_pins():
+    """Dequantization for prefill: BF16 nearest (ties to even) to the FP32 product e4m3(q) * s_n.
+    Power-of-two scales make every product exact (an e4m3 value has at most 4 significant bits),
+    so the BF16 equals torch's e4m3 value times the scale; hand-worked products pin the rounding."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)  # no NaN codes
+    for j in (-3, 0, 5):
+        s = np.float32(2.0 ** j)
+        got = oracle.dequantize_fp8(codes[None, :], np.array([s], np.float32))[0]
+        exact = (torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32) * float(s)).numpy()
+        bits = exact.view(np.uint32)
+        assert (bits & 0xFFFF == 0).all()
+        assert np.array_equal(got, (bits >> 16).astype(np.uint16))
+    q = np.array([[0x7E, 0x38, 0x39, 0x38, 0x7F, 0xFF, 0x00, 0x80, 0x01]], np.uint8)
+    third = np.float32(1.0 / 3.0)  # 0x3EAAAAAB
+    # 448 * fp32(1/3): the FP32 product is 0x43155556, whose low half 0x5556 rounds down -> 0x4315
+    assert oracle.dequantize_fp8(q[:, :1], np.array([third], np.float32))[0, 0] == 0x4315
+    # 1.0 * (1 + 2^-8) = 0x3F808000: a tie, high half even -> 0x3F80
+    # 1.125 * (1 + 2^-8) = 0x3F909000: above the tie -> 0x3F91
+    assert list(oracle.dequantize_fp8(q[:, 1:3], np.array([1 + 2.0 ** -8], np.float32))[0]) == [0x3F80, 0x3F91]
+    # 1.0 * (1 + 2^-7 + 2^-8) = 0x3F818000: a tie, high half odd -> 0x3F82
+    assert oracle.dequantize_fp8(q[:, 3:4], np.array([1 + 2.0 ** -7 + 2.0 ** -8], np.float32))[0, 0] == 0x3F82
+    # NaN codes -> 0x7FC0; +0 and -0 keep their sign; the smallest subnormal 2^-9 -> 0x3B00
+    assert list(oracle.dequantize_fp8(q[:, 4:], np.array([1.0], np.float32))[0]) == [0x7FC0, 0x7FC0, 0x0000,
+                                                                                      0x8000, 0x3B00]
