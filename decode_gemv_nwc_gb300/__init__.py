@@ -117,6 +117,18 @@ def encode(w_bits: np.ndarray, elem: int = BF16, threads: int = 0) -> bytes:
     return out.tobytes()
 
 
+def encode_fused(ws, elem: int = BF16, threads: int = 0):
+    """Fused projections (the NWC page's fuse step): matrices that read the same input (q, k, v;
+    gate, up) stacked row-wise and encoded as one blob, so that one GEMV serves them all.
+    ws: (N_i, K) BF16 bit arrays with a common K. Returns (blob, offsets), where rows
+    offsets[i] .. offsets[i + 1] of the fused output belong to ws[i]."""
+    ws = [np.asarray(w) for w in ws]
+    if not ws or any(w.ndim != 2 or w.shape[1] != ws[0].shape[1] for w in ws):
+        raise ValueError("encode_fused: 2-D matrices with a common column count")
+    offsets = np.concatenate([[0], np.cumsum([w.shape[0] for w in ws])]).astype(np.int64)
+    return encode(np.concatenate(ws, axis=0), elem=elem, threads=threads), offsets
+
+
 def encode_fp8(q: np.ndarray, scales: np.ndarray, threads: int = 0) -> bytes:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = np.ascontiguousarray(scales, dtype=np.float32)

@@ -86,3 +86,14 @@ def test_fp8_rejects_non_finite():
     w[1, 3] = 0x7F80  # +Inf
     with pytest.raises(nwc.NwcError):
         nwc.encode(w, elem=nwc.FP8)
+
+
+def test_encode_fused_stacks_rows():
+    """Fused projections: one blob of the row-stacked matrices (equal to encoding the stack),
+    with the row offsets of each part; a mismatched column count is refused."""
+    ws = [synth.normal_bf16((n, 700), 0.02, seed=n) for n in (24, 5, 5)]
+    blob, off = nwc.encode_fused(ws)
+    assert blob == oracle.encode(np.concatenate(ws))
+    assert list(off) == [0, 24, 29, 34]
+    with pytest.raises(ValueError):
+        nwc.encode_fused([ws[0], synth.normal_bf16((4, 600), 0.02, seed=1)])
