@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "BF16", "FP8", "NwcError", "lib", "encode", "encode_fp8", "quantize_fp8", "validate",
-    "Matrix", "check", "sm_count", "status_str", "save", "load",
+    "Matrix", "check", "sm_count", "status_str", "save", "load", "decode_table",
 ]
 
 BF16, FP8 = 0, 1
@@ -38,7 +38,7 @@ class NwcMatrix(ctypes.Structure):
         ("rank_exp", ctypes.c_uint8 * 16),
         ("block_tab", ctypes.c_void_p), ("data", ctypes.c_void_p), ("scales", ctypes.c_void_p),
         ("blob_bytes", ctypes.c_uint64), ("max_block_bytes", ctypes.c_uint64),
-        ("data_bytes", ctypes.c_uint64),
+        ("data_bytes", ctypes.c_uint64), ("table", ctypes.c_void_p),
     ]
 
 
@@ -75,10 +75,11 @@ def lib():
     L.nwc_gemv_batch.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, i32, p, i64, p, sz, p]
     L.nwc_gather.argtypes = [ctypes.POINTER(NwcMatrix), p, i64, p, i64, p]
     L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+    L.nwc_decode_table.argtypes = [ctypes.POINTER(NwcMatrix), p]
     L.nwc_sm_count.restype = i32
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
                  "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gemv_batch_prepare",
-                 "nwc_gemv_batch", "nwc_gather", "nwc_check"):
+                 "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -166,15 +167,24 @@ def check(stream=None):
     return int(st), int(flags.value)
 
 
+def decode_table(m: NwcMatrix) -> np.ndarray:
+    """The matrix's decode table (uint32[8192]) built on the host by nwc_decode_table."""
+    t = np.empty(8192, np.uint32)
+    _ok(lib().nwc_decode_table(ctypes.byref(m), _np_ptr(t)), "nwc_decode_table")
+    return t
+
+
 class Matrix:
     """A blob resident in device memory and bound through nwc_bind.
 
     ``device_blob`` is a torch uint8 CUDA tensor holding the blob (caller-visible so that
-    benchmarks can keep several copies); the GEMV workspace is allocated once, its counters
-    zeroed by nwc_gemv_prepare, and reused by every call.
+    benchmarks can keep several copies); the decode table is built on the host, copied to the
+    device once and named in the bound matrix (``table=False`` leaves it out: every kernel then
+    builds it in shared memory); the GEMV workspace is allocated once, put in its starting state
+    by nwc_gemv_prepare, and reused by every call.
     """
 
-    def __init__(self, blob: bytes, device="cuda", device_blob=None):
+    def __init__(self, blob: bytes, device="cuda", device_blob=None, table: bool = True):
         import torch
         host = np.frombuffer(blob, np.uint8)
         if device_blob is None:
@@ -183,6 +193,10 @@ class Matrix:
         self.m = NwcMatrix()
         _ok(lib().nwc_bind(_np_ptr(host), len(blob), ctypes.c_void_p(device_blob.data_ptr()), ctypes.byref(self.m)),
             "nwc_bind")
+        self.table = None
+        if table:
+            self.table = torch.from_numpy(decode_table(self.m).view(np.int32)).to(device_blob.device)
+            self.m.table = ctypes.c_void_p(self.table.data_ptr())
         self.elem, self.n, self.k = self.m.elem, self.m.n, self.m.k
         self.blob_bytes = len(blob)
         ws = int(lib().nwc_gemv_workspace_bytes(ctypes.byref(self.m)))

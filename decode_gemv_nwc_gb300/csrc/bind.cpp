@@ -1,12 +1,13 @@
 // bind.cpp -- host-side validation of an NWC blob and binding of its device copy.
 //
 // Validation covers everything the kernels trust without checking: header fields, the rank
-// table (exponents ranked by frequency, at most 11 ranked values), the block table,
-// each block region's size, which must equal its 32 lane word counts plus the mantissa
-// regions implied by the block's real rows and columns (fillers carry no mantissa, as the
-// "How it works" section of "NWC -- Neural Weight Compression" states) plus its escape list,
-// and the escape list itself: every entry names a real element of the block, in (lane, t)
-// order without repeats, with an unranked exponent, followed by fewer than four padding words.
+// table (exponents ranked by frequency, at most 12 ranked values), the block table, each
+// block region's size, which must equal its 32 lane code streams (at most 26 words each: 64
+// row pairs of at most 13 bits) plus the raw section implied by the block's real columns
+// (fillers past K carry no raw bits, as the "How it works" section of "NWC -- Neural Weight
+// Compression" states for padding) plus its escape list, and the escape list itself: every
+// entry names a real element of the block, in (lane, t) order without repeats, with an
+// exponent field of the element's width, followed by fewer than four padding words.
 // Lane stream contents are checked on the device while decoding.
 #include <cstring>
 #include <string>
@@ -53,6 +54,8 @@ nwc_status parse_and_check(const uint8_t *b, uint64_t bytes, Parsed &p) {
     if (p.n == 0 || p.k == 0 || p.n >= (1ull << 40) || p.k >= (1ull << 40)) return NWC_ERR_FORMAT;
     p.rb = cdiv(p.n, kRows);
     p.cb = cdiv(p.k, kCols);
+    // the block count must stay below 2^31; checked before the product so that it cannot wrap
+    if (p.rb > ((1ull << 31) - 1) / p.cb) return NWC_ERR_FORMAT;
     if (p.nb != p.rb * p.cb || p.nb >= (1ull << 31)) return NWC_ERR_FORMAT;
     if (p.total != bytes || p.off_blocks != kBlockTabOff) return NWC_ERR_FORMAT;
     const uint64_t tab_end = p.off_blocks + 4 * (p.nb + 1);
@@ -76,7 +79,7 @@ nwc_status parse_and_check(const uint8_t *b, uint64_t bytes, Parsed &p) {
     const uint8_t *tab = b + p.off_blocks;
     if (rd32(tab) != 0) return NWC_ERR_FORMAT;
     if (p.off_data + 16 * (uint64_t)rd32(tab + 4 * p.nb) != bytes) return NWC_ERR_FORMAT;
-    const int F = man_bits(p.elem);
+    const int eb = exp_bits(p.elem);
     p.max_block = 0;
     for (uint64_t i = 0; i < p.nb; i++) {
         uint64_t s = rd32(tab + 4 * i), e = rd32(tab + 4 * (i + 1));
@@ -84,14 +87,13 @@ nwc_status parse_and_check(const uint8_t *b, uint64_t bytes, Parsed &p) {
         uint64_t start = p.off_data + 16 * s, len = 16 * (e - s);
         if (len < 32 || start + len > bytes) return NWC_ERR_FORMAT;
         const uint8_t *lw = b + start;
-        uint64_t rb = i / p.cb, cb = i % p.cb, words = 0, man = 0;
+        uint64_t rb = i / p.cb, cb = i % p.cb, words = 0;
         int rows = real_rows(p.n, rb);
         for (int l = 0; l < kLanes; l++) {
             if (lw[l] > kMaxLaneWords) return NWC_ERR_FORMAT;
             words += lw[l];
-            man += man_words(rows, real_cols(p.k, cb, l), F);
         }
-        const uint64_t esc_off = up16(32 + 4 * words) + 4 * man;
+        const uint64_t esc_off = up16(32 + 4 * words) + raw_section_bytes(p.k, cb, p.elem);
         if (esc_off > len) return NWC_ERR_FORMAT;
         const uint64_t slots = (len - esc_off) / 4;
         int64_t last = -1;
@@ -105,10 +107,7 @@ nwc_status parse_and_check(const uint8_t *b, uint64_t bytes, Parsed &p) {
             last = key;
             const int t = (int)esc_t(e);
             if (t % kRows >= rows || t / kRows >= real_cols(p.k, cb, (int)esc_lane(e))) return NWC_ERR_FORMAT;
-            const uint32_t bits = esc_bits(e);
-            if (bits >> (p.elem == NWC_ELEM_BF16 ? 16 : 8)) return NWC_ERR_FORMAT;
-            const uint32_t v = p.elem == NWC_ELEM_BF16 ? (bits >> 7) & 0xFFu : (bits >> 3) & 0xFu;
-            if (seen[v]) return NWC_ERR_FORMAT;  // a ranked exponent is never escaped
+            if (esc_v(e) >> eb) return NWC_ERR_FORMAT;  // exponent field wider than the element's
             entries++;
         }
         if (slots - entries > 3) return NWC_ERR_FORMAT;

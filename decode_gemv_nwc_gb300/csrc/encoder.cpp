@@ -1,19 +1,22 @@
 // encoder.cpp -- host encoder of the NWC blob and the fp8 e4m3 quantizer.
 //
 // "NWC -- Neural Weight Compression", section "How it works": a BF16 weight is split into a
-// raw mantissa plane and an exponent/sign part; the exponent is ranked by frequency and
-// written as a unary rank code plus a raw sign bit, with an escape for rare values (in the
-// stream n_ranked ones and the sign; the element's bits go to the block's escape list, so that
-// no in-stream code is longer than 12 bits); every lane of a block of 8 rows x 512 columns has
-// its own bit stream; padding to any shape costs 2 bits per filler weight and no mantissa.
-// Mantissa regions are interleaved word by word across the lanes when all lanes have the same
-// word count (every block whose 512 columns are all inside K).
+// raw part and an entropy-coded exponent; the exponent is ranked by frequency and written as a
+// unary rank code, the sign is a raw bit (kept here beside the raw mantissa, a byte per
+// element), with an escape for rare values (n_ranked ones in the stream, the exponent in the
+// block's escape list); a 12-bit peek yields up to two codes: here every row pair of a lane is
+// written so that one 13-bit peek holds it (a longer pair keeps its first code and ones up to
+// 13 bits, and its second element is listed); every lane of a block of 8 rows x 512 columns
+// has its own bit stream; padding to any shape costs a one-bit code per filler weight and no
+// raw bits past K.
 // "Qwen3-4B-NWC-fp8": weight-only e4m3, symmetric per-output-channel scale, bytes coded
-// losslessly with the same code (4-bit exponent, 3-bit raw mantissa).
+// losslessly with the same code (4-bit exponent; sign and 3-bit mantissa raw, a nibble). The
+// subnormal and NaN codes are listed as well, so that the kernels can treat every other e4m3
+// value as a BF16 pattern.
 //
-// Work is split over row-blocks across host threads. Pass 1 sizes every block region from a
-// per-exponent code-length table, pass 2 writes each region at its prefix-summed offset, so
-// the bytes do not depend on the thread count.
+// Work is split over row-blocks across host threads. Pass 1 sizes every block region, pass 2
+// writes each region at its prefix-summed offset, so the bytes do not depend on the thread
+// count.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -29,9 +32,9 @@ using namespace nwcf;
 namespace {
 
 struct Codebook {
-    int elem = 0, nr = 0, eb = 8, F = 7;
-    uint32_t code[256];  // code of the exponent value with its sign slot (sign bit = 0)
-    uint8_t len[256];    // code length including the sign bit
+    int elem = 0, nr = 0;
+    uint32_t code[256];  // code bits of the exponent value, most significant bit first
+    uint8_t len[256];    // code length
     uint8_t rank_exp[16];
     bool escaped[256];
 };
@@ -41,25 +44,23 @@ struct Codebook {
 Codebook make_codebook(const uint64_t *hist, int elem) {
     Codebook cb;
     cb.elem = elem;
-    cb.eb = exp_bits(elem);
-    cb.F = man_bits(elem);
-    int nv = 1 << cb.eb;
+    const int nv = 1 << exp_bits(elem);
     std::vector<int> vals;
     for (int v = 0; v < nv; v++)
         if (hist[v]) vals.push_back(v);
     std::stable_sort(vals.begin(), vals.end(), [&](int a, int b) { return hist[a] > hist[b]; });
     cb.nr = std::min<int>((int)vals.size(), kMaxRanked);
     std::memset(cb.rank_exp, 0, sizeof(cb.rank_exp));
-    for (int v = 0; v < nv; v++) {  // escape: nr ones, sign
-        cb.code[v] = ((1u << cb.nr) - 1u) << 1;
-        cb.len[v] = (uint8_t)(cb.nr + 1);
+    for (int v = 0; v < nv; v++) {  // escape: nr ones
+        cb.code[v] = (1u << cb.nr) - 1u;
+        cb.len[v] = (uint8_t)cb.nr;
         cb.escaped[v] = true;
     }
-    for (int p = 0; p < cb.nr; p++) {  // rank p: p ones, a zero, sign
-        int v = vals[p];
+    for (int p = 0; p < cb.nr; p++) {  // rank p: p ones, a zero
+        const int v = vals[p];
         cb.rank_exp[p] = (uint8_t)v;
-        cb.code[v] = ((1u << p) - 1u) << 2;
-        cb.len[v] = (uint8_t)(p + 2);
+        cb.code[v] = ((1u << p) - 1u) << 1;
+        cb.len[v] = (uint8_t)(p + 1);
         cb.escaped[v] = false;
     }
     return cb;
@@ -78,7 +79,10 @@ inline void fields(int elem, uint32_t x, uint32_t &s, uint32_t &v, uint32_t &m) 
     else { s = (x >> 7) & 1; v = (x >> 3) & 0xF; m = x & 7; }
 }
 
-// MSB-first bit sink into 32-bit words.
+// fp8 codes the kernels cannot treat as a rebiased BF16 pattern: subnormals and NaN.
+inline bool fp8_listed(uint32_t v, uint32_t m) { return (v == 0 && m != 0) || (v == 15 && m == 7); }
+
+// MSB-first bit sink into 32-bit words (out == nullptr: count only).
 struct CodeSink {
     uint32_t *out;
     uint64_t acc = 0;
@@ -89,14 +93,14 @@ struct CodeSink {
         nacc += n;
         if (nacc >= 32) {
             nacc -= 32;
-            uint32_t w = (uint32_t)(acc >> nacc);
+            const uint32_t w = (uint32_t)(acc >> nacc);
             if (out) out[nw] = w;
             nw++;
         }
     }
     void flush() {
         if (nacc > 0) {
-            uint32_t w = (uint32_t)(acc << (32 - nacc));
+            const uint32_t w = (uint32_t)(acc << (32 - nacc));
             if (out) out[nw] = w;
             nw++;
             nacc = 0;
@@ -104,109 +108,105 @@ struct CodeSink {
     }
 };
 
-// LSB-first F-bit fields into 16-bit half-words.
-struct HalfSink {
-    uint16_t h[kSyms];
-    uint32_t acc = 0;
-    int nacc = 0, nh = 0;
-    void put(uint32_t m, int F) {
-        acc |= m << nacc;
-        nacc += F;
-        if (nacc >= 16) {
-            h[nh++] = (uint16_t)acc;
-            acc >>= 16;
-            nacc -= 16;
-        }
-    }
-    void flush() {
-        if (nacc > 0) { h[nh++] = (uint16_t)acc; acc = 0; nacc = 0; }
-    }
-};
-
-// Size in bytes of block (rb, cb)'s region; with lane word counts.
+// Lane l of block (rb, cbi): writes (or, with out == nullptr, counts) its code stream and
+// appends its listed elements (t | lane << 7 | v << 12) to esc (when non-null). Returns the
+// lane's word count; *n_list receives the number of listed elements.
 template <class E>
-uint64_t block_size(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *lw) {
-    int rows = real_rows(src.n, rb);
-    uint64_t code_words = 0, man = 0, n_esc = 0;
+uint32_t lane_stream(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, int l, uint32_t *out,
+                     uint32_t *esc, uint32_t *n_list) {
+    const int rows = real_rows(src.n, rb), cols = real_cols(src.k, cbi, l);
+    CodeSink cs;
+    cs.out = out;
+    uint32_t listed = 0;
+    for (int j = 0; j < kPairs; j++) {
+        const int c = j >> 2, r0 = 2 * (j & 3);
+        uint32_t code[2], v[2] = {0, 0};
+        int len[2];
+        bool real[2], lst[2] = {false, false};
+        for (int h = 0; h < 2; h++) {
+            real[h] = r0 + h < rows && c < cols;
+            if (!real[h]) {  // filler: the rank-0 code, a zero bit
+                code[h] = 0;
+                len[h] = 1;
+                continue;
+            }
+            uint32_t s, m;
+            fields(cbk.elem, src.at(rb * kRows + r0 + h, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v[h], m);
+            code[h] = cbk.code[v[h]];
+            len[h] = cbk.len[v[h]];
+            lst[h] = cbk.escaped[v[h]] || (cbk.elem == 1 && fp8_listed(v[h], m));
+        }
+        cs.put(code[0], len[0]);
+        if (len[0] + len[1] <= kPeek) {
+            cs.put(code[1], len[1]);
+        } else {  // the pair is cut: ones up to kPeek bits, the second element listed
+            const int tail = kPeek - len[0];
+            cs.put((1u << tail) - 1u, tail);
+            lst[1] = real[1];
+        }
+        for (int h = 0; h < 2; h++)
+            if (lst[h]) {
+                if (esc) esc[listed] = esc_entry((uint32_t)(8 * c + r0 + h), (uint32_t)l, v[h]);
+                listed++;
+            }
+    }
+    cs.flush();
+    *n_list = listed;
+    return cs.nw;
+}
+
+// Size in bytes of block (rb, cb)'s region.
+template <class E>
+uint64_t block_size(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi) {
+    uint64_t code_words = 0, n_esc = 0;
     for (int l = 0; l < kLanes; l++) {
-        int cols = real_cols(src.k, cbi, l);
-        uint32_t bits = 2u * (uint32_t)(kSyms - rows * cols);  // fillers
+        uint32_t nl;
+        code_words += lane_stream(src, cbk, rb, cbi, l, nullptr, nullptr, &nl);
+        n_esc += nl;
+    }
+    return up16(32 + 4 * code_words) + raw_section_bytes(src.k, cbi, cbk.elem) + up16(4 * n_esc);
+}
+
+// Writes block (rb, cb)'s region of `size` bytes at dst (16-byte aligned, zeroed).
+template <class E>
+void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *dst, uint64_t size) {
+    const int rows = real_rows(src.n, rb);
+    uint32_t *words = reinterpret_cast<uint32_t *>(dst + 32);
+    std::vector<uint32_t> esc;
+    esc.reserve(kSyms);
+    uint32_t pos = 0, lane_list[kSyms];
+    for (int l = 0; l < kLanes; l++) {
+        uint32_t nl;
+        const uint32_t nw = lane_stream(src, cbk, rb, cbi, l, words + pos, lane_list, &nl);
+        dst[l] = (uint8_t)nw;
+        pos += nw;
+        esc.insert(esc.end(), lane_list, lane_list + nl);
+    }
+    uint8_t *raw = dst + up16(32 + 4 * (uint64_t)pos);
+    const bool full = raw_full(src.k, cbi);
+    uint32_t lane_off = 0;
+    for (int l = 0; l < kLanes; l++) {
+        const int cols = real_cols(src.k, cbi, l);
         for (int c = 0; c < cols; c++)
             for (int r = 0; r < rows; r++) {
                 uint32_t s, v, m;
                 fields(cbk.elem, src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m);
-                bits += cbk.len[v];
-                n_esc += cbk.escaped[v];
+                if (cbk.elem == 0) {
+                    const uint32_t at = full ? 16u * (32u * (uint32_t)(c >> 1) + (uint32_t)l) + 8u * (uint32_t)(c & 1) + (uint32_t)r
+                                             : lane_off + 8u * (uint32_t)c + (uint32_t)r;
+                    raw[at] = (uint8_t)((s << 7) | m);
+                } else {
+                    const uint32_t at = full ? 16u * (32u * (uint32_t)(c >> 2) + (uint32_t)l) + 4u * (uint32_t)(c & 3) + (uint32_t)(r >> 1)
+                                             : lane_off + 4u * (uint32_t)c + (uint32_t)(r >> 1);
+                    raw[at] |= (uint8_t)(((s << 3) | m) << (4 * (r & 1)));
+                }
             }
-        uint32_t nw = (bits + 31) / 32;
-        if (lw) lw[l] = (uint8_t)nw;
-        code_words += nw;
-        man += man_words(rows, cols, cbk.F);
+        if (!full) lane_off += lane_raw_bytes(src.k, cbi, l, cbk.elem);
     }
-    return up16(32 + 4 * code_words) + 4 * man + up16(4 * n_esc);
-}
-
-template <class E>
-void write_block(const Src<E> &src, const Codebook &cbk, uint64_t rb, uint64_t cbi, uint8_t *dst, uint64_t size) {
-    int rows = real_rows(src.n, rb);
-    uint32_t *words = reinterpret_cast<uint32_t *>(dst + 32);  // dst is 16-byte aligned
-    uint32_t pos = 0;
-    for (int l = 0; l < kLanes; l++) {
-        int cols = real_cols(src.k, cbi, l);
-        CodeSink cs;
-        cs.out = words + pos;
-        for (int t = 0; t < kSyms; t++) {
-            int c = t / kRows, r = t % kRows;
-            if (r >= rows || c >= cols) { cs.put(0, 2); continue; }
-            uint32_t s, v, m;
-            fields(cbk.elem, src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m);
-            cs.put(cbk.code[v] | s, cbk.len[v]);
-        }
-        cs.flush();
-        dst[l] = (uint8_t)cs.nw;
-        pos += cs.nw;
-    }
-    uint8_t *man = dst + up16(32 + 4 * (uint64_t)pos);
-    // all lanes with the same word count: word k of lane l at 32k + l (interleaved)
-    bool uniform = true;
-    for (int l = 1; l < kLanes; l++)
-        uniform &= man_words(rows, real_cols(src.k, cbi, l), cbk.F) == man_words(rows, real_cols(src.k, cbi, 0), cbk.F);
-    uint32_t *man0 = reinterpret_cast<uint32_t *>(man);
-    for (int l = 0; l < kLanes; l++) {
-        int cols = real_cols(src.k, cbi, l);
-        HalfSink ev, od;
-        for (int t = 0; t < kSyms; t++) {
-            int c = t / kRows, r = t % kRows;
-            if (r >= rows || c >= cols) continue;
-            uint32_t s, v, m;
-            fields(cbk.elem, src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m);
-            (r % 2 == 0 ? ev : od).put(m, cbk.F);
-        }
-        ev.flush();
-        od.flush();
-        uint32_t mw = man_words(rows, cols, cbk.F);
-        uint32_t *mwp = reinterpret_cast<uint32_t *>(man);
-        for (uint32_t i = 0; i < mw; i++) {
-            uint32_t lo = (int)i < ev.nh ? ev.h[i] : 0, hi = (int)i < od.nh ? od.h[i] : 0;
-            if (uniform) man0[i * kLanes + (uint32_t)l] = lo | (hi << 16);
-            else mwp[i] = lo | (hi << 16);
-        }
-        man += 4 * mw;
-    }
-    // escape list: lanes in order, t increasing; padding to the region's end
-    uint32_t *esc = reinterpret_cast<uint32_t *>(man);
-    uint32_t *esc_end = reinterpret_cast<uint32_t *>(dst + size);
-    for (int l = 0; l < kLanes; l++) {
-        int cols = real_cols(src.k, cbi, l);
-        for (int t = 0; t < kSyms; t++) {
-            int c = t / kRows, r = t % kRows;
-            if (r >= rows || c >= cols) continue;
-            uint32_t x = src.at(rb * kRows + r, cbi * kCols + (uint64_t)l * kLaneCols + c), s, v, m;
-            fields(cbk.elem, x, s, v, m);
-            if (cbk.escaped[v]) *esc++ = esc_entry((uint32_t)t, (uint32_t)l, x);
-        }
-    }
-    while (esc < esc_end) *esc++ = kEscPad;
+    uint32_t *list = reinterpret_cast<uint32_t *>(raw + raw_section_bytes(src.k, cbi, cbk.elem));
+    uint32_t *list_end = reinterpret_cast<uint32_t *>(dst + size);
+    for (uint32_t e : esc) *list++ = e;
+    while (list < list_end) *list++ = kEscPad;
 }
 
 int pick_threads(int threads) {
@@ -264,7 +264,7 @@ nwc_status encode_impl(const Src<E> &src, int elem, const float *scales, int thr
 
     std::vector<uint64_t> size(NB);
     parallel_for(RB, threads, [&](uint64_t rb) {
-        for (uint64_t c = 0; c < CB; c++) size[rb * CB + c] = block_size(src, cbk, rb, c, nullptr);
+        for (uint64_t c = 0; c < CB; c++) size[rb * CB + c] = block_size(src, cbk, rb, c);
     });
     std::vector<uint64_t> off(NB + 1, 0);
     for (uint64_t b = 0; b < NB; b++) off[b + 1] = off[b] + size[b];

@@ -59,7 +59,10 @@ enum { NWC_ELEM_BF16 = 0, NWC_ELEM_FP8_E4M3 = 1 };
 
 /* Geometry of the format (fixed by the pages: blocks of 8 rows x 512 columns, 32 lanes of
  * 16 columns x 8 rows). */
-enum { NWC_BLOCK_ROWS = 8, NWC_BLOCK_COLS = 512, NWC_LANES = 32, NWC_MAX_RANKED = 11 };
+enum { NWC_BLOCK_ROWS = 8, NWC_BLOCK_COLS = 512, NWC_LANES = 32, NWC_MAX_RANKED = 12 };
+
+/* Entries and bytes of a matrix's decode table (see nwc_decode_table). */
+enum { NWC_TABLE_ENTRIES = 8192, NWC_TABLE_BYTES = 32768 };
 
 /*
  * A bound, validated matrix: plain data, safe to copy by value. Built by nwc_bind from the
@@ -79,6 +82,9 @@ typedef struct nwc_matrix {
     uint64_t blob_bytes;     /* size of the whole blob                                      */
     uint64_t max_block_bytes;/* largest block region                                        */
     uint64_t data_bytes;     /* bytes of all block regions                                  */
+    const uint32_t *table;   /* device copy of the decode table (nwc_decode_table), or NULL:   */
+                             /* set by the caller after nwc_bind; NULL makes every kernel      */
+                             /* build the table in shared memory itself (slower prologue)      */
 } nwc_matrix;
 
 /* Human-readable name of a status code (static string). */

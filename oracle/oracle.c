@@ -2,78 +2,85 @@
  * oracle.c -- plain, slow CPU reference for the NWC entropy-coded matrix format.
  *
  * TEST INFRASTRUCTURE ONLY. The product library never links, loads or calls this
- * file; only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg use it.
+ * file; only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline legs use it.
  * It shares no code with the library (decode_gemv_nwc_gb300/csrc): both are written
  * independently from the format definition below.
  *
  * Sources (the pages this restates; reading choices are marked READING):
  *   [P1] "NWC -- Neural Weight Compression" (PyPI project page, v0.9.0),
  *        section "How it works":
- *          - byte planes: the mantissa is stored raw, the exponent/sign part is
- *            entropy coded;
+ *          - byte planes: the mantissa is stored raw, the exponent is entropy coded;
  *          - prefix code: exponent ranked by frequency, written as a unary rank code
  *            plus a raw sign bit, escape for rare values;
+ *          - a 12-bit peek into a shared-memory table yields up to two complete codes;
  *          - fused kernel: each lane decodes its own bit stream for a block of
  *            8 rows x 512 columns (16 columns x 8 rows per lane); any shape works,
- *            padding costs 2 bits per filler weight and no mantissa.
+ *            padding costs a short code per filler weight and no mantissa.
  *   [P2] "Qwen3-4B-NWC-fp8" (model card): weight-only fp8 e4m3 with a symmetric
  *        per-output-channel scale; the fp8 bytes are coded losslessly.
  *
- * FORMAT (little-endian):
+ * FORMAT, version 4 (little-endian):
  *   header, 64 bytes
- *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 3
- *     6  u8  elem (0 = BF16, 1 = FP8 e4m3)  7  u8  n_ranked (1..11)
+ *     0  u32 magic 0x3143574E ("NWC1")      4  u16 version = 4
+ *     6  u8  elem (0 = BF16, 1 = FP8 e4m3)  7  u8  n_ranked R (1..12)
  *     8  u64 N    16 u64 K    24 u64 n_blocks = ceil(N/8) * ceil(K/512)
  *     32 u64 off_blocks   40 u64 off_scales (0 for BF16)   48 u64 off_data
  *     56 u64 total_bytes
- *   64: u8 rank_exp[16]  -- exponent value of rank 0..n_ranked-1, rest zero
+ *   64: u8 rank_exp[16]  -- exponent field value of rank 0..R-1, rest zero
  *   off_blocks: u32 tab[n_blocks + 1]; block b occupies bytes
  *        [off_data + 16*tab[b], off_data + 16*tab[b+1]); padded to 16 bytes
  *   off_scales (FP8 only): f32 scale[N]; padded to 16 bytes
  *   off_data: block regions, row-block-major (b = rb * CB + cb)
- *   block region: u8 lane_words[32]; then the 32 lane code streams (lane 0 first),
- *     each a whole number of u32 words; zero padding to 16 bytes; then the 32 lane
- *     mantissa regions (lane 0 first), each a multiple of 16 bytes; then the block's
- *     escape list: one u32 per escaped element, t | lane << 7 | value << 12 (value =
- *     the element's full bit pattern), lanes in order and t increasing within a lane,
- *     padded to 16 bytes with 0xFFFFFFFF.
+ *   block region: u8 lane_words[32]; the 32 lane code streams (lane 0 first), each
+ *     a whole number of u32 words; zero padding to 16 bytes; the raw section; the
+ *     escape list (u32 entries, padded to 16 bytes with 0xFFFFFFFF).
  *
- *   Fields of one element (READING: BF16 splits into a raw 7-bit mantissa and a
- *   coded 8-bit exponent with a raw sign; fp8 likewise with 4-bit exponent, 3-bit
- *   mantissa):  BF16 b: s = b>>15, v = (b>>7)&0xFF, m = b&0x7F
- *               FP8  q: s = q>>7,  v = (q>>3)&0xF,  m = q&7
+ *   Fields of one element (READING: the sign is a raw bit and is stored beside the
+ *   raw mantissa, so the raw plane is a whole byte per BF16 element and the coded
+ *   stream holds only the exponent's rank code):
+ *       BF16 b: s = b>>15, v = (b>>7)&0xFF, m = b&0x7F, raw byte   = s<<7 | m
+ *       FP8  q: s = q>>7,  v = (q>>3)&0xF,  m = q&7,    raw nibble = s<<3 | m
  *   Ranking: histogram of v over the N*K real elements; ranks by (count desc,
- *     v asc) over values with count > 0; n_ranked = min(11, #distinct values).
- *     (READING: tie-break by ascending value; at most 11 ranked values so that any
- *     ranked code with its sign fits a 12-bit peek.)
- *   Code of one element, bits appended in order:
- *     ranked (rank p < n_ranked): p one-bits, one zero-bit, the sign bit;
- *     escape (v unranked): n_ranked one-bits, the sign bit; the element's exponent
- *     bits (8 BF16 / 4 fp8, with the rest of the element) are in the block's escape
- *     list. (READING: the pages' escape for rare exponents, with the raw exponent kept outside the
- *     lane stream, so that every in-stream code is at most 12 bits.)
- *     filler (row >= N or col >= K): the rank-0 code with sign 0, i.e. two zero
- *     bits, and no mantissa.
- *   Lane stream of block (rb, cb), lane l: elements t = 8c + r, c = 0..15,
- *     r = 0..7, at row 8rb + r, column 512cb + 16l + c (READING: column-outer
- *     order). Bits fill u32 words most significant bit first (stream bit i is bit
+ *     v asc) over values with count > 0; R = min(12, #distinct values).
+ *     (READING: tie-break by ascending value.)
+ *   Code of one symbol: ranked v (rank p < R): p one-bits then a zero-bit (p + 1
+ *     bits); unranked v (escape): R one-bits; filler (row >= N or col >= K): the
+ *     rank-0 code, one zero-bit. (READING: an escape for rare exponents whose raw
+ *     exponent sits in the block's escape list, outside the stream.)
+ *   Lane stream of block (rb, cb), lane l: symbols t = 8c + r, c = 0..15, r = 0..7,
+ *     at row 8rb + r, column 512cb + 16l + c, taken in pairs j = 0..63 of symbols
+ *     (2j, 2j+1) (rows 2i, 2i+1 of column c = j/4, i = j%4). A pair with codes of
+ *     lengths La, Lb is written as both codes when La + Lb <= 13; otherwise as the
+ *     first code followed by 13 - La one-bits, and the second symbol's exponent goes
+ *     to the escape list (READING: the pages' peek yields up to two codes; here a
+ *     13-bit peek always holds one pair, and a pair too long for it is cut).
+ *     Bits fill u32 words most significant bit first (stream bit i is bit
  *     31 - i%32 of word i/32); the last word is zero padded.
- *   Lane mantissa region: the mantissas of the lane's REAL elements with even t
- *     form the even half-stream, those with odd t the odd half-stream, each in
- *     increasing t. Field j of a half-stream (F = 7 or 3 bits) occupies half-stream
- *     bits [F*j, F*j + F), least significant bit first; half-stream bit i is bit
- *     i%16 of half-word i/16. Word k of the region = even half-word k |
- *     (odd half-word k << 16). Word count = ceil(max(F*n_even, F*n_odd) / 16)
- *     rounded up to a multiple of 4. (READING: bit packed, so that the raw plane
- *     costs F bits per element; even/odd halves so that the two mantissas of a row
- *     pair sit 16 bits apart.)
- *   Mantissa regions of a block: when all 32 lanes have the same word count W, word k of
- *     lane l is word 32k + l of the block's mantissa section (interleaved, so that the 32
- *     lanes reading their word k touch 32 consecutive words); otherwise the lanes' regions
- *     follow one another, lane 0 first. (READING: a layout choice with no size cost.)
+ *   Escape list: one u32 per listed element, t | lane << 7 | v << 12, lanes in order
+ *     and t increasing within a lane. Listed are the real elements whose exponent is
+ *     unranked, the real second elements of cut pairs, and (FP8 only) the real
+ *     elements with v = 0 and m != 0 (subnormals) or v = 15 and m = 7 (NaN).
+ *     (READING: the FP8 exceptions are listed so that every other e4m3 value is a
+ *     BF16 bit pattern with exponent field v + 120.)
+ *   Raw section: a block whose 512 columns are all < K is "full": BF16 4096 bytes,
+ *     the byte of row r, column c of lane l at 16*(32*(c/2) + l) + 8*(c%2) + r;
+ *     FP8 2048 bytes, the byte holding rows 2i (low nibble) and 2i+1 (high nibble) of
+ *     column c of lane l at 16*(32*(c/4) + l) + 4*(c%4) + i. Any other block: the
+ *     lanes' regions follow one another (lane 0 first), lane l's region holding its
+ *     real columns in order (8 bytes, resp. 4 bytes, per column as above) and zero
+ *     padding to 16 bytes. Rows >= N of a real column hold zero.
+ *     (READING: the filler rows of the last row block keep a zero raw byte, so that
+ *     every real column has the same raw layout; fillers past K have none.)
  *   FP8 quantization of row n (READING of [P2]): a = max_k |w[n,k]| in FP32;
  *     s_n = a / 448 in FP32 (s_n = 1 when a = 0); q = e4m3 nearest to
  *     fp32(w) / s_n (FP32 division), ties to even, saturating at +-448.
+ *
+ *   Decoding a pair from the stream: count one-bits up to R: R of them is an escape,
+ *   fewer end at a zero-bit (rank = the count). The second code is read the same way
+ *   but if the first code took La bits and 13 - La < R one-bits follow with no zero
+ *   among them, the pair was cut: those bits are its tail and the second symbol is
+ *   listed. A listed element takes its exponent from the list, any other real element
+ *   the ranked exponent of its code.
  *
  *   Matrix-vector product (the plain definition): y_n = sum_k w[n,k] * x[k] with
  *   every product and the sum taken in FP64 (FP8: y_n = s_n * sum_k q[n,k] x[k]).
@@ -87,14 +94,15 @@
 #include <string.h>
 
 #define ORC_MAGIC 0x3143574Eu
-#define ORC_VERSION 3
-#define ORC_R 11
+#define ORC_VERSION 4
+#define ORC_R 12
+#define ORC_PEEK 13
 #define ORC_ROWS 8
 #define ORC_COLS 512
 #define ORC_LANES 32
 #define ORC_LANE_COLS 16
 #define ORC_SYMS 128
-#define ORC_MAX_LANE_WORDS 80 /* 128 codes * 20 bits / 32 */
+#define ORC_MAX_LANE_WORDS 26 /* 64 pairs * 13 bits / 32, rounded up */
 
 enum { ORC_BF16 = 0, ORC_FP8 = 1 };
 
@@ -134,13 +142,58 @@ static uint32_t join(int elem, uint32_t s, uint32_t v, uint32_t m) {
     return (s << 7) | (v << 3) | m;
 }
 static int exp_bits(int elem) { return elem == ORC_BF16 ? 8 : 4; }
-static int man_bits(int elem) { return elem == ORC_BF16 ? 7 : 3; }
+
+/* The raw bits of an element: BF16 a byte s<<7 | m, FP8 a nibble s<<3 | m. */
+static uint32_t raw_of(int elem, uint32_t s, uint32_t m) { return elem == ORC_BF16 ? (s << 7) | m : (s << 3) | m; }
+
+/* FP8 values that the format always lists: subnormals and NaN. */
+static int fp8_special(uint32_t v, uint32_t m) { return (v == 0 && m != 0) || (v == 15 && m == 7); }
 
 /* Position of element t of lane l in block (rb, cb). */
 static void position(uint64_t rb, uint64_t cb, int l, int t, uint64_t *row, uint64_t *col) {
     int c = t / ORC_ROWS, r = t % ORC_ROWS;
     *row = rb * ORC_ROWS + (uint64_t)r;
     *col = cb * ORC_COLS + (uint64_t)l * ORC_LANE_COLS + (uint64_t)c;
+}
+
+/* Real columns of lane l in column block cb. */
+static int lane_cols(uint64_t K, uint64_t cb, int l) {
+    uint64_t c0 = cb * ORC_COLS + (uint64_t)l * ORC_LANE_COLS;
+    if (c0 >= K) return 0;
+    return K - c0 >= ORC_LANE_COLS ? ORC_LANE_COLS : (int)(K - c0);
+}
+
+/* Bytes of raw data per column: 8 rows of a byte (BF16) or of a nibble (FP8). */
+static int col_bytes(int elem) { return elem == ORC_BF16 ? 8 : 4; }
+
+/* Offset of the raw bits of row r, column c of lane l inside the raw section, and the
+ * nibble (0 low, 1 high; always 0 for BF16). `full` selects the full-block layout;
+ * otherwise lane_off is the start of lane l's region. */
+static uint64_t raw_at(int elem, int full, int l, int c, int r, uint64_t lane_off, int *nib) {
+    if (elem == ORC_BF16) {
+        *nib = 0;
+        if (full) return 16 * (uint64_t)(32 * (c / 2) + l) + 8 * (uint64_t)(c % 2) + (uint64_t)r;
+        return lane_off + 8 * (uint64_t)c + (uint64_t)r;
+    }
+    *nib = r % 2;
+    if (full) return 16 * (uint64_t)(32 * (c / 4) + l) + 4 * (uint64_t)(c % 4) + (uint64_t)(r / 2);
+    return lane_off + 4 * (uint64_t)c + (uint64_t)(r / 2);
+}
+
+/* Size of a block's raw section; lane_off[l] receives each lane's region start
+ * (ragged layout). */
+static uint64_t raw_section(int elem, uint64_t K, uint64_t cb, uint64_t lane_off[ORC_LANES], int *full) {
+    *full = (cb + 1) * ORC_COLS <= K;
+    if (*full) {
+        for (int l = 0; l < ORC_LANES; l++) lane_off[l] = 0;
+        return (uint64_t)ORC_LANES * ORC_LANE_COLS * (uint64_t)col_bytes(elem);
+    }
+    uint64_t at = 0;
+    for (int l = 0; l < ORC_LANES; l++) {
+        lane_off[l] = at;
+        at += pad16((uint64_t)lane_cols(K, cb, l) * (uint64_t)col_bytes(elem));
+    }
+    return at;
 }
 
 /* --------------------------------------------------------------- bit writer */
@@ -151,16 +204,8 @@ static void bw_put(bitw *b, uint32_t bit) {
     if (bit) b->w[word] |= 1u << pos;
     b->nbits++;
 }
-
-/* half-stream writer: bit i -> bit i%16 of half-word i/16 */
-typedef struct { uint16_t h[ORC_SYMS]; int nbits; } halfw;
-
-static void hw_put_field(halfw *h, uint32_t value, int width) {
-    for (int i = 0; i < width; i++) {
-        int bit = h->nbits + i;
-        if ((value >> i) & 1) h->h[bit / 16] |= (uint16_t)(1u << (bit % 16));
-    }
-    h->nbits += width;
+static void bw_ones(bitw *b, int n) {
+    for (int i = 0; i < n; i++) bw_put(b, 1);
 }
 
 /* ------------------------------------------------------------------ ranking */
@@ -181,6 +226,15 @@ static int make_ranks(const uint64_t *count, int nvals, uint8_t *rank_exp, int *
 }
 
 /* ----------------------------------------------------------------- encoder */
+/* Code of one symbol: *len bits, most significant first in *code. */
+static void symbol_code(int nr, int rank, uint32_t *code, int *len) {
+    if (rank < 0) { *code = (1u << nr) - 1u; *len = nr; return; }      /* escape */
+    *code = ((1u << rank) - 1u) << 1; *len = rank + 1;                  /* rank ones, a zero */
+}
+static void put_code(bitw *b, uint32_t code, int len) {
+    for (int i = len - 1; i >= 0; i--) bw_put(b, (code >> i) & 1);
+}
+
 /*
  * Encodes an N x K matrix of BF16 bit patterns (elem 0, e[] holds uint16) or fp8
  * bytes (elem 1, e[] holds the byte values, scale[] the N row scales). Returns a
@@ -208,47 +262,47 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
     for (uint64_t b = 0; b < NB; b++) {
         uint64_t rb = b / CB, cb = b % CB;
         static bitw code[ORC_LANES];
-        static halfw even[ORC_LANES], odd[ORC_LANES];
         static uint32_t esc[ORC_LANES * ORC_SYMS];
         uint64_t n_esc = 0;
         memset(code, 0, sizeof(code));
-        memset(even, 0, sizeof(even));
-        memset(odd, 0, sizeof(odd));
-        int F = man_bits(elem);
         for (int l = 0; l < ORC_LANES; l++) {
-            for (int t = 0; t < ORC_SYMS; t++) {
-                uint64_t row, col;
-                position(rb, cb, l, t, &row, &col);
-                if (row >= N || col >= K) { /* filler: rank-0 code, sign 0 */
-                    bw_put(&code[l], 0);
-                    bw_put(&code[l], 0);
-                    continue;
+            int listed[ORC_SYMS] = {0};
+            uint32_t vals[ORC_SYMS] = {0};
+            for (int j = 0; j < ORC_SYMS / 2; j++) {
+                uint32_t c2[2];
+                int len[2], real[2];
+                for (int h = 0; h < 2; h++) {
+                    int t = 2 * j + h;
+                    uint64_t row, col;
+                    position(rb, cb, l, t, &row, &col);
+                    real[h] = row < N && col < K;
+                    if (!real[h]) { symbol_code(nr, 0, &c2[h], &len[h]); continue; }
+                    uint32_t s, v, m;
+                    split(elem, e[row * K + col], &s, &v, &m);
+                    vals[t] = v;
+                    symbol_code(nr, rank_of[v], &c2[h], &len[h]);
+                    if (rank_of[v] < 0) listed[t] = 1;
+                    if (elem == ORC_FP8 && fp8_special(v, m)) listed[t] = 1;
                 }
-                uint32_t s, v, m;
-                split(elem, e[row * K + col], &s, &v, &m);
-                int p = rank_of[v];
-                if (p >= 0) {
-                    for (int i = 0; i < p; i++) bw_put(&code[l], 1);
-                    bw_put(&code[l], 0);
-                } else {
-                    for (int i = 0; i < nr; i++) bw_put(&code[l], 1);
-                    esc[n_esc++] = (uint32_t)t | ((uint32_t)l << 7) | ((uint32_t)e[row * K + col] << 12);
+                put_code(&code[l], c2[0], len[0]);
+                if (len[0] + len[1] <= ORC_PEEK) {
+                    put_code(&code[l], c2[1], len[1]);
+                } else {                      /* cut pair: the tail, the second symbol listed */
+                    bw_ones(&code[l], ORC_PEEK - len[0]);
+                    if (real[1]) listed[2 * j + 1] = 1;
                 }
-                bw_put(&code[l], s);
-                if (t % 2 == 0) hw_put_field(&even[l], m, F);
-                else hw_put_field(&odd[l], m, F);
             }
+            for (int t = 0; t < ORC_SYMS; t++)
+                if (listed[t]) esc[n_esc++] = (uint32_t)t | ((uint32_t)l << 7) | (vals[t] << 12);
         }
-        uint64_t code_words = 0, man_words[ORC_LANES];
-        for (int l = 0; l < ORC_LANES; l++) {
-            code_words += ceil_div((uint64_t)code[l].nbits, 32);
-            uint64_t bits = (uint64_t)(even[l].nbits > odd[l].nbits ? even[l].nbits : odd[l].nbits);
-            man_words[l] = ceil_div(ceil_div(bits, 16), 4) * 4;
-        }
-        uint64_t len = pad16(32 + 4 * code_words);
-        for (int l = 0; l < ORC_LANES; l++) len += 4 * man_words[l];
-        uint64_t esc_at = len;
-        len += pad16(4 * n_esc);
+        uint64_t code_words = 0;
+        for (int l = 0; l < ORC_LANES; l++) code_words += ceil_div((uint64_t)code[l].nbits, 32);
+        uint64_t lane_off[ORC_LANES];
+        int full;
+        uint64_t raw_len = raw_section(elem, K, cb, lane_off, &full);
+        uint64_t raw0 = pad16(32 + 4 * code_words);
+        uint64_t esc_at = raw0 + raw_len;
+        uint64_t len = esc_at + pad16(4 * n_esc);
         uint8_t *r = (uint8_t *)calloc(len, 1);
         if (!r) return -2;
         uint64_t pos = 32;
@@ -257,16 +311,21 @@ int orc_encode(const uint16_t *e, const float *scale, uint64_t N, uint64_t K, in
             r[l] = (uint8_t)nw;
             for (uint64_t i = 0; i < nw; i++, pos += 4) put_u32(r + pos, code[l].w[i]);
         }
-        pos = pad16(pos);
-        int uniform = 1;
-        for (int l = 1; l < ORC_LANES; l++) uniform &= man_words[l] == man_words[0];
-        uint64_t man0 = pos;
-        for (int l = 0; l < ORC_LANES; l++) {
-            for (uint64_t k = 0; k < man_words[l]; k++, pos += 4) {
-                uint64_t at = uniform ? man0 + 4 * (k * ORC_LANES + (uint64_t)l) : pos;
-                put_u32(r + at, (uint32_t)even[l].h[k] | ((uint32_t)odd[l].h[k] << 16));
+        for (int l = 0; l < ORC_LANES; l++)
+            for (int t = 0; t < ORC_SYMS; t++) {
+                uint64_t row, col;
+                position(rb, cb, l, t, &row, &col);
+                if (col >= K) continue;                 /* no raw bits past K */
+                uint32_t raw = 0;                       /* rows past N: zero */
+                if (row < N) {
+                    uint32_t s, v, m;
+                    split(elem, e[row * K + col], &s, &v, &m);
+                    raw = raw_of(elem, s, m);
+                }
+                int nib;
+                uint64_t at = raw0 + raw_at(elem, full, l, t / ORC_ROWS, t % ORC_ROWS, lane_off[l], &nib);
+                r[at] |= (uint8_t)(raw << (4 * nib));
             }
-        }
         for (uint64_t i = 0; esc_at + 4 * i < len; i++)
             put_u32(r + esc_at + 4 * i, i < n_esc ? esc[i] : 0xFFFFFFFFu);
         reg[b] = r;
@@ -351,22 +410,21 @@ static uint32_t br_get(bitr *b) {
     return (get_u32(b->p + 4 * word) >> bitpos) & 1;
 }
 
-/* field j of a lane's even (odd = 0) or odd half-stream; the lane's word k is at
-   region + 4 * k * stride */
-static uint32_t half_field(const uint8_t *region, uint64_t stride, int odd, uint64_t j, int F) {
-    uint32_t v = 0;
-    for (int i = 0; i < F; i++) {
-        uint64_t bit = (uint64_t)F * j + (uint64_t)i;
-        uint32_t word = get_u32(region + 4 * (bit / 16) * stride);
-        uint32_t half = odd ? (word >> 16) : (word & 0xFFFF);
-        v |= ((half >> (bit % 16)) & 1u) << i;
+/* One code: counts one-bits up to `limit`; returns the count and whether a zero-bit
+ * ended it (*ended). */
+static int read_ones(bitr *b, int limit, int *ended) {
+    int ones = 0;
+    *ended = 0;
+    while (ones < limit) {
+        if (br_get(b) == 0) { *ended = 1; return ones; }
+        ones++;
     }
-    return v;
+    return ones;
 }
 
 /*
  * Decodes block b into tile[r][c] (8 x 512 element values; fillers left 0).
- * Returns 0, or -1 if a stream or region is malformed.
+ * Returns 0, or -1 if a stream, the raw section or the escape list is malformed.
  */
 static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint16_t tile[ORC_ROWS][ORC_COLS]) {
     uint64_t rb = b / h->CB, cb = b % h->CB;
@@ -380,69 +438,53 @@ static int decode_block(const uint8_t *blob, const orc_hdr *h, uint64_t b, uint1
         lane_code[l] = reg + pos;
         pos += 4 * (uint64_t)reg[l];
     }
-    pos = pad16(pos);
-    int F = man_bits(h->elem);
-    int ok = 0;
-    /* the mantissa regions' sizes follow from the real extents; the escape list follows them */
-    uint64_t man_at = pos, esc_at = pos, mwords[ORC_LANES];
-    for (int l = 0; l < ORC_LANES; l++) {
-        uint64_t n_even = 0, n_odd = 0;
-        for (int t = 0; t < ORC_SYMS; t++) {
-            uint64_t row, col;
-            position(rb, cb, l, t, &row, &col);
-            if (row < h->N && col < h->K) { if (t % 2 == 0) n_even++; else n_odd++; }
-        }
-        uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
-        mwords[l] = ceil_div(ceil_div(bits, 16), 4) * 4;
-        esc_at += 4 * mwords[l];
-    }
-    int uniform = 1;
-    for (int l = 1; l < ORC_LANES; l++) uniform &= mwords[l] == mwords[0];
+    uint64_t raw0 = pad16(pos), lane_off[ORC_LANES];
+    int full;
+    uint64_t esc_at = raw0 + raw_section(h->elem, h->K, cb, lane_off, &full);
     if (start + esc_at > end) return -1;
-    static uint32_t esc_value[ORC_LANES][ORC_SYMS];
+    /* the escape list: entry per (lane, t) */
+    static uint32_t esc_v[ORC_LANES][ORC_SYMS];
     static int esc_seen[ORC_LANES][ORC_SYMS];
     memset(esc_seen, 0, sizeof(esc_seen));
     for (uint64_t at = esc_at; start + at + 4 <= end; at += 4) {
         uint32_t ent = get_u32(reg + at);
         if (ent == 0xFFFFFFFFu) continue;
         int t = (int)(ent & 127u), l = (int)((ent >> 7) & 31u);
-        esc_value[l][t] = ent >> 12;
+        if (esc_seen[l][t] || (ent >> 12) >> exp_bits(h->elem)) return -1;
+        esc_v[l][t] = ent >> 12;
         esc_seen[l][t] = 1;
     }
-    pos = man_at;
+    int ok = 0;
     for (int l = 0; l < ORC_LANES; l++) {
         bitr br = {lane_code[l], reg[l], 0, 0};
-        uint32_t sv[ORC_SYMS], vv[ORC_SYMS];
-        int real[ORC_SYMS], escaped[ORC_SYMS];
-        uint64_t n_even = 0, n_odd = 0;
-        for (int t = 0; t < ORC_SYMS; t++) {
-            uint64_t row, col;
-            position(rb, cb, l, t, &row, &col);
-            real[t] = row < h->N && col < h->K;
-            int ones = 0;
-            while (ones < h->nr && br_get(&br) == 1) ones++;
-            escaped[t] = ones >= h->nr;
-            vv[t] = escaped[t] ? 0 : h->rank_exp[ones];
-            sv[t] = br_get(&br);
-            if (real[t]) { if (t % 2 == 0) n_even++; else n_odd++; }
+        for (int j = 0; j < ORC_SYMS / 2; j++) {
+            int rank[2], ended;
+            int a = read_ones(&br, h->nr, &ended);
+            rank[0] = ended ? a : -1;                    /* -1: escape */
+            int used = ended ? a + 1 : a;
+            int room = ORC_PEEK - used;                  /* bits of the peek left */
+            int lim = room < h->nr ? room : h->nr;
+            int bcount = read_ones(&br, lim, &ended);
+            if (ended) rank[1] = bcount;
+            else rank[1] = -1;                           /* an escape, or the tail of a cut pair */
+            for (int q = 0; q < 2; q++) {
+                int t = 2 * j + q;
+                uint64_t row, col;
+                position(rb, cb, l, t, &row, &col);
+                if (row >= h->N || col >= h->K) continue;
+                uint32_t v;
+                if (esc_seen[l][t]) v = esc_v[l][t];
+                else if (rank[q] >= 0) v = h->rank_exp[rank[q]];
+                else return -1;                          /* escaped but not listed */
+                int nib;
+                uint64_t at = raw0 + raw_at(h->elem, full, l, t / ORC_ROWS, t % ORC_ROWS, lane_off[l], &nib);
+                uint32_t raw = (reg[at] >> (4 * nib)) & (h->elem == ORC_BF16 ? 0xFFu : 0xFu);
+                uint32_t s = h->elem == ORC_BF16 ? raw >> 7 : raw >> 3;
+                uint32_t m = h->elem == ORC_BF16 ? raw & 0x7F : raw & 7;
+                tile[t % ORC_ROWS][l * ORC_LANE_COLS + t / ORC_ROWS] = (uint16_t)join(h->elem, s, v, m);
+            }
         }
         if (br.bad) ok = -1;
-        uint64_t bits = (uint64_t)F * (n_even > n_odd ? n_even : n_odd);
-        uint64_t words = ceil_div(ceil_div(bits, 16), 4) * 4;
-        const uint8_t *man = uniform ? reg + man_at + 4 * (uint64_t)l : reg + pos;
-        uint64_t stride = uniform ? ORC_LANES : 1;
-        uint64_t je = 0, jo = 0;
-        for (int t = 0; t < ORC_SYMS; t++) {
-            if (!real[t]) continue;
-            uint32_t m = (t % 2 == 0) ? half_field(man, stride, 0, je++, F) : half_field(man, stride, 1, jo++, F);
-            uint32_t value = join(h->elem, sv[t], vv[t], m);
-            if (escaped[t]) {
-                if (!esc_seen[l][t]) return -1;
-                value = esc_value[l][t];
-            }
-            tile[t % ORC_ROWS][l * ORC_LANE_COLS + t / ORC_ROWS] = (uint16_t)value;
-        }
-        pos += 4 * words;
     }
     return ok;
 }

@@ -18,13 +18,13 @@ def region_bounds(blob, i):
 
 def replace_code_streams(blob, i, lane_words, word=0xFFFFFFFF):
     """The blob with block i's code streams replaced: lane l gets lane_words[l] copies of `word`
-    (each count at most 48, so host validation still accepts the region); the block's mantissa
-    regions and escape list are kept, and the block table and total size follow the new size."""
-    assert len(lane_words) == 32 and all(0 <= w <= 48 for w in lane_words)
+    (each count at most 26, so host validation still accepts the region); the block's raw
+    section and escape list are kept, and the block table and total size follow the new size."""
+    assert len(lane_words) == 32 and all(0 <= w <= 26 for w in lane_words)
     a = bytearray(blob)
     start, end = region_bounds(blob, i)
     old_codes = 4 * sum(a[start:start + 32])
-    tail = bytes(a[start + ((32 + old_codes + 15) // 16) * 16:end])  # mantissas + escape list
+    tail = bytes(a[start + ((32 + old_codes + 15) // 16) * 16:end])  # raw section + escape list
     codes = np.full(sum(lane_words), word, np.uint32).astype("<u4").tobytes()
     head = bytes(lane_words) + codes
     head += b"\0" * (-len(head) % 16)

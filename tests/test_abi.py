@@ -61,17 +61,20 @@ def test_bind_geometry_and_workspace():
 
 def _esc_list(blob, i, n, k):
     """(byte offset, u32 words) of the escape list of block i (BF16, n x k matrix, one
-    column block): after the code streams and the closed-form mantissa regions."""
+    column block): after the code streams and the closed-form raw section (4096 bytes for a
+    block of 512 real columns, else each lane's real columns at 8 bytes, padded to 16)."""
     b = np.frombuffer(bytes(blob), np.uint8)
     nb = int(b[24:32].view(np.uint64)[0])
     off_data = int(b[48:56].view(np.uint64)[0])
     tab = b[80:80 + 4 * (nb + 1)].view(np.uint32)
     start, end = off_data + 16 * int(tab[i]), off_data + 16 * int(tab[i + 1])
     at = start + -(-(32 + 4 * int(b[start:start + 32].astype(np.int64).sum())) // 16) * 16
-    rows = min(8, n - 8 * i)
-    for lane in range(32):
-        cols = max(0, min(16, k - 16 * lane))
-        at += 4 * (-(-(-(-7 * cols * ((rows + 1) // 2) // 16)) // 4) * 4)
+    if k >= 512:
+        at += 4096
+    else:
+        for lane in range(32):
+            cols = max(0, min(16, k - 16 * lane))
+            at += -(-8 * cols // 16) * 16
     return at, b[at:end].view(np.uint32)
 
 
@@ -87,12 +90,14 @@ def test_validate_rejects_corruption():
         return nwc.validate(bytes(b))
     assert bad(lambda b: b.__setitem__(0, 0)) == 2           # magic
     assert bad(lambda b: b.__setitem__(4, 1)) == 2           # format version
-    assert bad(lambda b: b.__setitem__(7, 12)) == 2          # n_ranked > 11
+    assert bad(lambda b: b.__setitem__(7, 13)) == 2          # n_ranked > 12
     assert bad(lambda b: b.__setitem__(64 + 1, b[64])) == 2  # duplicate ranked exponent
     assert nwc.validate(bytes(blob[:-16])) == 2              # truncated
     off_data = int(np.frombuffer(bytes(blob[48:56]), np.uint64)[0])
-    assert bad(lambda b: b.__setitem__(off_data, b[off_data] + 4)) == 2  # lane word count (beyond padding)
-    assert bad(lambda b: b.__setitem__(off_data + 3, 200)) == 2           # > 48 words
+    def all_lanes_26(b):  # code streams that no longer leave room for the raw section
+        b[off_data:off_data + 32] = bytes([26] * 32)
+    assert bad(all_lanes_26) == 2
+    assert bad(lambda b: b.__setitem__(off_data + 3, 27)) == 2            # > 26 words (64 pairs x 13 bits)
     assert nwc.validate(bytes(blob) + b"\0" * 16) == 2       # trailing bytes
 
 
@@ -112,9 +117,7 @@ def test_validate_checks_escape_lists():
     e0 = int(words[0])
     assert with_word(at, e0 | 0xFFF) == 2                      # lane 31, t 127: out of order
     assert with_word(at, 0xFFFFFFFF) == 2                      # padding before an entry
-    ranked_exp = blob[64]
-    assert with_word(at, (e0 & 0xFFF) | (ranked_exp << 7) << 12) == 2  # ranked exponent listed
-    assert with_word(at, (e0 & 0xFFF) | (1 << 16) << 12) == 2          # bits wider than BF16
+    assert with_word(at, (e0 & 0xFFF) | (256 << 12)) == 2      # exponent field wider than BF16's 8 bits
     assert with_word(at + 4, e0) == 2                          # repeated entry
     if n_pad > 0:  # an entry after the last one that is out of order
         assert with_word(at + 4 * len(entries), e0) == 2
@@ -250,14 +253,14 @@ def test_code_bit_flips_pass_validation_and_the_oracle_never_crashes(elem):
 
 
 def test_inflated_code_streams_pass_validation_and_the_oracle_rejects_them():
-    """A block region whose lane streams are rewritten to the 48-word maximum (all ones, so every
-    code is 12 bits long) with one short last lane: structurally valid, so host validation takes
-    it and only decoding can tell; the oracle rejects it."""
+    """A block region whose lane streams are rewritten to the 26-word maximum (all ones, so every
+    row pair is a 13-bit escape) with one short last lane: structurally valid, so host validation
+    takes it and only decoding can tell; the oracle rejects it (escapes the list does not hold)."""
     import blob_edit
     from oracle import decode as oracle_decode
     w = synth.normal_bf16((64, 513), 0.02, seed=5)
     blob = nwc.encode(w)
-    bad = blob_edit.replace_code_streams(blob, 3, [48] * 31 + [8])
+    bad = blob_edit.replace_code_streams(blob, 3, [26] * 31 + [8])
     start, end = blob_edit.region_bounds(bad, 3)
     assert end - start <= 6144  # still fits a decoder's shared-memory stage
     assert nwc.validate(bad) == 0

@@ -136,8 +136,8 @@ def test_escape_list_mismatch_is_flagged_not_faulted():
     tab = b[80:80 + 4 * 9].view(np.uint32)
     for i in range(8):
         start, end = off_data + 16 * int(tab[i]), off_data + 16 * int(tab[i + 1])
-        # escape list: after the code streams and 32 full mantissa regions of 28 words
-        at = start + -(-(32 + 4 * int(b[start:start + 32].astype(np.int64).sum())) // 16) * 16 + 32 * 28 * 4
+        # escape list: after the code streams and the 4096-byte raw section of a full block
+        at = start + -(-(32 + 4 * int(b[start:start + 32].astype(np.int64).sum())) // 16) * 16 + 4096
         words = b[at:end].view(np.uint32)
         n_entries = int((words != 0xFFFFFFFF).sum())
         if n_entries >= 1 and len(words) - n_entries < 3:
@@ -149,6 +149,25 @@ def test_escape_list_mismatch_is_flagged_not_faulted():
     nwc.Matrix(bytes(blob)).decode()
     st, flags = nwc.check()
     assert st == 5 and flags & 1
+
+
+@pytest.mark.parametrize("elem", [0, 1])
+def test_table_built_in_kernel_equals_copied_table(elem):
+    """A bound matrix without a device decode table (every kernel builds it in shared memory)
+    gives bit for bit the same decode and GEMV as one whose table was copied in."""
+    w = synth.normal_bf16((200, 1300), 0.02, seed=17 + elem)
+    blob = nwc.encode(w, elem=elem)
+    a, b = nwc.Matrix(blob), nwc.Matrix(blob, table=False)
+    assert a.table is not None and b.table is None
+    da, db = a.decode(), b.decode()
+    if elem == 1:
+        assert torch.equal(da[0], db[0]) and torch.equal(da[1], db[1])
+    else:
+        assert torch.equal(da, db)
+    x = dev_bits(synth.activations_bf16(1300, 18))
+    assert torch.equal(a.gemv(x), b.gemv(x))
+    assert_clean()
+    gemv_check(blob, synth.activations_bf16(1300, 18), mat=b)
 
 
 def test_matmul_batch_via_decode_and_cublas():
@@ -613,12 +632,11 @@ def test_infinite_rank0_exponent_keeps_fillers_out_of_real_rows():
 
 
 def test_inflated_code_streams_in_the_last_stage_are_flagged_not_faulted():
-    """Blocks of a ragged K whose lane streams are rewritten to the 48-word maximum with a short
-    last lane (valid to the host, every code 12 bits long), placed where the last warp of each
-    CTA stages them (GEMV: warp 31, decode: warp 15): the last lane's decoder reads past its words
-    up to the end of the stage and beyond it into the slack that follows the last stage. Every
-    kernel finishes, the device error word reports the malformed blocks, and the context stays
-    usable."""
+    """Blocks of a ragged K whose lane streams are rewritten to the 26-word maximum with a short
+    last lane (valid to the host, every row pair a 13-bit escape), placed where the last warp of
+    each CTA stages them (GEMV: warp 31, decode: warp 15): the lanes' decoders read their longest
+    possible streams and the last lane reads past its words. Every kernel finishes, the device
+    error word reports the malformed blocks, and the context stays usable."""
     import blob_edit
     sms = nwc.sm_count()
     n, k = 8 * 2400, 513  # two column blocks; block 2 rb + 1 is the ragged one
@@ -628,7 +646,7 @@ def test_inflated_code_streams_in_the_last_stage_are_flagged_not_faulted():
     bad = blob
     for b in targets:
         assert b < 2 * (n // 8) and b % 2 == 1
-        bad = blob_edit.replace_code_streams(bad, b, [48] * 31 + [8])
+        bad = blob_edit.replace_code_streams(bad, b, [26] * 31 + [8])
         start, end = blob_edit.region_bounds(bad, b)
         assert end - start <= 6144
     assert nwc.validate(bad) == 0
