@@ -68,6 +68,7 @@ def lib():
     L.nwc_gemv_workspace_bytes.restype = sz
     L.nwc_gemv_prepare.argtypes = [ctypes.POINTER(NwcMatrix), p, sz, p]
     L.nwc_gemv.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, p]
+    L.nwc_gemv_next.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p, sz, ctypes.POINTER(NwcMatrix), p]
     L.nwc_gemv_noalloc.argtypes = [ctypes.POINTER(NwcMatrix), p, p, p]
     L.nwc_gemv_batch_workspace_bytes.argtypes = [ctypes.POINTER(NwcMatrix), i32]
     L.nwc_gemv_batch_workspace_bytes.restype = sz
@@ -79,7 +80,7 @@ def lib():
     L.nwc_sm_count.restype = i32
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
                  "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gemv_batch_prepare",
-                 "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table"):
+                 "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table", "nwc_gemv_next"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -205,15 +206,21 @@ class Matrix:
         _ok(lib().nwc_gemv_prepare(ctypes.byref(self.m), ctypes.c_void_p(self.workspace.data_ptr()), ws,
                                    _stream_ptr(None)), "nwc_gemv_prepare")
 
-    def gemv(self, x, y=None, stream=None):
-        """y (float32[N]) = W x for x a BF16 vector given as an int16/bfloat16 CUDA tensor."""
+    def gemv(self, x, y=None, stream=None, next=None):
+        """y (float32[N]) = W x for x a BF16 vector given as an int16/bfloat16 CUDA tensor. next: the
+        Matrix multiplied after this one, whose weights this call brings into L2 (nwc_gemv_next)."""
         import torch
         assert x.numel() == self.k and x.is_cuda and x.is_contiguous()
         if y is None:
             y = torch.empty(self.n, dtype=torch.float32, device=x.device)
-        _ok(lib().nwc_gemv(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
-                           ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes,
-                           _stream_ptr(stream)), "nwc_gemv")
+        if next is None:
+            _ok(lib().nwc_gemv(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+                               ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes,
+                               _stream_ptr(stream)), "nwc_gemv")
+        else:
+            _ok(lib().nwc_gemv_next(ctypes.byref(self.m), ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(y.data_ptr()),
+                                    ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes, ctypes.byref(next.m),
+                                    _stream_ptr(stream)), "nwc_gemv_next")
         return y
 
     def gemv_batch(self, x, y=None, stream=None):

@@ -446,33 +446,46 @@ __device__ __forceinline__ void finish_rows(const Mat &m, const float (&sum)[NB]
     for (int v = 0; v < NB; v++) {
         float s = 0.0f;
         if (live) {
-            for (uint64_t c2 = c0, q = 0; c2 < m.cbs; c2 += 4, q++) {
-                float val;
-                if (c2 == cb) {
-                    val = own[v];
-                } else {
-                    float *slot = partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2;
-                    uint32_t bits = kSentinel;
+            // slots c0 + 4q in a fixed order: the first kSpec from the loads above, the rest
+            // (more than 16 column blocks) kSpec at a time with their loads in flight together;
+            // a slot still holding the sentinel is loaded again (bounded)
+            for (uint64_t q0 = 0; c0 + 4 * q0 < m.cbs; q0 += kSpec) {
+                uint32_t bits[kSpec];
 #pragma unroll
-                    for (int qq = 0; qq < kSpec; qq++)
-                        if ((uint64_t)qq == q) bits = pv[v][qq];
-                    while (bits == kSentinel) {
-                        bits = ld_relaxed(slot);
-                        if (bits == kSentinel && clock64() - t0 > (1ll << 32)) {
+                for (int qq = 0; qq < kSpec; qq++) {
+                    const uint64_t c2 = c0 + 4 * (q0 + qq);
+                    bits[qq] = q0 == 0 ? pv[v][qq] : kSentinel;
+                    if (q0 != 0 && c2 < m.cbs && c2 != cb) bits[qq] = ld_relaxed(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
+                }
+#pragma unroll
+                for (int qq = 0; qq < kSpec; qq++) {
+                    const uint64_t c2 = c0 + 4 * (q0 + qq);
+                    if (c2 >= m.cbs) break;
+                    if (c2 == cb) {
+                        s += own[v];
+                        continue;
+                    }
+                    while (bits[qq] == kSentinel) {
+                        bits[qq] = ld_relaxed(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
+                        if (bits[qq] == kSentinel && clock64() - t0 > (1ll << 32)) {
                             timed_out = true;
-                            bits = 0u;
+                            bits[qq] = 0u;
                         }
                     }
-                    val = __uint_as_float(bits);
-                    st_relaxed(slot, kSentinel);
+                    s += __uint_as_float(bits[qq]);
                 }
-                s += val;
             }
         }
         s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
         s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
         if (lane < kRows && live) y[v * ld_y + (int64_t)r2] = ELEM == 0 ? s : s * m.scales[r2];
     }
+    // every slot read goes back to the sentinel (the warp's own slot below, after its writer)
+#pragma unroll
+    for (int v = 0; v < NB; v++)
+        if (live)
+            for (uint64_t c2 = c0; c2 < m.cbs; c2 += 4)
+                if (c2 != cb) st_relaxed(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2, kSentinel);
     // the warp's own slots: written by the writer lanes above, reset here after them
     __syncwarp();
 #pragma unroll
@@ -616,16 +629,15 @@ __device__ __forceinline__ void esc_correct(uint32_t list0, uint32_t raw0, const
 }
 
 // Block from its staged region (shared address `stage`, `bytes` long) for NB vectors (vector v
-// at xb + v ld_x from the block's first column). EDGE: the block's real columns kc < 512 (the
+// at xb + v ld_x from the block's first column; xs = the lane's 16 activations of each, loaded
+// by the caller while the region lands, zero past K). EDGE: the block's real columns kc < 512 (the
 // lanes' raw regions follow one another; columns past K give 0). rows = the block's real rows:
 // rows past N decode to finite fillers whose sums are never stored.
 template <int ELEM, int NB, bool EDGE>
 __device__ __forceinline__ void gemv_block(uint32_t stage, uint32_t bytes, int lane, uint32_t lutb, const uint16_t *xb,
-                                           int64_t ld_x, float (&acc)[NB][8], bool &bad, int kc, int rows) {
+                                           int64_t ld_x, const uint32_t (&xs)[NB][8], float (&acc)[NB][8], bool &bad,
+                                           int kc, int rows) {
     const LaneBlock lb = lane_block<ELEM, EDGE>(stage, lane, kc);
-    uint32_t xs[NB][8];
-#pragma unroll
-    for (int v = 0; v < NB; v++) load_x16(xb + v * ld_x + kLaneCols * lane, EDGE ? lb.cols : kLaneCols, xs[v]);
     Fs s;
     fs_init(s, lb.code, lb.lw);
 #pragma unroll
@@ -654,7 +666,7 @@ __device__ __forceinline__ void gemv_block(uint32_t stage, uint32_t bytes, int l
 // arithmetic, one row pair at a time, every word read bounded by the lane's own words (zeros
 // past them) and every raw read by the region.
 template <int ELEM, int NB>
-__device__ __noinline__ void gemv_block_global(const uint8_t *reg, uint32_t bytes, int lane, uint32_t lutb,
+__device__ __forceinline__ void gemv_block_global(const uint8_t *reg, uint32_t bytes, int lane, uint32_t lutb,
                                                const uint16_t *xb, int64_t ld_x, float (&acc)[NB][8], bool &bad, int kc,
                                                int rows) {
     const uint32_t lw = reg[lane];
@@ -728,10 +740,40 @@ __device__ __noinline__ void gemv_block_global(const uint8_t *reg, uint32_t byte
 // partial sums at partial + v col_blocks n_pad). KR: K % 512 != 0, and the last column block's
 // blocks take the fast decoder with the ragged raw layout, in a kernel of its own so that the
 // others keep their registers.
+// The matrix multiplied after this one, whose bytes this kernel brings into L2 once its own
+// first regions have landed (its decode phase leaves HBM idle): the block regions, the block
+// table and the decode table. bytes == 0: nothing to prefetch.
+struct Prefetch {
+    const uint8_t *data;
+    uint64_t bytes;
+    const uint32_t *tab;
+    uint64_t tab_bytes;
+    const uint32_t *table;
+};
+
+// This warp's share of the prefetch: the regions split evenly (16-byte pieces) over the `ways`
+// warps that have a block; warp 0 also takes the block table and the decode table.
+__device__ __forceinline__ void prefetch_share(const Prefetch &pf, uint64_t w, uint64_t ways) {
+    if (pf.bytes == 0 || w >= ways) return;
+    const uint64_t units = pf.bytes / 16, per = (units + ways - 1) / ways;
+    const uint64_t u0 = w * per, u1 = u0 + per < units ? u0 + per : units;
+    // one bulk prefetch per 64 KB at most
+    for (uint64_t u = u0; u < u1; u += 4096) {
+        const uint64_t n = u1 - u < 4096 ? u1 - u : 4096;
+        l2_prefetch(pf.data + 16 * u, (uint32_t)(16 * n));
+    }
+    if (w == 0) {
+        for (uint64_t o = 0; o < pf.tab_bytes; o += 65536)
+            l2_prefetch(reinterpret_cast<const uint8_t *>(pf.tab) + o,
+                        (uint32_t)(pf.tab_bytes - o < 65536 ? pf.tab_bytes - o : 65536));
+        if (pf.table) l2_prefetch(pf.table, kLutBytes);
+    }
+}
+
 template <int ELEM, int NB, bool KR = false>
 __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     gemv_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, float *__restrict__ y, int64_t ld_y,
-                float *partial, uint32_t *counters, uint64_t n_pad) {
+                float *partial, uint32_t *counters, uint64_t n_pad, Prefetch pf) {
     using C = GemvCfg<NB>;
     using S = Smem<C::kWarps>;
     // A kernel launched after this one with programmatic stream serialization may start as soon
@@ -748,28 +790,28 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     uint32_t phase = 0;
     bool bad = false, timed_out = false, inflight = false;
 
-    // Region bounds of block bb, read by lane 0 and broadcast.
-    auto region = [&](uint64_t bb, const uint8_t *&ptr, uint32_t &bytes) {
-        uint32_t s0 = 0, s1 = 0;
-        if (lane == 0) {
-            s0 = m.tab[bb];
-            s1 = m.tab[bb + 1];
-        }
-        s0 = __shfl_sync(0xFFFFFFFFu, s0, 0);
-        s1 = __shfl_sync(0xFFFFFFFFu, s1, 0);
-        ptr = m.data + 16 * (uint64_t)s0;
-        bytes = 16 * (s1 - s0);
-    };
+    // Block bounds (16-byte units from the data section) travel with the warp: c0/c1 of block b
+    // in every lane; n0/n1 of the warp's next block in lane 0, read one iteration ahead, so that
+    // no read of the block table sits on the decode path.
+    uint32_t c0 = 0, c1 = 0, n0 = 0, n1 = 0;
+    if (lane == 0 && b < m.nb) {
+        c0 = m.tab[b];
+        c1 = m.tab[b + 1];
+    }
+    if (lane == 0 && b + total_warps < m.nb) {
+        n0 = m.tab[b + total_warps];
+        n1 = m.tab[b + total_warps + 1];
+    }
+    c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
+    c1 = __shfl_sync(0xFFFFFFFFu, c1, 0);
     // reuse = the stage held an earlier region that this warp read through the generic proxy
-    auto issue = [&](uint64_t bb, bool reuse) {
-        const uint8_t *src;
-        uint32_t bytes;
-        region(bb, src, bytes);
+    auto issue = [&](uint32_t s0, uint32_t s1, bool reuse) {
+        const uint32_t bytes = 16 * (s1 - s0);
         if (bytes <= (uint32_t)kStageBytes) {
             if (lane == 0) {
                 if (reuse) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_expect_tx(bar, bytes);
-                tma_load_1d(stage, src, bytes, bar);
+                tma_load_1d(stage, m.data + 16 * (uint64_t)s0, bytes, bar);
             }
             inflight = true;
         }
@@ -782,7 +824,7 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    if (b < m.nb) issue(b, false);
+    if (b < m.nb) issue(c0, c1, false);
     lut_start(m, smem, lut_bar);
     __syncthreads();
     if (!lut_ready(m, lut_bar)) timed_out = true;
@@ -790,15 +832,21 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     // the kernel before this one on the stream: wait for it to complete.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t lutb = smem_u32(smem);
+    const uint64_t w_id = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;  // = the warp's first block
+    const uint64_t ways = m.nb < total_warps ? m.nb : total_warps;
+    bool prefetched = false;
     while (b < m.nb && !timed_out) {
-        const uint64_t nxt = b + total_warps;
-        if (nxt < m.nb && lane == 0) {
-            const uint32_t s0 = m.tab[nxt], s1 = m.tab[nxt + 1];
-            l2_prefetch(m.data + 16 * (uint64_t)s0, 16 * (s1 - s0));
+        const uint64_t nxt = b + total_warps, nn = nxt + total_warps;
+        uint32_t f0 = 0, f1 = 0;  // bounds of block nn, for the next iteration
+        if (lane == 0) {
+            if (nn < m.nb) {
+                f0 = m.tab[nn];
+                f1 = m.tab[nn + 1];
+            }
+            if (nxt < m.nb) l2_prefetch(m.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
         }
-        const uint8_t *src;
-        uint32_t bytes;
-        region(b, src, bytes);
+        const uint32_t bytes = 16 * (c1 - c0);
+        const uint8_t *src = m.data + 16 * (uint64_t)c0;
         const uint64_t rb = b / m.cbs, cb = b % m.cbs;
         const int rows = real_rows(m.n, rb);
         const uint64_t kc64 = m.k - cb * kCols;
@@ -810,15 +858,24 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
 #pragma unroll
             for (int r = 0; r < 8; r++) acc[v][r] = 0.0f;
         if (bytes <= (uint32_t)kStageBytes) {
+            // the lane's activations, loaded while the region lands
+            uint32_t xs[NB][8];
+            const int cl = kc - kLaneCols * lane, cols = cl < 0 ? 0 : (cl > kLaneCols ? kLaneCols : cl);
+#pragma unroll
+            for (int v = 0; v < NB; v++) load_x16(xb + v * ld_x + kLaneCols * lane, cols, xs[v]);
             if (!mbar_wait(bar, phase & 1u)) {
                 timed_out = true;
                 break;
             }
             inflight = false;
             phase ^= 1u;
-            if (KR && kc < kCols) gemv_block<ELEM, NB, KR>(stage, bytes, lane, lutb, xb, ld_x, acc, bad, kc, rows);
-            else gemv_block<ELEM, NB, false>(stage, bytes, lane, lutb, xb, ld_x, acc, bad, kCols, rows);
+            if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
+            prefetched = true;
+            if (KR && kc < kCols) gemv_block<ELEM, NB, KR>(stage, bytes, lane, lutb, xb, ld_x, xs, acc, bad, kc, rows);
+            else gemv_block<ELEM, NB, false>(stage, bytes, lane, lutb, xb, ld_x, xs, acc, bad, kCols, rows);
         } else {
+            if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
+            prefetched = true;
             gemv_block_global<ELEM, NB>(src, bytes, lane, lutb, xb, ld_x, acc, bad, kc, rows);
         }
         float sum[NB];
@@ -826,7 +883,11 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
         for (int v = 0; v < NB; v++) sum[v] = transpose_reduce(acc[v], lane);
         finish_rows<ELEM, NB>(m, sum, lane, rb, cb, y, ld_y, partial, counters, n_pad, timed_out);
         __syncwarp();
-        if (nxt < m.nb) issue(nxt, true);
+        c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
+        c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
+        if (nxt < m.nb) issue(c0, c1, true);
+        n0 = f0;
+        n1 = f1;
         b = nxt;
     }
     if (timed_out) {
@@ -1144,19 +1205,34 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
             if (ticket == (uint32_t)m.cbs - 1) {
                 __syncwarp();
                 // (vector, row) pairs i, vector i / 8, row i % 8, summed over the column blocks in a
-                // fixed order; each slot read is put back to the sentinel that the single- and
+                // fixed order, every pair's loads of a round in flight together (4 pairs a lane at
+                // 16 vectors); then each slot read goes back to the sentinel that the single- and
                 // two-vector kernel expect of a prepared workspace.
-                for (int i0 = 0; i0 < nb * kRows; i0 += 32) {
-                    const int i = i0 + lane, v = i >> 3;
+                constexpr int PL = kBatchMax * kRows / 32;
+                float sv[PL];
+                bool live[PL];
+                float *pp[PL];
+#pragma unroll
+                for (int k2 = 0; k2 < PL; k2++) {
+                    const int i = lane + 32 * k2, v = i >> 3;
                     const uint64_t r2 = rb * kRows + (uint64_t)(i & 7);
-                    if (v >= nb || r2 >= m.n) continue;
-                    float *pp = partial + (uint64_t)v * m.cbs * n_pad + r2;
-                    float sv = 0.0f;
-                    for (uint64_t c2 = 0; c2 < m.cbs; c2++) {
-                        sv += __ldcg(pp + c2 * n_pad);
-                        st_relaxed(pp + c2 * n_pad, kSentinel);
-                    }
-                    y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv : sv * m.scales[r2];
+                    live[k2] = v < nb && r2 < m.n;
+                    pp[k2] = partial + (uint64_t)(live[k2] ? v : 0) * m.cbs * n_pad + r2;
+                    sv[k2] = 0.0f;
+                }
+#pragma unroll 4
+                for (uint64_t c2 = 0; c2 < m.cbs; c2++) {
+#pragma unroll
+                    for (int k2 = 0; k2 < PL; k2++)
+                        if (live[k2]) sv[k2] += __ldcg(pp[k2] + c2 * n_pad);
+                }
+#pragma unroll
+                for (int k2 = 0; k2 < PL; k2++) {
+                    if (!live[k2]) continue;
+                    const int i = lane + 32 * k2, v = i >> 3;
+                    const uint64_t r2 = rb * kRows + (uint64_t)(i & 7);
+                    y[(int64_t)v * ld_y + (int64_t)r2] = ELEM == 0 ? sv[k2] : sv[k2] * m.scales[r2];
+                    for (uint64_t c2 = 0; c2 < m.cbs; c2++) __stcg(pp[k2] + c2 * n_pad, __uint_as_float(kSentinel));
                 }
                 if (lane == 0) counters[rb] = 0;
             }
@@ -1374,9 +1450,9 @@ __device__ __forceinline__ void unpack_fast(uint32_t stage, uint32_t bytes, int 
 // Any block read in place from global memory (a region too large for a stage), element by
 // element: every word read bounded by the lane's own words, every raw read by the region.
 template <int ELEM, int MODE>
-__device__ __noinline__ void unpack_global(const uint8_t *reg, uint32_t bytes, int lane, uint32_t lutb, void *out,
-                                           int64_t ld_out, uint64_t row0, uint64_t colb, int want, bool &bad, int kc,
-                                           int rows) {
+__device__ __noinline__ bool unpack_global(const uint8_t *reg, uint32_t bytes, int lane, uint32_t lutb, void *out,
+                                           int64_t ld_out, uint64_t row0, uint64_t colb, int want, int kc, int rows) {
+    bool bad = false;
     const uint32_t lw = reg[lane];
     uint32_t incl = lw;
 #pragma unroll
@@ -1388,10 +1464,7 @@ __device__ __noinline__ void unpack_global(const uint8_t *reg, uint32_t bytes, i
     const uint32_t *code = reinterpret_cast<const uint32_t *>(reg + 32) + (incl - lw);
     const uint32_t raw0 = (uint32_t)up16(32u + 4u * total);
     const uint32_t list0 = raw0 + raw_bytes<ELEM>(kc);
-    if (list0 > bytes) {
-        bad = true;
-        return;
-    }
+    if (list0 > bytes) return true;
     const int cl = kc - kLaneCols * lane, cols = cl < 0 ? 0 : (cl > kLaneCols ? kLaneCols : cl);
     const uint64_t col0 = colb + (uint64_t)(kLaneCols * lane);
     uint64_t win = 0;
@@ -1436,6 +1509,7 @@ __device__ __noinline__ void unpack_global(const uint8_t *reg, uint32_t bytes, i
     __syncwarp();
     unpack_patch<ELEM>(0u, 0u, reinterpret_cast<const uint32_t *>(reg + list0), reg + raw0, (bytes - list0) / 4u, lane,
                        nesc, kc, rows, MODE == 0 ? -1 : want, out, ld_out, row0, colb, bad);
+    return bad;
 }
 
 // Decode: 16 warps per SM with up to 128 registers each, so that a lane holds its whole 8x16
@@ -1569,7 +1643,7 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
                     unpack_fast<ELEM, MODE, false>(stage, bytes, lane, lutb, out, ld_out, orow, colb, want, vec, bad, kCols,
                                                    rows);
             } else {
-                unpack_global<ELEM, MODE>(src, bytes, lane, lutb, out, ld_out, orow, colb, want, bad, kc, rows);
+                bad |= unpack_global<ELEM, MODE>(src, bytes, lane, lutb, out, ld_out, orow, colb, want, kc, rows);
             }
         }
         __syncwarp();
@@ -1756,45 +1830,58 @@ extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws
 namespace {
 template <int ELEM, int NB>
 cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, float *partial,
-                           uint32_t *counters, uint64_t n_pad, int sms, cudaStream_t stream) {
+                           uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int sms, cudaStream_t stream) {
     using C = GemvCfg<NB>;
     const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
     if (k_ragged(m)) {
         if (!smem_ready<gemv_kernel<ELEM, NB, true>>(C::kSmem)) return cudaErrorInvalidConfiguration;
         return launch_pdl(gemv_kernel<ELEM, NB, true>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y,
-                          partial, counters, n_pad);
+                          partial, counters, n_pad, pf);
     }
     if (!smem_ready<gemv_kernel<ELEM, NB, false>>(C::kSmem)) return cudaErrorInvalidConfiguration;
     return launch_pdl(gemv_kernel<ELEM, NB, false>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y, partial,
-                      counters, n_pad);
+                      counters, n_pad, pf);
 }
 
 // The GEMV for nb = 1 or 2 vectors on `partial` (nb x col_blocks x n_pad floats, sentinels) and
-// `counters` (row_blocks, zero); arguments already checked.
+// `counters` (row_blocks, zero); arguments already checked. next: the matrix to prefetch, or null.
 nwc_status launch_gemv(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, int nb, float *partial,
-                       uint32_t *counters, uint64_t n_pad, cudaStream_t stream) {
+                       uint32_t *counters, uint64_t n_pad, cudaStream_t stream, const nwc_matrix *next = nullptr) {
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
+    Prefetch pf = {nullptr, 0, nullptr, 0, nullptr};
+    if (next && next->data && next->block_tab) {
+        pf.data = next->data;
+        pf.bytes = next->data_bytes & ~uint64_t(15);
+        pf.tab = next->block_tab;
+        pf.tab_bytes = up16(4 * ((uint64_t)next->row_blocks * (uint64_t)next->col_blocks + 1)) & ~uint64_t(15);
+        pf.table = next->table;
+    }
     cudaError_t rc;
     if (nb == 1)
-        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream)
-                                     : launch_gemv_nb<1, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream);
+        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream)
+                                     : launch_gemv_nb<1, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream);
     else
-        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream)
-                                     : launch_gemv_nb<1, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, sms, stream);
+        rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream)
+                                     : launch_gemv_nb<1, 2>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream);
     return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 }  // namespace
 
-extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
-                               nwc_stream stream) {
+extern "C" nwc_status nwc_gemv_next(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                                    const nwc_matrix *next, nwc_stream stream) {
     if (!mp || !x || !y || !ws) return NWC_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(ws) & 15)) return NWC_ERR_INVALID_ARG;
     if (ws_bytes < nwc_gemv_workspace_bytes(mp)) return NWC_ERR_INVALID_ARG;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     return launch_gemv(to_mat(*mp), x, 0, y, 0, 1, reinterpret_cast<float *>(w8),
                        reinterpret_cast<uint32_t *>(w8 + ws_counter_off(*mp)), pad_rows(*mp),
-                       reinterpret_cast<cudaStream_t>(stream));
+                       reinterpret_cast<cudaStream_t>(stream), next);
+}
+
+extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                               nwc_stream stream) {
+    return nwc_gemv_next(mp, x, y, ws, ws_bytes, nullptr, stream);
 }
 
 // ---------------------------------------------------------------- small-batch GEMV

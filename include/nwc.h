@@ -4,13 +4,17 @@
  *
  * What the calls compute is defined by two pages:
  *   "NWC -- Neural Weight Compression" (PyPI project page, v0.9.0), section "How it works":
- *     a BF16 weight splits into a raw mantissa plane and an entropy-coded exponent/sign part;
- *     the exponent is ranked by frequency and written as a unary rank code plus a raw sign
- *     bit, with an escape for rare values (in this format the escape code is n_ranked ones
- *     and the sign, and the escaped element's bits sit in a per-block escape list after the
- *     mantissa regions); lanes decode their own bit streams over blocks of
- *     8 rows x 512 columns inside the matrix-vector kernel; dequantization and the embedding
- *     lookup run on the same decoder; any shape works (2 bits per filler, no mantissa).
+ *     a BF16 weight splits into a raw part and an entropy-coded exponent; the exponent is ranked
+ *     by frequency and written as a unary rank code plus a raw sign bit, with an escape for rare
+ *     values; a peek into a shared-memory table yields up to two complete codes; lanes decode
+ *     their own bit streams over blocks of 8 rows x 512 columns inside the matrix-vector kernel;
+ *     dequantization and the embedding lookup run on the same decoder; any shape works (fillers
+ *     cost a short code and no mantissa).
+ *     In this format (version 4) the sign sits beside the 7 raw mantissa bits (a byte per
+ *     element), the coded stream holds only the unary rank codes, written by row pairs so that
+ *     one 13-bit peek always holds a pair (a pair longer than that keeps its first code and a
+ *     tail of ones, and its second element is listed), and an escape code is n_ranked ones whose
+ *     raw exponent sits in the block's escape list.
  *   "Qwen3-4B-NWC-fp8" (model card): weight-only e4m3 with a symmetric per-output-channel
  *     scale, fp8 bytes coded losslessly, the scale applied at the end of the matvec.
  *
@@ -31,6 +35,8 @@
  *   - Any call may come from any host thread. Calls that share a workspace (or the one
  *     scratch array of nwc_gemv_noalloc) must not overlap on the GPU; order them on one
  *     stream or with events. The device error word is per device, shared by all streams.
+ *   - Every device the process uses gets its own kernel configuration on its first call
+ *     there (made with that device current).
  */
 #ifndef NWC_H
 #define NWC_H
@@ -71,7 +77,7 @@ enum { NWC_TABLE_ENTRIES = 8192, NWC_TABLE_BYTES = 32768 };
  */
 typedef struct nwc_matrix {
     int32_t elem;            /* NWC_ELEM_BF16 or NWC_ELEM_FP8_E4M3                          */
-    int32_t n_ranked;        /* exponents with a unary code (1..11)                         */
+    int32_t n_ranked;        /* exponents with a unary code (1..12)                         */
     int64_t n, k;            /* rows (output features), columns (input features)           */
     int64_t row_blocks;      /* ceil(n / 8)                                                 */
     int64_t col_blocks;      /* ceil(k / 512)                                               */
@@ -90,7 +96,7 @@ typedef struct nwc_matrix {
 /* Human-readable name of a status code (static string). */
 const char *nwc_status_str(nwc_status s);
 
-/* Library version string, e.g. "nwc 3 (format 3, sm_103a)". */
+/* Library version string, e.g. "nwc 4 (format 4, sm_103a)". */
 const char *nwc_version(void);
 
 /*
@@ -125,19 +131,31 @@ nwc_status nwc_quantize_fp8(const uint16_t *w, int64_t n, int64_t k, int64_t ld,
 
 /*
  * nwc_validate -- host check of a blob: header, rank table, block table, every block
- * region's size against its lane word counts and real-element counts, and every escape list
- * (entries name real elements with unranked exponents, in lane-then-t order, then at most
- * three padding words). NWC_ERR_FORMAT if any
- * check fails. Stream contents are checked by the kernels while decoding.
+ * region's size against its lane word counts (at most 26 each) and its raw section, and every
+ * escape list (entries name real elements, carry an exponent field of the element's width,
+ * come in lane-then-t order, then at most three padding words). NWC_ERR_FORMAT if any check
+ * fails. Stream contents are checked by the kernels while decoding.
  */
 nwc_status nwc_validate(const void *blob_host, size_t bytes);
 
 /*
  * nwc_bind -- validates the host copy of a blob (as nwc_validate) and fills *out with its
  * geometry and the device pointers of the same blob copied to blob_dev (16-byte aligned,
- * caller-owned). No device call is made.
+ * caller-owned). out->table is NULL. No device call is made.
  */
 nwc_status nwc_bind(const void *blob_host, size_t bytes, const void *blob_dev, nwc_matrix *out);
+
+/*
+ * nwc_decode_table -- the matrix's decode table on the host (the NWC page, "How it works": a
+ * shared-memory table indexed by the next bits of a lane's stream): NWC_TABLE_ENTRIES u32
+ * entries into table_host, entry p for the 13-bit peek p (first stream bit = bit 12): the row
+ * pair it holds, bits 0..4 its length in bits, bits 7..14 and 23..30 the two elements'
+ * exponent fields in BF16 position (fp8: v + 120, 0 for 0; an escape or the tail of a cut pair:
+ * 0), bits 16..17 how many of them the escape list holds. Copy it to device memory (16-byte
+ * aligned, kept alive and unchanged while in use) and set m->table to that copy: every kernel
+ * then loads it with one bulk copy instead of building it in shared memory. Host only.
+ */
+nwc_status nwc_decode_table(const nwc_matrix *m, uint32_t *table_host);
 
 /*
  * nwc_decode -- dequantization to the stored elements, bit-exact (the NWC page, "How it
@@ -164,19 +182,17 @@ nwc_status nwc_dequantize_fp8(const uint8_t *q, int64_t ld_q, const float *scale
 
 /*
  * nwc_gemv_workspace_bytes -- device scratch nwc_gemv needs for m (at least 16 bytes): FP32
- * partial sums per (row, 512-column block) and one counter per 8-row block (both only when
- * K > 512). The 4096-entry decode table (the NWC page: a 16 KB shared-memory table indexed by
- * the next 12 stream bits) is built by every CTA in its own shared memory and needs no
- * workspace.
+ * partial-sum slots per (row, 512-column block) and one counter per 8-row block (both only when
+ * K > 512).
  */
 size_t nwc_gemv_workspace_bytes(const nwc_matrix *m);
 
 /*
- * nwc_gemv_prepare -- readies a workspace for m: zeroes its counters (asynchronously on the
- * stream). Call once per workspace before its first nwc_gemv; every
- * nwc_gemv leaves the counters at zero again, so the workspace serves repeated calls and CUDA-
- * graph replays. ws is 16-byte aligned, ws_bytes >= nwc_gemv_workspace_bytes(m). Calls sharing
- * one workspace must not overlap on the GPU.
+ * nwc_gemv_prepare -- readies a workspace for m: every partial-sum slot to the empty marker
+ * (all bits set) and every counter to zero (asynchronously on the stream). Call once per
+ * workspace before its first nwc_gemv; every nwc_gemv leaves the workspace in that state
+ * again, so it serves repeated calls and CUDA-graph replays. ws is 16-byte aligned, ws_bytes >=
+ * nwc_gemv_workspace_bytes(m). Calls sharing one workspace must not overlap on the GPU.
  */
 nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_stream stream);
 
@@ -189,6 +205,19 @@ nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_
  */
 nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                     nwc_stream stream);
+
+/*
+ * nwc_gemv_next -- nwc_gemv on m, which also brings the block regions, block table and decode
+ * table of `next` (the matrix the caller multiplies after this one; NULL: none) into L2 while
+ * this call decodes: each warp issues bulk L2 prefetches for its share once its own first
+ * regions have landed, so the next call's weights are read from HBM during this call's decode
+ * phase instead of at the start of its own. The result is nwc_gemv's, bit for bit. Worth it
+ * when next's blob is a small part of the 129 MB L2 (the prefetched lines are evicted before
+ * use otherwise). The pages run a whole decoding step as one CUDA graph ("Run a model"); this
+ * is the overlap such a fixed sequence of products allows.
+ */
+nwc_status nwc_gemv_next(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
+                         const nwc_matrix *next, nwc_stream stream);
 
 /*
  * nwc_gemv_noalloc -- nwc_gemv for callers that cannot allocate device memory: no workspace

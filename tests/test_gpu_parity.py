@@ -170,6 +170,21 @@ def test_table_built_in_kernel_equals_copied_table(elem):
     gemv_check(blob, synth.activations_bf16(1300, 18), mat=b)
 
 
+def test_gemv_next_equals_gemv_bitwise():
+    """nwc_gemv_next (the same product, with the next matrix's bytes prefetched into L2) gives
+    nwc_gemv's result bit for bit, for a chain of three matrices of different shapes."""
+    shapes = [(4096, 1024), (1000, 4096), (300, 700)]
+    mats, xs = [], []
+    for i, (n, k) in enumerate(shapes):
+        mats.append(nwc.Matrix(nwc.encode(synth.normal_bf16((n, k), 0.02, seed=60 + i))))
+        xs.append(dev_bits(synth.activations_bf16(k, 70 + i)))
+    for i, m in enumerate(mats):
+        a = m.gemv(xs[i])
+        b = m.gemv(xs[i], next=mats[(i + 1) % 3])
+        assert torch.equal(a, b)
+    assert_clean()
+
+
 def test_matmul_batch_via_decode_and_cublas():
     """Batch > 1 (prefill): decode to BF16, then cuBLAS. Output BF16, so each entry is checked
     against the FP64 product with BF16 rounding added to the GEMV bound."""
