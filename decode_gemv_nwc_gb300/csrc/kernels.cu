@@ -827,14 +827,15 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     if (b < m.nb) issue(c0, c1, false);
     lut_start(m, smem, lut_bar);
     __syncthreads();
-    if (!lut_ready(m, lut_bar)) timed_out = true;
     // Up to here only the matrix and its table were read. x, the workspace and y may belong to
-    // the kernel before this one on the stream: wait for it to complete.
+    // the kernel before this one on the stream: wait for it to complete. The table copy is
+    // waited for only before the first decode, so that it lands while the activations load
+    // and the first region arrives.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t lutb = smem_u32(smem);
     const uint64_t w_id = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;  // = the warp's first block
     const uint64_t ways = m.nb < total_warps ? m.nb : total_warps;
-    bool prefetched = false;
+    bool prefetched = false, lut_ok = false;
     while (b < m.nb && !timed_out) {
         const uint64_t nxt = b + total_warps, nn = nxt + total_warps;
         uint32_t f0 = 0, f1 = 0;  // bounds of block nn, for the next iteration
@@ -869,11 +870,25 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
             }
             inflight = false;
             phase ^= 1u;
+            if (!lut_ok) {
+                if (!lut_ready(m, lut_bar)) {
+                    timed_out = true;
+                    break;
+                }
+                lut_ok = true;
+            }
             if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
             prefetched = true;
             if (KR && kc < kCols) gemv_block<ELEM, NB, KR>(stage, bytes, lane, lutb, xb, ld_x, xs, acc, bad, kc, rows);
             else gemv_block<ELEM, NB, false>(stage, bytes, lane, lutb, xb, ld_x, xs, acc, bad, kCols, rows);
         } else {
+            if (!lut_ok) {
+                if (!lut_ready(m, lut_bar)) {
+                    timed_out = true;
+                    break;
+                }
+                lut_ok = true;
+            }
             if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
             prefetched = true;
             gemv_block_global<ELEM, NB>(src, bytes, lane, lutb, xb, ld_x, acc, bad, kc, rows);
