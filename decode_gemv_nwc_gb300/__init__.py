@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "BF16", "FP8", "NwcError", "lib", "encode", "encode_fp8", "quantize_fp8", "validate",
-    "Matrix", "check", "sm_count", "status_str", "save", "load", "decode_table",
+    "Matrix", "check", "sm_count", "status_str", "save", "load", "file_entries", "decode_table", "gemv_list",
 ]
 
 BF16, FP8 = 0, 1
@@ -29,6 +29,9 @@ class NwcError(RuntimeError):
         self.status = status
 
 
+LIST_MAX = 256  # NWC_GEMV_LIST_MAX: products per nwc_gemv_list call
+
+
 class NwcMatrix(ctypes.Structure):
     """Mirror of struct nwc_matrix."""
     _fields_ = [
@@ -40,6 +43,12 @@ class NwcMatrix(ctypes.Structure):
         ("blob_bytes", ctypes.c_uint64), ("max_block_bytes", ctypes.c_uint64),
         ("data_bytes", ctypes.c_uint64), ("table", ctypes.c_void_p),
     ]
+
+
+class NwcGemvItem(ctypes.Structure):
+    """Mirror of struct nwc_gemv_item."""
+    _fields_ = [("m", ctypes.POINTER(NwcMatrix)), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -78,9 +87,19 @@ def lib():
     L.nwc_check.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
     L.nwc_decode_table.argtypes = [ctypes.POINTER(NwcMatrix), p]
     L.nwc_sm_count.restype = i32
+    cp = ctypes.c_char_p
+    L.nwc_file_save.argtypes = [cp, i32, ctypes.POINTER(cp), ctypes.POINTER(p), ctypes.POINTER(sz)]
+    L.nwc_file_count.argtypes = [cp, ctypes.POINTER(i32)]
+    L.nwc_file_entry.argtypes = [cp, i32, p, sz, ctypes.POINTER(sz)]
+    L.nwc_file_find.argtypes = [cp, cp, ctypes.POINTER(i32)]
+    L.nwc_file_read.argtypes = [cp, i32, p, sz, ctypes.POINTER(sz)]
+    L.nwc_file_load.argtypes = [cp, i32, p, sz, p, sz, ctypes.POINTER(NwcMatrix), p]
+    L.nwc_gemv_list.argtypes = [ctypes.POINTER(NwcGemvItem), i32, p]
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
                  "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gemv_batch_prepare",
-                 "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table", "nwc_gemv_next"):
+                 "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table", "nwc_gemv_next",
+                 "nwc_dequantize_fp8", "nwc_file_save", "nwc_file_count", "nwc_file_entry", "nwc_file_find",
+                 "nwc_file_read", "nwc_file_load", "nwc_gemv_list"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -190,21 +209,46 @@ class Matrix:
         host = np.frombuffer(blob, np.uint8)
         if device_blob is None:
             device_blob = torch.from_numpy(host.copy()).to(device)
-        self.device_blob = device_blob
-        self.m = NwcMatrix()
-        _ok(lib().nwc_bind(_np_ptr(host), len(blob), ctypes.c_void_p(device_blob.data_ptr()), ctypes.byref(self.m)),
+        m = NwcMatrix()
+        _ok(lib().nwc_bind(_np_ptr(host), len(blob), ctypes.c_void_p(device_blob.data_ptr()), ctypes.byref(m)),
             "nwc_bind")
+        self._set_up(m, device_blob, table, None)
+
+    @classmethod
+    def from_file(cls, path: str, name: str, device="cuda", table: bool = True, stream=None):
+        """The blob called ``name`` in a file written by save(), loaded straight into device memory
+        by nwc_file_load (read into a page-locked host buffer, validated, bound, one copy)."""
+        import torch
+        idx, size = ctypes.c_int(), ctypes.c_size_t()
+        path_b = os.fsencode(path)
+        _ok(lib().nwc_file_find(path_b, name.encode(), ctypes.byref(idx)), f"nwc_file_find {name}")
+        _ok(lib().nwc_file_entry(path_b, idx.value, None, 0, ctypes.byref(size)), "nwc_file_entry")
+        host = torch.empty(size.value, dtype=torch.uint8, pin_memory=True)
+        device_blob = torch.empty(size.value, dtype=torch.uint8, device=device)
+        m = NwcMatrix()
+        _ok(lib().nwc_file_load(path_b, idx.value, ctypes.c_void_p(host.data_ptr()), size.value,
+                                ctypes.c_void_p(device_blob.data_ptr()), size.value, ctypes.byref(m),
+                                _stream_ptr(stream)), f"nwc_file_load {name}")
+        self = cls.__new__(cls)
+        self._set_up(m, device_blob, table, stream)
+        (stream or torch.cuda.current_stream()).synchronize()  # the host buffer may go now
+        return self
+
+    def _set_up(self, m: NwcMatrix, device_blob, table: bool, stream):
+        import torch
+        self.device_blob = device_blob
+        self.m = m
         self.table = None
         if table:
             self.table = torch.from_numpy(decode_table(self.m).view(np.int32)).to(device_blob.device)
             self.m.table = ctypes.c_void_p(self.table.data_ptr())
         self.elem, self.n, self.k = self.m.elem, self.m.n, self.m.k
-        self.blob_bytes = len(blob)
+        self.blob_bytes = int(m.blob_bytes)
         ws = int(lib().nwc_gemv_workspace_bytes(ctypes.byref(self.m)))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device_blob.device)
         self.ws_bytes = ws
         _ok(lib().nwc_gemv_prepare(ctypes.byref(self.m), ctypes.c_void_p(self.workspace.data_ptr()), ws,
-                                   _stream_ptr(None)), "nwc_gemv_prepare")
+                                   _stream_ptr(stream)), "nwc_gemv_prepare")
 
     def gemv(self, x, y=None, stream=None, next=None):
         """y (float32[N]) = W x for x a BF16 vector given as an int16/bfloat16 CUDA tensor. next: the
@@ -306,43 +350,53 @@ class Matrix:
         return out
 
 
+def gemv_list(items, stream=None):
+    """y_i = W_i x_i for independent products in one launch (nwc_gemv_list). items: (Matrix, x,
+    y) triples (x BF16 [K] as an int16/bfloat16 CUDA tensor, y float32 [N]), each matrix with
+    its device decode table and using its own workspace; every x must be ready (no item reads
+    another's y). Each y equals Matrix.gemv's result bit for bit."""
+    arr = (NwcGemvItem * len(items))()
+    for i, (mat, x, y) in enumerate(items):
+        assert x.numel() == mat.k and x.is_cuda and x.is_contiguous() and y.numel() == mat.n and y.is_contiguous()
+        arr[i].m = ctypes.pointer(mat.m)
+        arr[i].x = x.data_ptr()
+        arr[i].y = y.data_ptr()
+        arr[i].ws = mat.workspace.data_ptr()
+        arr[i].ws_bytes = mat.ws_bytes
+    _ok(lib().nwc_gemv_list(arr, len(items), _stream_ptr(stream)), "nwc_gemv_list")
+
+
 # ------------------------------------------------------------------ blob files
-_FILE_MAGIC = b"NWCF"
-
-
 def save(path: str, blobs: dict) -> None:
-    """Writes named blobs to one file: "NWCF", u32 count, then per entry u32 name length, the
-    UTF-8 name, u64 blob length and the blob, each blob starting on a 16-byte boundary."""
-    import struct
-    with open(path, "wb") as f:
-        f.write(_FILE_MAGIC + struct.pack("<I", len(blobs)))
-        for name, blob in blobs.items():
-            nb = name.encode()
-            f.write(struct.pack("<I", len(nb)) + nb + struct.pack("<Q", len(blob)))
-            f.write(b"\0" * (-f.tell() % 16))
-            f.write(blob)
+    """Writes named blobs (name -> blob bytes) to one file with nwc_file_save (every blob
+    validated; the file is replaced whole or left as it was)."""
+    names = list(blobs)
+    n = len(names)
+    c_names = (ctypes.c_char_p * n)(*[k.encode() for k in names])
+    bufs = [np.frombuffer(blobs[k], np.uint8) for k in names]
+    c_blobs = (ctypes.c_void_p * n)(*[b.ctypes.data for b in bufs])
+    c_sizes = (ctypes.c_size_t * n)(*[b.size for b in bufs])
+    _ok(lib().nwc_file_save(os.fsencode(path), n, c_names, c_blobs, c_sizes), f"nwc_file_save {path}")
+
+
+def file_entries(path: str) -> list:
+    """(name, blob length) of every entry of a blob file, in file order."""
+    path_b = os.fsencode(path)
+    count = ctypes.c_int()
+    _ok(lib().nwc_file_count(path_b, ctypes.byref(count)), f"nwc_file_count {path}")
+    out, name, size = [], ctypes.create_string_buffer(4097), ctypes.c_size_t()
+    for i in range(count.value):
+        _ok(lib().nwc_file_entry(path_b, i, name, len(name), ctypes.byref(size)), "nwc_file_entry")
+        out.append((name.value.decode(), size.value))
+    return out
 
 
 def load(path: str) -> dict:
-    """Reads a file written by save(); every blob is validated (nwc_validate) before it is
-    returned."""
-    import struct
-    with open(path, "rb") as f:
-        data = f.read()
-    if data[:4] != _FILE_MAGIC:
-        raise NwcError(2, "nwc load: not an NWC blob file")
-    (count,) = struct.unpack_from("<I", data, 4)
-    pos, out = 8, {}
-    for _ in range(count):
-        (ln,) = struct.unpack_from("<I", data, pos)
-        name = data[pos + 4:pos + 4 + ln].decode()
-        (size,) = struct.unpack_from("<Q", data, pos + 4 + ln)
-        pos += 4 + ln + 8
-        pos += -pos % 16
-        blob = data[pos:pos + size]
-        if len(blob) != size:
-            raise NwcError(2, f"nwc load: {name} truncated")
-        _ok(validate(blob), f"nwc load: {name}")
-        out[name] = blob
-        pos += size
+    """Every blob of a file written by save(), read and validated by nwc_file_read."""
+    path_b = os.fsencode(path)
+    out = {}
+    for i, (name, size) in enumerate(file_entries(path)):
+        buf = np.empty(size, np.uint8)
+        _ok(lib().nwc_file_read(path_b, i, _np_ptr(buf), size, None), f"nwc_file_read {name}")
+        out[name] = buf.tobytes()
     return out

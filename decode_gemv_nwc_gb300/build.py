@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU = ["kernels.cu", "dequant.cu"]
-CPP = ["encoder.cpp", "bind.cpp"]
+CPP = ["encoder.cpp", "bind.cpp", "blobfile.cpp"]
 
 
 def _sources():

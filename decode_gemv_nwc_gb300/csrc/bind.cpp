@@ -128,6 +128,7 @@ extern "C" const char *nwc_status_str(nwc_status s) {
         case NWC_ERR_TIMEOUT: return "device wait timed out";
         case NWC_ERR_DEVICE_FLAG: return "device error flag raised";
         case NWC_ERR_UNSUPPORTED: return "unsupported";
+        case NWC_ERR_IO: return "file could not be opened, read or written";
     }
     return "unknown status";
 }

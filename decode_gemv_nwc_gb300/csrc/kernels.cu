@@ -40,7 +40,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "nwc.h"
 #include "nwc_format.h"
@@ -911,6 +914,200 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
         if (inflight) mbar_wait(bar, phase & 1u);
     }
     if (m.table) mbar_wait(lut_bar, 0);  // the table copy has landed (a no-op unless it timed out)
+    if (bad) raise_error(kErrFormat);
+}
+
+// =================================================================== GEMV list
+// y_i = W_i x_i for up to kListMax independent products in one launch. The items' blocks are
+// numbered one after another (item by item, each in its blob's row-block-major order) and CTA c
+// takes the contiguous range [c T / G, (c + 1) T / G) of the T blocks; its warps take the range's
+// blocks item by item, warp w every kGemvWarps-th block from the item's first one in the range.
+// A CTA thus meets only the few items its range crosses and brings in each one's decode table
+// once: at an item boundary all warps meet at a barrier and thread 0 copies the next table over
+// the previous one (each warp's first copy of the next item is already in flight). Each block
+// is decoded, and its row block reduced, exactly as by gemv_kernel (the same code, the same
+// fixed-order sum over column blocks, on the item's own workspace), so every y_i equals
+// nwc_gemv's bit for bit.
+constexpr int kListMax = NWC_GEMV_LIST_MAX;
+struct ListItem {
+    const uint32_t *tab;
+    const uint8_t *data;
+    const float *scales;
+    const uint32_t *table;
+    const uint16_t *x;
+    float *y;
+    float *partial;
+    uint32_t *counters;
+    uint64_t n, k, cbs, n_pad, start;  // start: the item's first block in the list's numbering
+};
+struct ListParams {
+    uint64_t total;  // blocks of all items
+    int count;
+    ListItem items[kListMax];
+};
+static_assert(sizeof(ListParams) <= 32764, "kernel parameters");
+
+template <int ELEM, bool KR = false>
+__global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __grid_constant__ ListParams p) {
+    using S = Smem<kGemvWarps>;
+    constexpr uint64_t W = kGemvWarps;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bar = smem_u32(smem + S::kBar + 8 * warp), lut_bar = smem_u32(smem + S::kLutBar);
+    const uint32_t stage = smem_u32(smem + S::kStage + warp * kStageBytes);
+    const uint32_t lutb = smem_u32(smem);
+    const uint64_t s0 = p.total * blockIdx.x / gridDim.x, s1 = p.total * (blockIdx.x + 1) / gridDim.x;
+    if (s0 >= s1) return;
+    // the items the range crosses: f .. l
+    int f = 0;
+    while (f + 1 < p.count && p.items[f + 1].start <= s0) f++;
+    int l = f;
+    while (l + 1 < p.count && p.items[l + 1].start < s1) l++;
+    auto range_end = [&](int j) {
+        const uint64_t e = j + 1 < p.count ? p.items[j + 1].start : p.total;
+        return e < s1 ? e : s1;
+    };
+    auto load_table = [&](int j) {
+        mbar_expect_tx(lut_bar, kLutBytes);
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            tma_load_1d(lutb + q * (kLutBytes / 4), p.items[j].table + q * (kLutEntries / 4), kLutBytes / 4, lut_bar);
+    };
+
+    uint32_t phase = 0;
+    bool bad = false, timed_out = false, inflight = false;
+    auto issue = [&](const uint8_t *data, uint32_t s0u, uint32_t s1u, bool reuse) {
+        const uint32_t bytes = 16 * (s1u - s0u);
+        if (bytes <= (uint32_t)kStageBytes) {
+            if (lane == 0) {
+                if (reuse) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_expect_tx(bar, bytes);
+                tma_load_1d(stage, data + 16 * (uint64_t)s0u, bytes, bar);
+            }
+            inflight = true;
+        }
+    };
+    // Bounds of the warp's current block (c0/c1, every lane) and of its next one (n0/n1, lane 0),
+    // for the warp's first block of item j.
+    uint32_t c0 = 0, c1 = 0, n0 = 0, n1 = 0;
+    auto first_bounds = [&](int j) {
+        const ListItem &it = p.items[j];
+        const uint64_t beg = it.start > s0 ? it.start : s0, end = range_end(j), b = beg + (uint64_t)warp;
+        c0 = c1 = n0 = n1 = 0;
+        if (lane == 0 && b < end) {
+            c0 = it.tab[b - it.start];
+            c1 = it.tab[b - it.start + 1];
+        }
+        if (lane == 0 && b + W < end) {
+            n0 = it.tab[b + W - it.start];
+            n1 = it.tab[b + W - it.start + 1];
+        }
+        c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
+        c1 = __shfl_sync(0xFFFFFFFFu, c1, 0);
+        return b < end;
+    };
+
+    // the warp's barrier and first copy, and the first item's table, before anything else
+    if (lane == 0) {
+        mbar_init(bar);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (first_bounds(f)) issue(p.items[f].data, c0, c1, false);
+    if (threadIdx.x == 0) {
+        mbar_init(lut_bar);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        load_table(f);
+    }
+    __syncthreads();
+    // x, the workspaces and y may belong to the kernel before this one on the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    for (int j = f; j <= l; j++) {
+        const ListItem &it = p.items[j];
+        Mat m;  // the fields finish_rows reads
+        m.n = it.n;
+        m.cbs = it.cbs;
+        m.scales = it.scales;
+        const uint64_t beg = it.start > s0 ? it.start : s0, end = range_end(j);
+        if (j > f) {
+            __syncthreads();  // every warp is done with the previous table
+            if (threadIdx.x == 0) {
+                // the previous copy has landed (already waited for, unless a wait timed out)
+                mbar_wait(lut_bar, (uint32_t)(j - 1 - f) & 1u);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                load_table(j);
+            }
+        }
+        bool lut_ok = false;
+        uint64_t b = beg + (uint64_t)warp;
+        while (b < end && !timed_out) {
+            const uint64_t nxt = b + W, nn = nxt + W;
+            uint32_t f0 = 0, f1 = 0;  // bounds of block nn, for the next iteration
+            if (lane == 0) {
+                if (nn < end) {
+                    f0 = it.tab[nn - it.start];
+                    f1 = it.tab[nn - it.start + 1];
+                }
+                if (nxt < end) l2_prefetch(it.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
+            }
+            const uint32_t bytes = 16 * (c1 - c0);
+            const uint64_t bi = b - it.start, rb = bi / it.cbs, cb = bi % it.cbs;
+            const int rows = real_rows(it.n, rb);
+            const uint64_t kc64 = it.k - cb * kCols;
+            const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;
+            const uint16_t *xb = it.x + cb * kCols;
+            float acc[1][8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) acc[0][r] = 0.0f;
+            if (bytes <= (uint32_t)kStageBytes) {
+                uint32_t xs[1][8];
+                const int cl = kc - kLaneCols * lane, cols = cl < 0 ? 0 : (cl > kLaneCols ? kLaneCols : cl);
+                load_x16(xb + kLaneCols * lane, cols, xs[0]);
+                if (!mbar_wait(bar, phase & 1u)) {
+                    timed_out = true;
+                    break;
+                }
+                inflight = false;
+                phase ^= 1u;
+                if (!lut_ok) {
+                    if (!mbar_wait(lut_bar, (uint32_t)(j - f) & 1u)) {
+                        timed_out = true;
+                        break;
+                    }
+                    lut_ok = true;
+                }
+                if (KR && kc < kCols) gemv_block<ELEM, 1, KR>(stage, bytes, lane, lutb, xb, 0, xs, acc, bad, kc, rows);
+                else gemv_block<ELEM, 1, false>(stage, bytes, lane, lutb, xb, 0, xs, acc, bad, kCols, rows);
+            } else {
+                if (!lut_ok) {
+                    if (!mbar_wait(lut_bar, (uint32_t)(j - f) & 1u)) {
+                        timed_out = true;
+                        break;
+                    }
+                    lut_ok = true;
+                }
+                gemv_block_global<ELEM, 1>(it.data + 16 * (uint64_t)c0, bytes, lane, lutb, xb, 0, acc, bad, kc, rows);
+            }
+            float sum[1] = {transpose_reduce(acc[0], lane)};
+            finish_rows<ELEM, 1>(m, sum, lane, rb, cb, it.y, 0, it.partial, it.counters, it.n_pad, timed_out);
+            __syncwarp();
+            c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
+            c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
+            if (nxt < end) issue(it.data, c0, c1, true);
+            n0 = f0;
+            n1 = f1;
+            b = nxt;
+        }
+        // the warp's first copy of the next item goes out before the barrier
+        if (j < l && first_bounds(j + 1) && !timed_out) issue(p.items[j + 1].data, c0, c1, true);
+    }
+    if (timed_out) {
+        raise_error(kErrTimeout);
+        if (inflight) mbar_wait(bar, phase & 1u);
+    }
+    mbar_wait(lut_bar, (uint32_t)(l - f) & 1u);  // the last table copy has landed
     if (bad) raise_error(kErrFormat);
 }
 
@@ -1897,6 +2094,66 @@ extern "C" nwc_status nwc_gemv_next(const nwc_matrix *mp, const uint16_t *x, flo
 extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                                nwc_stream stream) {
     return nwc_gemv_next(mp, x, y, ws, ws_bytes, nullptr, stream);
+}
+
+// ---------------------------------------------------------------- GEMV list
+namespace {
+template <int ELEM, bool KR>
+cudaError_t launch_list(const ListParams &p, int grid, cudaStream_t s) {
+    if (!smem_ready<gemv_list_kernel<ELEM, KR>>(kGemvSmem)) return cudaErrorInvalidConfiguration;
+    return launch_pdl(gemv_list_kernel<ELEM, KR>, grid, kGemvWarps * 32, kGemvSmem, s, p);
+}
+}  // namespace
+
+extern "C" nwc_status nwc_gemv_list(const nwc_gemv_item *items, int count, nwc_stream stream) {
+    if (!items || count < 1 || count > kListMax) return NWC_ERR_INVALID_ARG;
+    static thread_local ListParams p;  // 26 KB: kept off the stack
+    std::vector<std::pair<uintptr_t, uintptr_t>> used;  // workspace bytes the items touch
+    p.count = count;
+    p.total = 0;
+    int elem = -1;
+    bool kr = false;
+    for (int i = 0; i < count; i++) {
+        const nwc_gemv_item &it = items[i];
+        if (!it.m || !it.x || !it.y || !it.ws) return NWC_ERR_INVALID_ARG;
+        const nwc_matrix &m = *it.m;
+        if (!m.table || (reinterpret_cast<uintptr_t>(m.table) & 15)) return NWC_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(it.x) & 15) || (reinterpret_cast<uintptr_t>(it.ws) & 15)) return NWC_ERR_INVALID_ARG;
+        if (it.ws_bytes < nwc_gemv_workspace_bytes(&m)) return NWC_ERR_INVALID_ARG;
+        if (elem >= 0 && m.elem != elem) return NWC_ERR_INVALID_ARG;
+        elem = m.elem;
+        kr |= (m.k % kCols) != 0;
+        ListItem &d = p.items[i];
+        d.tab = m.block_tab;
+        d.data = m.data;
+        d.scales = m.scales;
+        d.table = m.table;
+        d.x = it.x;
+        d.y = it.y;
+        d.partial = static_cast<float *>(it.ws);
+        d.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(it.ws) + ws_counter_off(m));
+        d.n = (uint64_t)m.n;
+        d.k = (uint64_t)m.k;
+        d.cbs = (uint64_t)m.col_blocks;
+        d.n_pad = pad_rows(m);
+        d.start = p.total;
+        p.total += (uint64_t)m.row_blocks * (uint64_t)m.col_blocks;
+        if (m.col_blocks > 1) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(it.ws);
+            used.push_back({a, a + nwc_gemv_workspace_bytes(&m)});
+        }
+    }
+    std::sort(used.begin(), used.end());
+    for (size_t i = 1; i < used.size(); i++)
+        if (used[i].first < used[i - 1].second) return NWC_ERR_INVALID_ARG;  // two items share workspace
+    const int sms = sm_count();
+    if (sms <= 0) return NWC_ERR_CUDA;
+    const int grid = (int)(p.total < (uint64_t)sms ? p.total : (uint64_t)sms);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t rc;
+    if (elem == NWC_ELEM_BF16) rc = kr ? launch_list<0, true>(p, grid, s) : launch_list<0, false>(p, grid, s);
+    else rc = kr ? launch_list<1, true>(p, grid, s) : launch_list<1, false>(p, grid, s);
+    return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- small-batch GEMV

@@ -58,7 +58,8 @@ typedef enum nwc_status {
     NWC_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed              */
     NWC_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (reported by nwc_check)    */
     NWC_ERR_DEVICE_FLAG = 5, /* a kernel raised the device error word (see nwc_check)    */
-    NWC_ERR_UNSUPPORTED = 6  /* valid request this build does not implement              */
+    NWC_ERR_UNSUPPORTED = 6, /* valid request this build does not implement              */
+    NWC_ERR_IO = 7           /* a blob file could not be opened, read or written         */
 } nwc_status;
 
 enum { NWC_ELEM_BF16 = 0, NWC_ELEM_FP8_E4M3 = 1 };
@@ -236,6 +237,34 @@ nwc_status nwc_gemv_next(const nwc_matrix *m, const uint16_t *x, float *y, void 
  */
 nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
 
+/* Largest item count of one nwc_gemv_list call. */
+#define NWC_GEMV_LIST_MAX 256
+
+/* One product of an nwc_gemv_list call. */
+typedef struct nwc_gemv_item {
+    const nwc_matrix *m; /* bound matrix whose device decode table is set (m->table)          */
+    const uint16_t *x;   /* BF16[K], 16-byte aligned                                          */
+    float *y;            /* FP32[N]                                                           */
+    void *ws;            /* a workspace prepared by nwc_gemv_prepare for m, 16-byte aligned   */
+    size_t ws_bytes;     /* >= nwc_gemv_workspace_bytes(m)                                    */
+} nwc_gemv_item;
+
+/*
+ * nwc_gemv_list -- y_i = W_i x_i for `count` independent products (1..NWC_GEMV_LIST_MAX) in one
+ * launch. The pages run a whole decoding step, with fused projections, as one CUDA graph ("Run a
+ * model": graph_decode with --fusion); this call puts many of that step's matrix-vector products
+ * into one persistent kernel instead of one kernel each: every SM takes a contiguous share of all
+ * items' blocks, so the per-launch start-up (decode table, first copies) is paid about once per
+ * SM instead of once per matrix, and one item's final sums overlap the next item's decoding.
+ * Each y_i equals nwc_gemv's result for its item bit for bit. Requirements: every item's x is
+ * ready when the call starts (no item reads another item's y: dependent products go in separate
+ * calls, in stream order); the y_i overlap neither one another nor any x or workspace; the items'
+ * workspaces do not overlap (checked: NWC_ERR_INVALID_ARG); all items have the same element type
+ * (NWC_ERR_INVALID_ARG otherwise). The items array is read during the call only. Asynchronous on
+ * the stream; a workspace is left in its prepared state, as by nwc_gemv.
+ */
+nwc_status nwc_gemv_list(const nwc_gemv_item *items, int count, nwc_stream stream);
+
 /* Largest vector count of one nwc_gemv_batch call. */
 #define NWC_GEMV_BATCH_MAX 16
 
@@ -289,6 +318,49 @@ nwc_status nwc_gather(const nwc_matrix *m, const int32_t *ids, int64_t n_ids, vo
  * (a bounded wait ran out) otherwise; *flags (if not NULL) receives the raw bits.
  */
 nwc_status nwc_check(nwc_stream stream, uint32_t *flags);
+
+/*
+ * Blob files -- compressed checkpoints (the NWC page's usage block: a compressed model is
+ * saved once and later loaded straight onto the GPU, without the BF16 originals). A file holds
+ * named blobs: "NWCF", u32 entry count, then per entry u32 name length, the UTF-8 name (1..4096
+ * bytes, unique, no NUL), u64 blob length, zero bytes to the next 16-byte file offset, the blob;
+ * the file ends with the last blob. Host calls only, except the copy nwc_file_load enqueues.
+ * A file that cannot be opened, read or written is NWC_ERR_IO; a file whose index does not hold
+ * together (lengths past its end, duplicate names, trailing bytes) or one of whose blobs fails
+ * nwc_validate is NWC_ERR_FORMAT; an index outside [0, count) is NWC_ERR_INVALID_ARG.
+ */
+
+/* nwc_file_save -- writes count named blobs (blobs[i], bytes[i] bytes, names[i] a NUL-terminated
+ * string) to path, replacing it. Every blob is validated first; on any error nothing at path
+ * changes (the file is written beside it and renamed over it). */
+nwc_status nwc_file_save(const char *path, int count, const char *const *names, const void *const *blobs,
+                         const size_t *bytes);
+
+/* nwc_file_count -- number of entries in the file (its whole index is checked). */
+nwc_status nwc_file_count(const char *path, int *count);
+
+/* nwc_file_entry -- name (copied with its NUL into name, name_cap bytes; NULL to skip) and blob
+ * length (*bytes; NULL to skip) of entry index. A name longer than name_cap - 1 bytes is
+ * NWC_ERR_INVALID_ARG, with *bytes still set. */
+nwc_status nwc_file_entry(const char *path, int index, char *name, size_t name_cap, size_t *bytes);
+
+/* nwc_file_find -- index of the entry called name (NWC_ERR_INVALID_ARG if none is). */
+nwc_status nwc_file_find(const char *path, const char *name, int *index);
+
+/* nwc_file_read -- entry index's blob into blob_host (cap bytes) and validated; *bytes (if not
+ * NULL) receives its length, also when cap is too small (then NWC_ERR_INVALID_ARG). */
+nwc_status nwc_file_read(const char *path, int index, void *blob_host, size_t cap, size_t *bytes);
+
+/*
+ * nwc_file_load -- entry index read into blob_host (host_cap bytes; page-locked memory makes the
+ * copy asynchronous), validated and bound to blob_dev (dev_cap bytes, 16-byte aligned,
+ * caller-owned) as nwc_bind does, then copied to blob_dev with one cudaMemcpyAsync on the
+ * stream. *out is set only on success; out->table is NULL. blob_host must stay unchanged until
+ * the stream has passed the copy; kernels using *out go on the same stream (or wait for it).
+ * The blob's length comes from nwc_file_entry.
+ */
+nwc_status nwc_file_load(const char *path, int index, void *blob_host, size_t host_cap, void *blob_dev,
+                         size_t dev_cap, nwc_matrix *out, nwc_stream stream);
 
 /* Streaming multiprocessors of the current device (queried, never assumed). */
 int nwc_sm_count(void);

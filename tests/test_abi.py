@@ -144,20 +144,6 @@ def test_encode_argument_errors():
     assert L.nwc_encode(p, 2, 2, 2, 0, 1, buf.ctypes.data_as(ctypes.c_void_p), ctypes.byref(small)) == 1
 
 
-def test_blob_file_round_trip(tmp_path):
-    blobs = {"q": nwc.encode(synth.normal_bf16((9, 513), 0.02, 1)),
-             "lm_head": nwc.encode(synth.normal_bf16((17, 100), 0.02, 2))}
-    path = str(tmp_path / "model.nwc")
-    nwc.save(path, blobs)
-    back = nwc.load(path)
-    assert back == blobs
-    raw = bytearray(open(path, "rb").read())
-    raw[60] ^= 0xFF  # byte 28 of the first blob: its block count
-    open(path, "wb").write(bytes(raw))
-    with pytest.raises(nwc.NwcError):
-        nwc.load(path)
-
-
 def test_gpu_entry_points_reject_bad_arguments_before_any_launch():
     """Argument checks return NWC_ERR_INVALID_ARG before any CUDA call, so they run here with
     addresses that are never dereferenced."""

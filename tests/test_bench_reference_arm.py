@@ -1,5 +1,6 @@
-"""The reference arm of bench.py (the CPU oracle timed on a bounded slice of the square matrix)
-prints one JSON line with the keys of the benchmark contract; it needs no GPU."""
+"""The reference arm of bench.py (the CPU oracle timed on whole 4096x4096 matrices, rows split over
+the host's cores) prints one JSON line with the keys of the benchmark contract, and its step time
+is what the run actually spent; it needs no GPU."""
 import json
 import os
 import subprocess
@@ -24,3 +25,6 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert cb["cores"] == len(os.sched_getaffinity(0))
+    # the timed steps are whole matrices: their sum is the timed wall time, not a projection
+    assert abs(d["steps"] * d["ms_per_step"] / 1e3 - d["timed_seconds"]) <= 0.05 * d["timed_seconds"] + 0.01

@@ -18,8 +18,11 @@ TOL_REL, TOL_ABS = 2.0 ** -10, 1e-6
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     from decode_gemv_nwc_gb300 import build
+    from oracle import parallel
     build.build()
     torch.cuda.init()
+    yield
+    parallel.shutdown()
 
 
 def dev_bits(a: np.ndarray):
@@ -43,6 +46,23 @@ def gemv_check(blob, x_bits, rows=None, mat=None):
     bound = TOL_REL * scale + TOL_ABS
     worst = int(np.argmax(err - bound))
     assert (err <= bound).all(), f"row {rows[worst]}: |{y[rows][worst]} - {ref[worst]}| > {bound[worst]}"
+    return y
+
+
+def gemv_check_all(blob, x_bits, mat):
+    """gemv_check on every row of a large matrix: the oracle's rows split by 8-row blocks over
+    the host's cores (oracle.parallel, bit-identical to one process)."""
+    from oracle import parallel
+    y = mat.gemv(dev_bits(x_bits)).cpu().numpy().astype(np.float64)
+    assert_clean()
+    with parallel.Oracle(blob) as po:
+        ref = po.gemv(x_bits)
+        scale = po.abs_dot(x_bits)
+    assert ref.shape == y.shape
+    err = np.abs(y - ref)
+    bound = TOL_REL * scale + TOL_ABS
+    worst = int(np.argmax(err - bound))
+    assert (err <= bound).all(), f"row {worst}: |{y[worst]} - {ref[worst]}| > {bound[worst]}"
     return y
 
 
@@ -237,16 +257,16 @@ def test_fp8_decode_and_gemv(shape):
     assert_clean()
     assert np.array_equal(qd.cpu().numpy(), q) and np.array_equal(sd.cpu().numpy(), s)
     x = synth.activations_bf16(shape[1], 77)
-    rows = None if shape[0] * shape[1] < 10 ** 6 else np.sort(np.random.default_rng(0).choice(shape[0], 512, False))
-    gemv_check(blob, x, rows=rows, mat=mat)
+    gemv_check_all(blob, x, mat)
 
 
+@pytest.mark.parametrize("layer", [0, 17, 35])
 @pytest.mark.parametrize("name", [s[0] for s in synth.LAYER_SHAPES])
-def test_decoder_stack_matrices_full_size(name):
-    """Each matrix of the 36-layer stack's first layer at full size (BF16, per-layer sigma):
-    decode bit-exact, GEMV within tolerance on 384 sampled rows (the shapes the benchmark
-    times)."""
-    w = synth.layer_matrix(0, name)  # BF16 bits, numpy uint16
+def test_decoder_stack_matrices_full_size(name, layer):
+    """Matrices of the 36-layer stack at full size (BF16; each layer has its own sigma and so its
+    own exponent ranking): the first, a middle and the last layer, decode bit-exact and the GEMV
+    within tolerance on every row (the shapes the benchmark times)."""
+    w = synth.layer_matrix(layer, name)  # BF16 bits, numpy uint16
     n, k = w.shape
     blob = nwc.encode(w)
     mat = nwc.Matrix(blob)
@@ -254,8 +274,32 @@ def test_decoder_stack_matrices_full_size(name):
     assert_clean()
     assert np.array_equal(out, w)
     x = synth.activations_bf16(k, 2000 + k)
-    rows = np.sort(np.random.default_rng(n + k).choice(n, 384, False))
-    gemv_check(blob, x, rows=rows, mat=mat)
+    gemv_check_all(blob, x, mat)
+
+
+@pytest.mark.parametrize("layer", [0, 35])
+@pytest.mark.parametrize("group", [("q", "k", "v"), ("gate", "up")])
+def test_fused_projection_blobs(group, layer):
+    """Fused projections (the NWC page's fuse step): q|k|v and gate|up of one layer stacked
+    row-wise and coded as one blob. The blob decodes to the parts one after another (bit-exact,
+    at the offsets encode_fused returns) and its GEMV is within tolerance on every row; each
+    part's rows also agree with the GEMV of that part's own blob within the same bound."""
+    parts = [synth.layer_matrix(layer, g) for g in group]
+    k = parts[0].shape[1]
+    blob, offsets = nwc.encode_fused(parts)
+    assert offsets.tolist() == np.cumsum([0] + [p.shape[0] for p in parts]).tolist()
+    mat = nwc.Matrix(blob)
+    out = mat.decode().cpu().numpy().view(np.uint16)
+    assert_clean()
+    assert np.array_equal(out, np.concatenate(parts))
+    x = synth.activations_bf16(k, 2000 + k)
+    y = gemv_check_all(blob, x, mat)
+    for i, p in enumerate(parts):
+        pb = nwc.encode(p)
+        yp = nwc.Matrix(pb).gemv(dev_bits(x)).cpu().numpy().astype(np.float64)
+        assert_clean()
+        bound = 2 * (TOL_REL * oracle.abs_dot(pb, x) + TOL_ABS)
+        assert (np.abs(y[offsets[i]:offsets[i + 1]] - yp) <= bound).all()
 
 
 def test_fp8_subnormal_and_zero_codes():
@@ -345,9 +389,9 @@ def test_gather_escape_heavy_rows():
 
 
 @pytest.mark.slow
-def test_embedding_table_gather_and_lm_head_sampled():
-    """151936 x 2560 tied table: 4096 random ids bit-exact, then the lm_head GEMV on
-    sampled rows (full size, the launch configuration the benchmark times)."""
+def test_embedding_table_gather_and_lm_head_every_row():
+    """151936 x 2560 tied table: 4096 random ids bit-exact, then the lm_head GEMV on every
+    row (full size, the launch configuration the benchmark times)."""
     w = synth.normal_bf16((synth.VOCAB, synth.HIDDEN), 0.02, seed=7)
     blob = nwc.encode(w)
     mat = nwc.Matrix(blob)
@@ -356,8 +400,7 @@ def test_embedding_table_gather_and_lm_head_sampled():
     assert_clean()
     assert np.array_equal(out, w[ids])
     x = synth.activations_bf16(synth.HIDDEN, 9)
-    rows = np.sort(np.random.default_rng(1).choice(synth.VOCAB, 2048, False))
-    gemv_check(blob, x, rows=rows, mat=mat)
+    gemv_check_all(blob, x, mat)
 
 
 # --------------------------------------------------------------------- small-batch GEMV
@@ -728,3 +771,106 @@ def test_fp8_dequantize_bit_exact_and_prefill():
     ref = Xf @ Wf.T
     bound = 2.0 ** -7 * (np.abs(Xf) @ np.abs(Wf).T) + 1e-6
     assert (np.abs(Y - ref) <= bound).all()
+
+
+# --------------------------------------------------------------------- GEMV list (one launch)
+def _list_run(items, stream=None):
+    """nwc_gemv_list over (blob, x_bits) pairs; returns the matrices, the outputs and the inputs."""
+    mats = [nwc.Matrix(b) for b, _ in items]
+    xs = [dev_bits(x) for _, x in items]
+    ys = [torch.full((m.n,), float("nan"), dtype=torch.float32, device="cuda") for m in mats]
+    nwc.gemv_list(list(zip(mats, xs, ys)), stream=stream)
+    return mats, xs, ys
+
+
+def test_gemv_list_full_layer_every_row():
+    """One decoder layer's products (q|k|v and gate|up fused, o, down, and the seven unfused
+    matrices) as one list launch: every y equals that matrix's own nwc_gemv bit for bit and is
+    within tolerance of the oracle on every row."""
+    ws = {name: synth.layer_matrix(17, name) for name, _, _ in synth.LAYER_SHAPES}
+    blobs = [nwc.encode_fused([ws["q"], ws["k"], ws["v"]])[0], nwc.encode(ws["o"]),
+             nwc.encode_fused([ws["gate"], ws["up"]])[0], nwc.encode(ws["down"])]
+    blobs += [nwc.encode(ws[name]) for name, _, _ in synth.LAYER_SHAPES]
+    items = []
+    for b in blobs:
+        k = oracle.info(b)["K"]
+        items.append((b, synth.activations_bf16(k, 5000 + k + len(items))))
+    mats, xs, ys = _list_run(items)
+    torch.cuda.synchronize()
+    assert_clean()
+    from oracle import parallel
+    for (blob, x), mat, xd, y in zip(items, mats, xs, ys):
+        y_one = mat.gemv(xd)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int32), y_one.view(torch.int32))
+        with parallel.Oracle(blob) as po:
+            ref, scale = po.gemv(x), po.abs_dot(x)
+        yy = y.cpu().numpy().astype(np.float64)
+        assert (np.abs(yy - ref) <= TOL_REL * scale + TOL_ABS).all()
+    assert_clean()
+
+
+@pytest.mark.parametrize("elem", [nwc.BF16, nwc.FP8])
+def test_gemv_list_mixed_shapes_and_many_items(elem):
+    """Ragged rows and columns, single-block and one-column-block items, and 200 small items, so
+    that CTA ranges cross many item boundaries (a table copy each): every y equals nwc_gemv's bit
+    for bit and the oracle's within tolerance."""
+    rng = np.random.default_rng(3 + elem)
+    shapes = [(1, 1), (7, 9), (9, 513), (17, 1100), (64, 512), (130, 2049), (4095, 4100), (300, 1030)]
+    shapes += [(int(rng.integers(1, 40)), int(rng.integers(1, 1600))) for _ in range(192)]
+    items = []
+    for i, s in enumerate(shapes):
+        w = synth.normal_bf16(s, 0.02, seed=900 + i)
+        items.append((nwc.encode(w, elem=elem), synth.activations_bf16(s[1], 901 + i)))
+    mats, xs, ys = _list_run(items)
+    torch.cuda.synchronize()
+    assert_clean()
+    for (blob, x), mat, xd, y in zip(items, mats, xs, ys):
+        assert torch.equal(y.view(torch.int32), mat.gemv(xd).view(torch.int32))
+        ref, scale = oracle.gemv(blob, x), oracle.abs_dot(blob, x)
+        yy = y.cpu().numpy().astype(np.float64)
+        assert (np.abs(yy - ref) <= TOL_REL * scale + TOL_ABS).all()
+    assert_clean()
+
+
+def test_gemv_list_repeats_in_a_graph_and_checks_arguments():
+    """The list launch leaves every workspace prepared: graph replays give the same bits. Bad
+    lists are rejected before any launch."""
+    items = [(nwc.encode(synth.normal_bf16((520, 1500), 0.02, seed=i)), synth.activations_bf16(1500, i))
+             for i in range(3)]
+    mats, xs, ys = _list_run(items)
+    torch.cuda.synchronize()
+    first = [y.clone() for y in ys]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nwc.gemv_list(list(zip(mats, xs, ys)), stream=s)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert all(torch.equal(a.view(torch.int32), b.view(torch.int32)) for a, b in zip(ys, first))
+    assert_clean()
+    import ctypes
+    L = nwc.lib()
+    arr = (nwc.NwcGemvItem * 2)()
+    for i in range(2):
+        arr[i].m = ctypes.pointer(mats[i].m)
+        arr[i].x = xs[i].data_ptr()
+        arr[i].y = ys[i].data_ptr()
+        arr[i].ws = mats[0].workspace.data_ptr()  # both items on one workspace
+        arr[i].ws_bytes = mats[0].ws_bytes
+    st = torch.cuda.current_stream().cuda_stream
+    assert L.nwc_gemv_list(arr, 2, ctypes.c_void_p(st)) == 1
+    assert L.nwc_gemv_list(arr, 0, ctypes.c_void_p(st)) == 1
+    assert L.nwc_gemv_list(arr, 257, ctypes.c_void_p(st)) == 1
+    fp8 = nwc.Matrix(nwc.encode(synth.normal_bf16((16, 600), 0.02, seed=5), elem=nwc.FP8))
+    arr[1].m = ctypes.pointer(fp8.m)  # mixed element types
+    arr[1].ws = fp8.workspace.data_ptr()
+    arr[1].ws_bytes = fp8.ws_bytes
+    assert L.nwc_gemv_list(arr, 2, ctypes.c_void_p(st)) == 1
+    notable = nwc.Matrix(items[0][0], table=False)  # no device decode table
+    arr[0].m = ctypes.pointer(notable.m)
+    arr[0].ws = notable.workspace.data_ptr()
+    assert L.nwc_gemv_list(arr, 1, ctypes.c_void_p(st)) == 1
