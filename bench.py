@@ -504,8 +504,8 @@ def run_batch_only(args):
 def run_only(args):
     """One workload of the pages' configurations alone (few launches, for profiling): the
     lm_head GEMV of the 151936x2560 table, the gather of 4096 ids from it, the fp8 gate / down
-    GEMV (12 rotated copies) or the odd 4095x4100 BF16 GEMV (24 rotated copies). One JSON line,
-    not the benchmark contract's."""
+    GEMV (12 rotated copies), the odd 4095x4100 BF16 GEMV (24 rotated copies) or the 24 rotated
+    4096x4096 copies as one nwc_gemv_list launch. One JSON line, not the benchmark contract's."""
     import torch
     import decode_gemv_nwc_gb300 as nwc
     from decode_gemv_nwc_gb300 import build, synth
@@ -533,6 +533,18 @@ def run_only(args):
             ms = time_graph(lambda: m.gather(ids, out=g, stream=stream), stream, args.steps, args.warmup)
             out = {"workload": "gather 4096 ids from the 151936x2560 table", "us": ms * 1e3,
                    "rows_per_s": 4096 / (ms * 1e-3)}
+    elif name == "list4096":
+        w = synth.normal_bf16((N_ROWS, K_COLS), 0.02, seed=0)
+        blob = nwc.encode(w)
+        host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+        mats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(COPIES)]
+        x = torch.from_numpy(synth.activations_bf16(K_COLS, 1).view(np.int16)).to(dev)
+        ys = torch.empty((COPIES, N_ROWS), dtype=torch.float32, device=dev)
+        items = [(mm, x, ys[i]) for i, mm in enumerate(mats)]
+        ms = time_graph(lambda: nwc.gemv_list(items, stream=stream), stream, args.steps, args.warmup) / COPIES
+        gbs = len(blob) / (ms * 1e-3) / 1e9
+        out = {"workload": "24 rotated 4096x4096 copies as one nwc_gemv_list launch", "us_per_matrix": ms * 1e3,
+               "compressed_gbs": gbs, "frac_of_hbm": gbs / peak}
     elif name == "odd":
         w = synth.normal_bf16((4095, 4100), 0.02, 1, device=dev)
         blob = encode_on_host(w)
@@ -574,7 +586,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--only-batch", type=int, default=0, metavar="NB",
                     help="time only nwc_gemv_batch with NB vectors on the headline matrix")
-    ap.add_argument("--only", choices=["lm_head", "gather", "fp8_gate", "fp8_down", "odd"],
+    ap.add_argument("--only", choices=["lm_head", "gather", "fp8_gate", "fp8_down", "odd", "list4096"],
                     help="time only this workload (few launches; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

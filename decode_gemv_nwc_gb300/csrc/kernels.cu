@@ -144,8 +144,9 @@ constexpr int kLutEntries = 1 << kPeek;
 constexpr int kLutBytes = kLutEntries * 4;
 static_assert(kLutEntries == NWC_TABLE_ENTRIES && kLutBytes == NWC_TABLE_BYTES, "decode table size");
 // A lane's fast decoder consumes at most 64 x 13 = 832 bits (every table entry's length is at
-// most 13), so its window takes in at most 26 words after the first two and reads one word
-// ahead: at most 29 words (116 bytes) from its first code word, whatever the code bits.
+// most 13); its window moves on by a word only after 32 of them, so it takes in at most 26
+// words after the first two and reads one word ahead: at most 29 words (116 bytes) from its
+// first code word, whatever the code bits.
 // Validation caps a lane at 26 words, so every lane's reads stay below 32 + 31 * 26 * 4 + 116
 // = 3372 bytes of its stage; raw and list reads stay inside the region. The slack after the
 // last stage is kept for good measure.
@@ -204,13 +205,13 @@ __device__ __forceinline__ bool lut_ready(const Mat &m, uint32_t lut_bar) {
 }
 
 // ------------------------------------------------------------------ the lane decoder
-// Window state in registers: window wh:wl (most significant bit = next stream bit); V holds
-// (valid bits - 1) in its low 7 bits (at most 64 bits are buffered), so whole table entries,
-// whose bits 5..6 are zero and whose low five bits are the pair's length, can be subtracted
-// from it; pa = shared-memory address of the next word to insert, nw = that word (loaded one
-// refill ahead, off the decode chain).
+// Window state in registers: the 64 stream bits wh:wl (most significant bit first) and the
+// offset o of the next unread bit in them; pa = shared-memory address of the next word to
+// insert, nw = that word (loaded one refill ahead, off the decode chain). Whole table entries
+// are added to o: their low five bits are the pair's length and bits 5..6 are zero, and o stays
+// below 64, so o's low six bits are exact and the bits above them are ignored.
 struct Fs {
-    uint32_t wh, wl, V, pa, nw;
+    uint32_t wh, wl, o, pa, nw;
 };
 
 // First two words of a lane's stream at shared address `code` (lw words).
@@ -218,48 +219,50 @@ __device__ __forceinline__ void fs_init(Fs &s, uint32_t code, uint32_t lw) {
     s.wh = lw > 0 ? lds32(code) : 0u;
     s.wl = lw > 1 ? lds32(code + 4) : 0u;
     s.pa = code + 8;
-    s.V = 63u;
+    s.o = 0u;
     s.nw = lds32(s.pa);
 }
 
-// Branch-free refill: when at most 32 bits are valid, the next word goes right below them by a
-// multiply-add with 2^(32 - valid) (the pages refill with one wide multiply-add; here it is
-// split into its low and high halves: the bits below the valid ones are zero, so no carry
-// crosses); otherwise the multiplier is 0. Leaves at least 33 valid bits: two row pairs.
+// Before every second row pair: once the offset has passed the first word, the window moves on
+// by a word (wh:wl <- wl:nw). Leaves o < 32, so the window holds at least 33 unread bits: two
+// row pairs.
 __device__ __forceinline__ void fs_refill(Fs &s) {
     asm("{\n\t"
         ".reg .pred q;\n\t"
-        ".reg .u32 t, mul;\n\t"
-        "and.b32 t, %3, 127;\n\t"
-        "shf.r.clamp.b32 mul, 0x80000000, 0, t;\n\t"
-        "setp.ne.u32 q, mul, 0;\n\t"
-        "mad.lo.u32 %1, %4, mul, %1;\n\t"
-        "mad.hi.u32 %0, %4, mul, %0;\n\t"
-        "@q add.u32 %2, %2, 4;\n\t"
-        "@q add.u32 %3, %3, 32;\n\t"
-        "@q ld.shared.u32 %4, [%2];\n\t"
+        ".reg .u32 t;\n\t"
+        "and.b32 t, %2, 32;\n\t"
+        "setp.ne.u32 q, t, 0;\n\t"
+        "@q mov.b32 %0, %1;\n\t"
+        "@q mov.b32 %1, %4;\n\t"
+        "@q xor.b32 %2, %2, 32;\n\t"
+        "@q add.u32 %3, %3, 4;\n\t"
+        "@q ld.shared.u32 %4, [%3];\n\t"
         "}"
-        : "+r"(s.wh), "+r"(s.wl), "+r"(s.pa), "+r"(s.V), "+r"(s.nw));
+        : "+r"(s.wh), "+r"(s.wl), "+r"(s.o), "+r"(s.pa), "+r"(s.nw));
 }
 
-// One row pair: the table entry of the next 13 bits, and the window advanced past the pair.
+// One row pair: the table entry of the next 13 bits; the offset moves past the pair.
 __device__ __forceinline__ uint32_t fs_pair(Fs &s, uint32_t lutb) {
     uint32_t e;
-    asm volatile("{\n\t.reg .u32 a;\n\tshr.u32 a, %1, 19;\n\tmad.lo.u32 a, a, 4, %2;\n\tld.shared.u32 %0, [a];\n\t}"
+    asm volatile("{\n\t.reg .u32 a, h, n;\n\t.reg .b64 w;\n\t"
+                 "and.b32 n, %3, 63;\n\t"
+                 "mov.b64 w, {%2, %1};\n\t"
+                 "shl.b64 w, w, n;\n\t"
+                 "mov.b64 {a, h}, w;\n\t"
+                 "shr.u32 a, h, 19;\n\t"
+                 "mad.lo.u32 a, a, 4, %4;\n\t"
+                 "ld.shared.u32 %0, [a];\n\t}"
                  : "=r"(e)
-                 : "r"(s.wh), "r"(lutb));
-    const uint32_t h = __funnelshift_l(s.wl, s.wh, e);
-    s.wl = __funnelshift_l(0u, s.wl, e);
-    s.wh = h;
-    s.V -= e;
+                 : "r"(s.wh), "r"(s.wl), "r"(s.o), "r"(lutb));
+    s.o += e;
     return e;
 }
 
-// Whether the lane consumed more bits than its lw words hold (a malformed stream).
+// Whether the lane consumed more bits than its lw words hold (a malformed stream): the window
+// holds the two words before pa, o bits of them read.
 __device__ __forceinline__ bool fs_overrun(const Fs &s, uint32_t code, uint32_t lw) {
-    const uint32_t valid = (s.V & 127u) + 1u;
-    const uint32_t inserted = (s.pa - code) * 8u;
-    return inserted - valid > 32u * lw;
+    const uint32_t consumed = (s.pa - code) * 8u - 64u + (s.o & 63u);
+    return consumed > 32u * lw;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
