@@ -60,9 +60,25 @@ namespace {
 constexpr uint32_t kErrFormat = 1u, kErrId = 2u, kErrTimeout = 4u;
 constexpr uint32_t kSentinel = 0xFFFFFFFFu;  // an empty partial-sum slot (no float sum has these bits)
 
+// floor(n / d) for 0 <= n < 2^31 by one wide multiply and a shift: m = ceil(2^(31+l) / d) with
+// l = ceil(log2 d) fits 32 bits, and (n m) >> (31 + l) is exact for every such n (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994, theorem 4.2, with
+// 31-bit dividends). Block indices stay below 2^31 (validation bounds the block count), so every
+// per-block division by the column-block count takes this form.
+struct Div {
+    uint32_t m, s;
+};
+Div make_div(uint64_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) l++;
+    return Div{(uint32_t)(((1ull << (31 + l)) + d - 1) / d), 31u + l};
+}
+__device__ __forceinline__ uint32_t div_q(uint32_t n, Div v) { return (uint32_t)(((uint64_t)n * v.m) >> v.s); }
+
 struct Mat {
     int elem, nr;
     uint64_t n, k, rbs, cbs, nb;
+    Div cdiv;  // division by cbs
     const uint32_t *tab;
     const uint8_t *data;
     const float *scales;
@@ -79,6 +95,7 @@ Mat to_mat(const nwc_matrix &m) {
     t.rbs = (uint64_t)m.row_blocks;
     t.cbs = (uint64_t)m.col_blocks;
     t.nb = t.rbs * t.cbs;
+    t.cdiv = make_div(t.cbs);
     t.tab = m.block_tab;
     t.data = m.data;
     t.scales = m.scales;
@@ -854,7 +871,8 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
         }
         const uint32_t bytes = 16 * (c1 - c0);
         const uint8_t *src = m.data + 16 * (uint64_t)c0;
-        const uint64_t rb = b / m.cbs, cb = b % m.cbs;
+        const uint32_t rb32 = div_q((uint32_t)b, m.cdiv);
+        const uint64_t rb = rb32, cb = b - (uint64_t)rb32 * m.cbs;
         const int rows = real_rows(m.n, rb);
         const uint64_t kc64 = m.k - cb * kCols;
         const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
@@ -942,6 +960,7 @@ struct ListItem {
     float *partial;
     uint32_t *counters;
     uint64_t n, k, cbs, n_pad, start;  // start: the item's first block in the list's numbering
+    Div cdiv;                          // division by cbs
 };
 struct ListParams {
     uint64_t total;  // blocks of all items
@@ -1056,7 +1075,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
                 if (nxt < end) l2_prefetch(it.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
             }
             const uint32_t bytes = 16 * (c1 - c0);
-            const uint64_t bi = b - it.start, rb = bi / it.cbs, cb = bi % it.cbs;
+            const uint64_t bi = b - it.start;
+            const uint32_t rb32 = div_q((uint32_t)bi, it.cdiv);
+            const uint64_t rb = rb32, cb = bi - (uint64_t)rb32 * it.cbs;
             const int rows = real_rows(it.n, rb);
             const uint64_t kc64 = it.k - cb * kCols;
             const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;
@@ -1757,10 +1778,10 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
         if (MODE == 0) {
             b = it;
             want = -1;
-            orow = (it / m.cbs) * kRows;
+            orow = (uint64_t)div_q((uint32_t)it, m.cdiv) * kRows;
             ok = true;
         } else {
-            const uint64_t i = it / m.cbs, cb = it % m.cbs;
+            const uint64_t i = div_q((uint32_t)it, m.cdiv), cb = it - i * m.cbs;
             int32_t id = 0;
             if (lane == 0) id = ids[i];
             id = __shfl_sync(0xFFFFFFFFu, id, 0);
@@ -1826,7 +1847,7 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
                 l2_prefetch(m.data + 16 * (uint64_t)s0, 16 * (s1 - s0));
             }
         }
-        const uint64_t cb = it % m.cbs;
+        const uint64_t cb = it - (uint64_t)div_q((uint32_t)it, m.cdiv) * m.cbs;
         const uint64_t colb = cb * kCols;
         if (!ok) {
             // gather id out of range: a zero row, and the error word
@@ -1841,7 +1862,7 @@ __global__ void __launch_bounds__(UnpackCfg<MODE>::kWarps * 32, 1)
             const uint8_t *src;
             uint32_t bytes;
             region(b, src, bytes);
-            const uint64_t rb = b / m.cbs;
+            const uint64_t rb = div_q((uint32_t)b, m.cdiv);
             const int rows = real_rows(m.n, rb);
             const uint64_t kc64 = m.k - cb * kCols;
             const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;  // the block's real columns
@@ -2005,6 +2026,8 @@ extern "C" nwc_status nwc_gather(const nwc_matrix *mp, const int32_t *ids, int64
     if (n_ids == 0) return NWC_OK;
     if (!ids || !out) return NWC_ERR_INVALID_ARG;
     const Mat m = to_mat(*mp);
+    // work items (id, column block) are numbered below 2^31
+    if ((uint64_t)n_ids >= ((1ull << 31) - 1) / m.cbs) return NWC_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int vec = vec_ok(out, ld_out, m.elem);
     const uint64_t items = (uint64_t)n_ids * m.cbs;
@@ -2138,6 +2161,7 @@ extern "C" nwc_status nwc_gemv_list(const nwc_gemv_item *items, int count, nwc_s
         d.n = (uint64_t)m.n;
         d.k = (uint64_t)m.k;
         d.cbs = (uint64_t)m.col_blocks;
+        d.cdiv = make_div(d.cbs);
         d.n_pad = pad_rows(m);
         d.start = p.total;
         p.total += (uint64_t)m.row_blocks * (uint64_t)m.col_blocks;

@@ -307,7 +307,8 @@ nwc_status nwc_gemv_batch(const nwc_matrix *m, const uint16_t *x, int64_t ld_x, 
  * bit-exact (uint16 BF16 or uint8 e4m3), out[i*ld_out + k]. An id outside [0, N) writes a
  * zero row and raises the device error word. Every id decodes its whole 8-row block row (the
  * format's unit), so a gather costs about 8x the bytes of the rows it returns. Store alignment
- * as for nwc_decode.
+ * as for nwc_decode. n_ids x ceil(K / 512) must stay below 2^31 (NWC_ERR_INVALID_ARG otherwise;
+ * the output of such a call would not fit in device memory anyway).
  */
 nwc_status nwc_gather(const nwc_matrix *m, const int32_t *ids, int64_t n_ids, void *out,
                       int64_t ld_out, nwc_stream stream);
