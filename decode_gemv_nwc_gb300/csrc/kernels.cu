@@ -423,13 +423,19 @@ __device__ __forceinline__ void st_relaxed(float *p, uint32_t v) {
 __device__ __forceinline__ uint32_t canon(float f) { return f != f ? 0x7FC00000u : __float_as_uint(f); }
 
 // Row block rb done for NB vectors (sum[v] in the lanes that transpose_reduce left it in):
-// one column block writes y directly; otherwise every warp stores its partial sums, takes a
-// ticket and loads the other column blocks' partials of its row block in the same round trip
-// (lane i: row i % 8, column blocks i / 8, i / 8 + 4, ...); the warp that took the last ticket
-// adds them in that fixed order (a slot still holding the sentinel is loaded again, a bounded
-// number of times), writes y (times the row scale for fp8), and puts the sentinels and the
-// counter back for the next call. Partial slots: partial[(v cbs + cb) n_pad + row].
-template <int ELEM, int NB>
+// one column block writes y directly; otherwise every warp stores its partial sums and takes a
+// ticket, and the warp that took the last ticket loads the other column blocks' partials of its
+// row block (lane i: row i % 8, column blocks i / 8, i / 8 + 4, ...), adds them in that fixed
+// order, writes y (times the row scale for fp8), and puts the sentinels and the counter back for
+// the next call. Two ways to reach the loads, with the same sums bit for bit:
+//   SPEC: every warp loads the other partials while its (relaxed) ticket is in flight, so the
+//     last warp usually has them at once; a slot still holding the sentinel is loaded again (a
+//     bounded number of times). Best when warps have further blocks to decode meanwhile.
+//   otherwise: the ticket is an acquire-release atomic after a warp barrier (the writer lanes'
+//     stores precede it), and only the last warp loads, after it; far fewer loads reach L2 at a
+//     launch's end, which is what a launch with at most one block per warp waits for.
+// Partial slots: partial[(v cbs + cb) n_pad + row].
+template <int ELEM, int NB, bool SPEC>
 __device__ __forceinline__ void finish_rows(const Mat &m, const float (&sum)[NB], int lane, uint64_t rb, uint64_t cb,
                                             float *y, int64_t ld_y, float *partial, uint32_t *counters,
                                             uint64_t n_pad, bool &timed_out) {
@@ -444,23 +450,35 @@ __device__ __forceinline__ void finish_rows(const Mat &m, const float (&sum)[NB]
     const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
     const bool live = r2 < m.n;
     const uint64_t c0 = (uint64_t)(lane >> 3);
-    constexpr int kSpec = 4;  // speculative loads per lane: column blocks up to 16
+    constexpr int kSpec = 4;  // loads per lane in one round: column blocks up to 16
 #pragma unroll
     for (int v = 0; v < NB; v++)
         if (writer) st_relaxed(partial + ((uint64_t)v * m.cbs + cb) * n_pad + row, canon(sum[v]));
     uint32_t pv[NB][kSpec];
+    auto load_round = [&]() {
 #pragma unroll
-    for (int v = 0; v < NB; v++)
+        for (int v = 0; v < NB; v++)
 #pragma unroll
-        for (int q = 0; q < kSpec; q++) {
-            const uint64_t c2 = c0 + 4 * q;
-            pv[v][q] = kSentinel;
-            if (live && c2 < m.cbs && c2 != cb) pv[v][q] = ld_relaxed(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
-        }
+            for (int q = 0; q < kSpec; q++) {
+                const uint64_t c2 = c0 + 4 * q;
+                pv[v][q] = kSentinel;
+                if (live && c2 < m.cbs && c2 != cb) pv[v][q] = ld_relaxed(partial + ((uint64_t)v * m.cbs + c2) * n_pad + r2);
+            }
+    };
     uint32_t ticket = 0;
-    if (lane == 0) asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
+    if (SPEC) {
+        load_round();
+        if (lane == 0) asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
+    } else {
+        __syncwarp();
+        if (lane == 0) asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(counters + rb) : "memory");
+    }
     ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
     if (ticket != (uint32_t)m.cbs - 1) return;
+    if (!SPEC) {
+        __syncwarp();  // lane 0's acquire precedes every lane's loads
+        load_round();
+    }
     float own[NB];
 #pragma unroll
     for (int v = 0; v < NB; v++) own[v] = __shfl_sync(0xFFFFFFFFu, sum[v], row_holder(lane & 7));
@@ -793,7 +811,7 @@ __device__ __forceinline__ void prefetch_share(const Prefetch &pf, uint64_t w, u
     }
 }
 
-template <int ELEM, int NB, bool KR = false>
+template <int ELEM, int NB, bool KR, bool SPEC>
 __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     gemv_kernel(Mat m, const uint16_t *__restrict__ x, int64_t ld_x, float *__restrict__ y, int64_t ld_y,
                 float *partial, uint32_t *counters, uint64_t n_pad, Prefetch pf) {
@@ -920,7 +938,7 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
         float sum[NB];
 #pragma unroll
         for (int v = 0; v < NB; v++) sum[v] = transpose_reduce(acc[v], lane);
-        finish_rows<ELEM, NB>(m, sum, lane, rb, cb, y, ld_y, partial, counters, n_pad, timed_out);
+        finish_rows<ELEM, NB, SPEC>(m, sum, lane, rb, cb, y, ld_y, partial, counters, n_pad, timed_out);
         __syncwarp();
         c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
         c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
@@ -969,7 +987,7 @@ struct ListParams {
 };
 static_assert(sizeof(ListParams) <= 32764, "kernel parameters");
 
-template <int ELEM, bool KR = false>
+template <int ELEM, bool KR, bool SPEC>
 __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __grid_constant__ ListParams p) {
     using S = Smem<kGemvWarps>;
     constexpr uint64_t W = kGemvWarps;
@@ -1115,7 +1133,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
                 gemv_block_global<ELEM, 1>(it.data + 16 * (uint64_t)c0, bytes, lane, lutb, xb, 0, acc, bad, kc, rows);
             }
             float sum[1] = {transpose_reduce(acc[0], lane)};
-            finish_rows<ELEM, 1>(m, sum, lane, rb, cb, it.y, 0, it.partial, it.counters, it.n_pad, timed_out);
+            finish_rows<ELEM, 1, SPEC>(m, sum, lane, rb, cb, it.y, 0, it.partial, it.counters, it.n_pad, timed_out);
             __syncwarp();
             c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
             c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
@@ -2066,19 +2084,26 @@ extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws
 }
 
 namespace {
+template <int ELEM, int NB, bool KR, bool SPEC>
+cudaError_t launch_gemv_k(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, float *partial,
+                          uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int grid, cudaStream_t stream) {
+    using C = GemvCfg<NB>;
+    if (!smem_ready<gemv_kernel<ELEM, NB, KR, SPEC>>(C::kSmem)) return cudaErrorInvalidConfiguration;
+    return launch_pdl(gemv_kernel<ELEM, NB, KR, SPEC>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y,
+                      partial, counters, n_pad, pf);
+}
+
 template <int ELEM, int NB>
 cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, float *partial,
                            uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int sms, cudaStream_t stream) {
     using C = GemvCfg<NB>;
     const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
-    if (k_ragged(m)) {
-        if (!smem_ready<gemv_kernel<ELEM, NB, true>>(C::kSmem)) return cudaErrorInvalidConfiguration;
-        return launch_pdl(gemv_kernel<ELEM, NB, true>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y,
-                          partial, counters, n_pad, pf);
-    }
-    if (!smem_ready<gemv_kernel<ELEM, NB, false>>(C::kSmem)) return cudaErrorInvalidConfiguration;
-    return launch_pdl(gemv_kernel<ELEM, NB, false>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y, partial,
-                      counters, n_pad, pf);
+    const bool spec = m.nb > (uint64_t)grid * C::kWarps;  // some warps decode more than one block
+    if (k_ragged(m))
+        return spec ? launch_gemv_k<ELEM, NB, true, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream)
+                    : launch_gemv_k<ELEM, NB, true, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream);
+    return spec ? launch_gemv_k<ELEM, NB, false, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream)
+                : launch_gemv_k<ELEM, NB, false, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream);
 }
 
 // The GEMV for nb = 1 or 2 vectors on `partial` (nb x col_blocks x n_pad floats, sentinels) and
@@ -2124,10 +2149,16 @@ extern "C" nwc_status nwc_gemv(const nwc_matrix *mp, const uint16_t *x, float *y
 
 // ---------------------------------------------------------------- GEMV list
 namespace {
+template <int ELEM, bool KR, bool SPEC>
+cudaError_t launch_list_k(const ListParams &p, int grid, cudaStream_t s) {
+    if (!smem_ready<gemv_list_kernel<ELEM, KR, SPEC>>(kGemvSmem)) return cudaErrorInvalidConfiguration;
+    return launch_pdl(gemv_list_kernel<ELEM, KR, SPEC>, grid, kGemvWarps * 32, kGemvSmem, s, p);
+}
 template <int ELEM, bool KR>
 cudaError_t launch_list(const ListParams &p, int grid, cudaStream_t s) {
-    if (!smem_ready<gemv_list_kernel<ELEM, KR>>(kGemvSmem)) return cudaErrorInvalidConfiguration;
-    return launch_pdl(gemv_list_kernel<ELEM, KR>, grid, kGemvWarps * 32, kGemvSmem, s, p);
+    // some warps decode more than one block: the final sums' speculative loads (finish_rows)
+    return p.total > (uint64_t)grid * kGemvWarps ? launch_list_k<ELEM, KR, true>(p, grid, s)
+                                                 : launch_list_k<ELEM, KR, false>(p, grid, s);
 }
 }  // namespace
 
