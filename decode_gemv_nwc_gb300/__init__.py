@@ -304,7 +304,9 @@ class Matrix:
 
     def dequantize(self, out=None, stream=None):
         """fp8 matrices: BF16 weights [N, K] (int16 bits), each the BF16 nearest to e4m3(q) * s_n
-        (nwc_decode to e4m3 bytes and scales, then nwc_dequantize_fp8)."""
+        (nwc_decode to e4m3 bytes and scales, then nwc_dequantize_fp8). The e4m3 bytes and scales
+        pass through one scratch pair kept by this Matrix, so calls on the same Matrix must be
+        ordered on one stream (calls on different streams that overlap would overwrite it)."""
         import torch
         assert self.elem == FP8, "dequantize serves fp8 matrices"
         dev = self.device_blob.device
@@ -324,7 +326,8 @@ class Matrix:
         """Batch > 1 (prefill): Y[B, N] = X[B, K] W^T in BF16. The matrix is decoded into a BF16
         scratch (allocated once and kept unless given; fp8 matrices are dequantized into it) and
         multiplied by cuBLAS through torch: the pages' prefill (weights back to BF16, then a BF16
-        GEMM)."""
+        GEMM). The kept scratch is shared by every call on this Matrix: order such calls on one
+        stream, or pass each stream its own scratch."""
         import torch
         if scratch is None:
             scratch = getattr(self, "_scratch", None)

@@ -99,6 +99,17 @@ def test_validate_rejects_corruption():
     assert bad(all_lanes_26) == 2
     assert bad(lambda b: b.__setitem__(off_data + 3, 27)) == 2            # > 26 words (64 pairs x 13 bits)
     assert nwc.validate(bytes(blob) + b"\0" * 16) == 2       # trailing bytes
+    # a header whose row blocks x column blocks wraps 64 bits (2^33 x 2^31 = 2^64 -> 0): rejected
+    # before the product is formed, whatever block count it claims
+    def huge(nb):
+        def f(b):
+            b[8:16] = np.array([1 << 36], "<u8").tobytes()
+            b[16:24] = np.array([(1 << 40) - 1], "<u8").tobytes()
+            b[24:32] = np.array([nb], "<u8").tobytes()
+        return f
+    assert bad(huge(0)) == 2
+    assert bad(huge(1)) == 2
+    assert bad(huge((1 << 33) * (1 << 31) % (1 << 64))) == 2
 
 
 def test_validate_checks_escape_lists():
