@@ -1004,15 +1004,67 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
     while (f + 1 < p.count && p.items[f + 1].start <= s0) f++;
     int l = f;
     while (l + 1 < p.count && p.items[l + 1].start < s1) l++;
-    auto range_end = [&](int j) {
-        const uint64_t e = j + 1 < p.count ? p.items[j + 1].start : p.total;
-        return e < s1 ? e : s1;
-    };
     auto load_table = [&](int j) {
         mbar_expect_tx(lut_bar, kLutBytes);
 #pragma unroll
         for (int q = 0; q < 4; q++)
             tma_load_1d(lutb + q * (kLutBytes / 4), p.items[j].table + q * (kLutEntries / 4), kLutBytes / 4, lut_bar);
+    };
+
+    // The CTA's share of item j, [r0, r1) in the item's own block numbering, as work units taken
+    // by the warps in turn (warp w: units w, w + W, ...). The first L units are whole row blocks
+    // lying inside the share, L a multiple of W (every warp gets the same number): one warp
+    // decodes all of such a row block's column blocks and sums them itself, in the order the
+    // final sums of finish_rows use, so every y is bit for bit the same. The remaining units are
+    // single blocks (those of the row blocks cut by the share's ends, and of the whole row blocks
+    // left over), each with finish_rows' ticket; they keep the warps' shares within one block of
+    // each other.
+    // (block indices stay below 2^31, so the plan is kept in 32 bits)
+    struct Plan {
+        uint32_t r0, ra, L, nhead, single0, units, cbs;
+    };
+    auto plan_of = [&](int j) {
+        const ListItem &it = p.items[j];
+        const uint64_t e = j + 1 < p.count ? p.items[j + 1].start : p.total;
+        Plan q;
+        q.r0 = (uint32_t)((it.start > s0 ? it.start : s0) - it.start);
+        const uint32_t r1 = (uint32_t)((e < s1 ? e : s1) - it.start);
+        q.cbs = (uint32_t)it.cbs;
+        const uint32_t ra = div_q(q.r0 + q.cbs - 1, it.cdiv), rz = div_q(r1, it.cdiv);
+        const uint32_t whole = q.cbs > 1 && rz > ra ? rz - ra : 0;
+        q.L = whole / W * W;
+        if (q.L > 0) {
+            q.ra = ra;
+            q.nhead = ra * q.cbs - q.r0;
+            q.single0 = (ra + q.L) * q.cbs;
+        } else {
+            q.ra = 0;
+            q.nhead = r1 - q.r0;
+            q.single0 = r1;
+        }
+        q.units = q.L + q.nhead + (r1 - q.single0);
+        return q;
+    };
+    // A warp's walk through its units: step (u, k) is block k of unit u, in the item's block
+    // numbering; next() moves to the following step.
+    struct Walk {
+        uint32_t u, k, b;
+    };
+    auto at = [&](const Plan &q, uint32_t u, uint32_t k) -> Walk {
+        Walk w;
+        w.u = u;
+        w.k = k;
+        if (u < q.L) {
+            w.b = (q.ra + u) * q.cbs + k;
+        } else {
+            const uint32_t e = u - q.L;
+            w.b = e < q.nhead ? q.r0 + e : q.single0 + (e - q.nhead);
+        }
+        return w;
+    };
+    auto next = [&](const Plan &q, const Walk &w) -> Walk {
+        if (w.u < q.L && w.k + 1 < q.cbs) return Walk{w.u, w.k + 1, w.b + 1};
+        return at(q, w.u + (uint32_t)W, 0);
     };
 
     uint32_t phase = 0;
@@ -1029,23 +1081,26 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
         }
     };
     // Bounds of the warp's current block (c0/c1, every lane) and of its next one (n0/n1, lane 0),
-    // for the warp's first block of item j.
+    // for the warp's first step in item j.
     uint32_t c0 = 0, c1 = 0, n0 = 0, n1 = 0;
     auto first_bounds = [&](int j) {
         const ListItem &it = p.items[j];
-        const uint64_t beg = it.start > s0 ? it.start : s0, end = range_end(j), b = beg + (uint64_t)warp;
+        const Plan q = plan_of(j);
+        const Walk w0 = at(q, (uint32_t)warp, 0);
         c0 = c1 = n0 = n1 = 0;
-        if (lane == 0 && b < end) {
-            c0 = it.tab[b - it.start];
-            c1 = it.tab[b - it.start + 1];
-        }
-        if (lane == 0 && b + W < end) {
-            n0 = it.tab[b + W - it.start];
-            n1 = it.tab[b + W - it.start + 1];
+        const bool have = w0.u < q.units;
+        if (lane == 0 && have) {
+            c0 = it.tab[w0.b];
+            c1 = it.tab[w0.b + 1];
+            const Walk w1 = next(q, w0);
+            if (w1.u < q.units) {
+                n0 = it.tab[w1.b];
+                n1 = it.tab[w1.b + 1];
+            }
         }
         c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
         c1 = __shfl_sync(0xFFFFFFFFu, c1, 0);
-        return b < end;
+        return have;
     };
 
     // the warp's barrier and first copy, and the first item's table, before anything else
@@ -1070,7 +1125,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
         m.n = it.n;
         m.cbs = it.cbs;
         m.scales = it.scales;
-        const uint64_t beg = it.start > s0 ? it.start : s0, end = range_end(j);
+        const Plan q = plan_of(j);
         if (j > f) {
             __syncthreads();  // every warp is done with the previous table
             if (threadIdx.x == 0) {
@@ -1081,21 +1136,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
             }
         }
         bool lut_ok = false;
-        uint64_t b = beg + (uint64_t)warp;
-        while (b < end && !timed_out) {
-            const uint64_t nxt = b + W, nn = nxt + W;
-            uint32_t f0 = 0, f1 = 0;  // bounds of block nn, for the next iteration
+        float sloc = 0.0f;  // a whole row block's sum so far (lane i: column blocks i / 8 mod 4)
+        Walk w = at(q, (uint32_t)warp, 0), w1 = next(q, w), w2 = next(q, w1);
+        while (w.u < q.units && !timed_out) {
+            const bool has1 = w1.u < q.units, has2 = w2.u < q.units;
+            uint32_t f0 = 0, f1 = 0;  // bounds of the step after next, for the next iteration
             if (lane == 0) {
-                if (nn < end) {
-                    f0 = it.tab[nn - it.start];
-                    f1 = it.tab[nn - it.start + 1];
+                if (has2) {
+                    f0 = it.tab[w2.b];
+                    f1 = it.tab[w2.b + 1];
                 }
-                if (nxt < end) l2_prefetch(it.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
+                if (has1) l2_prefetch(it.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
             }
             const uint32_t bytes = 16 * (c1 - c0);
-            const uint64_t bi = b - it.start;
-            const uint32_t rb32 = div_q((uint32_t)bi, it.cdiv);
-            const uint64_t rb = rb32, cb = bi - (uint64_t)rb32 * it.cbs;
+            const uint32_t rb32 = div_q(w.b, it.cdiv);
+            const uint64_t rb = rb32, cb = w.b - rb32 * q.cbs;
             const int rows = real_rows(it.n, rb);
             const uint64_t kc64 = it.k - cb * kCols;
             const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;
@@ -1133,14 +1188,28 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) gemv_list_kernel(const __g
                 gemv_block_global<ELEM, 1>(it.data + 16 * (uint64_t)c0, bytes, lane, lutb, xb, 0, acc, bad, kc, rows);
             }
             float sum[1] = {transpose_reduce(acc[0], lane)};
-            finish_rows<ELEM, 1, SPEC>(m, sum, lane, rb, cb, it.y, 0, it.partial, it.counters, it.n_pad, timed_out);
+            if (w.u >= q.L) {
+                finish_rows<ELEM, 1, SPEC>(m, sum, lane, rb, cb, it.y, 0, it.partial, it.counters, it.n_pad, timed_out);
+            } else {
+                const float v = __shfl_sync(0xFFFFFFFFu, sum[0], row_holder(lane & 7));
+                if ((uint32_t)(cb & 3u) == (uint32_t)(lane >> 3)) sloc += v;
+                if (cb + 1 == it.cbs) {
+                    sloc += __shfl_xor_sync(0xFFFFFFFFu, sloc, 8);
+                    sloc += __shfl_xor_sync(0xFFFFFFFFu, sloc, 16);
+                    const uint64_t r2 = rb * kRows + (uint64_t)(lane & 7);
+                    if (lane < kRows && r2 < it.n) it.y[r2] = ELEM == 0 ? sloc : sloc * it.scales[r2];
+                    sloc = 0.0f;
+                }
+            }
             __syncwarp();
             c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
             c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
-            if (nxt < end) issue(it.data, c0, c1, true);
+            if (has1) issue(it.data, c0, c1, true);
             n0 = f0;
             n1 = f1;
-            b = nxt;
+            w = w1;
+            w1 = w2;
+            w2 = next(q, w2);
         }
         // the warp's first copy of the next item goes out before the barrier
         if (j < l && first_bounds(j + 1) && !timed_out) issue(p.items[j + 1].data, c0, c1, true);
