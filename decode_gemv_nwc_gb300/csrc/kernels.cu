@@ -2175,12 +2175,56 @@ cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float 
                 : launch_gemv_k<ELEM, NB, false, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream);
 }
 
+template <int ELEM, bool KR>
+cudaError_t launch_list(const ListParams &p, int grid, cudaStream_t s);
+
+// The list launch's parameters (28 KB) for the calling thread, kept off the stack.
+ListParams &list_params() {
+    static thread_local ListParams p;
+    return p;
+}
+// Item i of a list launch: matrix m with x, y and its workspace's partial sums and counters.
+void set_item(ListParams &p, int i, const Mat &m, const uint16_t *x, float *y, float *partial, uint32_t *counters,
+              uint64_t n_pad) {
+    ListItem &d = p.items[i];
+    d.tab = m.tab;
+    d.data = m.data;
+    d.scales = m.scales;
+    d.table = m.table;
+    d.x = x;
+    d.y = y;
+    d.partial = partial;
+    d.counters = counters;
+    d.n = m.n;
+    d.k = m.k;
+    d.cbs = m.cbs;
+    d.n_pad = n_pad;
+    d.start = p.total;
+    d.cdiv = m.cdiv;
+    p.total += m.nb;
+}
+
 // The GEMV for nb = 1 or 2 vectors on `partial` (nb x col_blocks x n_pad floats, sentinels) and
 // `counters` (row_blocks, zero); arguments already checked. next: the matrix to prefetch, or null.
 nwc_status launch_gemv(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, int nb, float *partial,
                        uint32_t *counters, uint64_t n_pad, cudaStream_t stream, const nwc_matrix *next = nullptr) {
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
+    // A tall matrix (every SM's share of the blocks holds at least 32 whole row blocks) runs the
+    // list kernel with one item: its whole row blocks are summed by one warp each, without partial
+    // sums, with the same y bit for bit (the list kernel needs the device decode table).
+    if (nb == 1 && !next && m.table && m.cbs > 1 && m.rbs >= 33 * (uint64_t)sms) {
+        ListParams &p = list_params();
+        p.count = 1;
+        p.total = 0;
+        set_item(p, 0, m, x, y, partial, counters, n_pad);
+        const int grid = sms;
+        const bool kr = k_ragged(m);
+        cudaError_t rc;
+        if (m.elem == NWC_ELEM_BF16) rc = kr ? launch_list<0, true>(p, grid, stream) : launch_list<0, false>(p, grid, stream);
+        else rc = kr ? launch_list<1, true>(p, grid, stream) : launch_list<1, false>(p, grid, stream);
+        return rc == cudaSuccess ? NWC_OK : NWC_ERR_CUDA;
+    }
     Prefetch pf = {nullptr, 0, nullptr, 0, nullptr};
     if (next && next->data && next->block_tab) {
         pf.data = next->data;
@@ -2233,7 +2277,7 @@ cudaError_t launch_list(const ListParams &p, int grid, cudaStream_t s) {
 
 extern "C" nwc_status nwc_gemv_list(const nwc_gemv_item *items, int count, nwc_stream stream) {
     if (!items || count < 1 || count > kListMax) return NWC_ERR_INVALID_ARG;
-    static thread_local ListParams p;  // 26 KB: kept off the stack
+    ListParams &p = list_params();
     std::vector<std::pair<uintptr_t, uintptr_t>> used;  // workspace bytes the items touch
     p.count = count;
     p.total = 0;
@@ -2249,22 +2293,8 @@ extern "C" nwc_status nwc_gemv_list(const nwc_gemv_item *items, int count, nwc_s
         if (elem >= 0 && m.elem != elem) return NWC_ERR_INVALID_ARG;
         elem = m.elem;
         kr |= (m.k % kCols) != 0;
-        ListItem &d = p.items[i];
-        d.tab = m.block_tab;
-        d.data = m.data;
-        d.scales = m.scales;
-        d.table = m.table;
-        d.x = it.x;
-        d.y = it.y;
-        d.partial = static_cast<float *>(it.ws);
-        d.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(it.ws) + ws_counter_off(m));
-        d.n = (uint64_t)m.n;
-        d.k = (uint64_t)m.k;
-        d.cbs = (uint64_t)m.col_blocks;
-        d.cdiv = make_div(d.cbs);
-        d.n_pad = pad_rows(m);
-        d.start = p.total;
-        p.total += (uint64_t)m.row_blocks * (uint64_t)m.col_blocks;
+        set_item(p, i, to_mat(m), it.x, it.y, static_cast<float *>(it.ws),
+                 reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(it.ws) + ws_counter_off(m)), pad_rows(m));
         if (m.col_blocks > 1) {
             const uintptr_t a = reinterpret_cast<uintptr_t>(it.ws);
             used.push_back({a, a + nwc_gemv_workspace_bytes(&m)});

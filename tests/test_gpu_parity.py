@@ -874,3 +874,20 @@ def test_gemv_list_repeats_in_a_graph_and_checks_arguments():
     arr[0].m = ctypes.pointer(notable.m)
     arr[0].ws = notable.workspace.data_ptr()
     assert L.nwc_gemv_list(arr, 1, ctypes.c_void_p(st)) == 1
+
+
+@pytest.mark.parametrize("elem", [nwc.BF16, nwc.FP8])
+def test_tall_matrix_through_the_list_kernel_equals_the_single_kernel(elem):
+    """A matrix tall enough that every SM's share holds 32 whole row blocks (41000 x 1030: ragged
+    K, three column blocks) runs nwc_gemv through the list kernel, whose whole row blocks are
+    summed by one warp each: y equals the single-matrix kernel's (the path taken without a device
+    decode table) bit for bit, and the oracle's within tolerance on every row."""
+    w = synth.normal_bf16((41000, 1030), 0.02, seed=77)
+    blob = nwc.encode(w, elem=elem)
+    x = synth.activations_bf16(1030, 78)
+    routed = nwc.Matrix(blob)
+    single = nwc.Matrix(blob, table=False)
+    y = gemv_check_all(blob, x, routed)
+    y_single = single.gemv(dev_bits(x)).cpu().numpy().astype(np.float64)
+    assert_clean()
+    assert np.array_equal(y.view(np.uint64), y_single.view(np.uint64))
