@@ -202,7 +202,9 @@ nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_
  * fused kernel): x is BF16[K] (16-byte
  * aligned), y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
  * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes: a workspace
- * prepared by nwc_gemv_prepare for this matrix.
+ * prepared by nwc_gemv_prepare for this matrix. Whatever the launch configuration (a tall
+ * matrix with a device decode table runs the kernel of nwc_gemv_list), the column blocks' sums
+ * are added in one fixed order, so results are bitwise repeatable.
  */
 nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                     nwc_stream stream);
