@@ -178,7 +178,7 @@ struct Smem {
     static constexpr int kEnd = kStage + W * kStageBytes;
 };
 constexpr int kGemvWarps = 32;
-constexpr int kGemv2Warps = 24;  // two vectors: a second accumulator set, up to 85 registers
+constexpr int kGemv2Warps = 28;  // two vectors: a second accumulator set, up to 72 registers
 constexpr int kGemvSmem = Smem<kGemvWarps>::kEnd + kStageSlack;
 constexpr int kGemv2Smem = Smem<kGemv2Warps>::kEnd + kStageSlack;
 static_assert(kGemvSmem <= 232448 && kGemv2Smem <= 232448, "shared memory per CTA");
