@@ -825,8 +825,9 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     const uint32_t bar = smem_u32(smem + S::kBar + 8 * warp), lut_bar = smem_u32(smem + S::kLutBar);
     const uint32_t stage = smem_u32(smem + S::kStage + warp * kStageBytes);
 
-    // Block b goes to CTA b % grid, so every SM gets within one block of the same count.
-    const uint64_t total_warps = (uint64_t)gridDim.x * C::kWarps;
+    // Block b goes to CTA b % grid, so every SM gets within one block of the same count. The CTA
+    // may have fewer warps than its shared memory is laid out for (the launch picks the count).
+    const uint64_t total_warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
     uint64_t b = (uint64_t)blockIdx.x + (uint64_t)gridDim.x * warp;
     uint32_t phase = 0;
     bool bad = false, timed_out = false, inflight = false;
@@ -2155,10 +2156,11 @@ extern "C" nwc_status nwc_gemv_prepare(const nwc_matrix *mp, void *ws, size_t ws
 namespace {
 template <int ELEM, int NB, bool KR, bool SPEC>
 cudaError_t launch_gemv_k(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, int64_t ld_y, float *partial,
-                          uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int grid, cudaStream_t stream) {
+                          uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int grid, int warps,
+                          cudaStream_t stream) {
     using C = GemvCfg<NB>;
     if (!smem_ready<gemv_kernel<ELEM, NB, KR, SPEC>>(C::kSmem)) return cudaErrorInvalidConfiguration;
-    return launch_pdl(gemv_kernel<ELEM, NB, KR, SPEC>, grid, C::kWarps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y,
+    return launch_pdl(gemv_kernel<ELEM, NB, KR, SPEC>, grid, warps * 32, C::kSmem, stream, m, x, ld_x, y, ld_y,
                       partial, counters, n_pad, pf);
 }
 
@@ -2167,12 +2169,17 @@ cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float 
                            uint32_t *counters, uint64_t n_pad, const Prefetch &pf, int sms, cudaStream_t stream) {
     using C = GemvCfg<NB>;
     const int grid = (int)(m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
-    const bool spec = m.nb > (uint64_t)grid * C::kWarps;  // some warps decode more than one block
+    // The fewest warps per CTA that keep the number of rounds (blocks per warp) of a full CTA, so
+    // that every warp of a round has a block: 6080 blocks on 152 SMs take 20 warps with two blocks
+    // each instead of 32 warps of which a quarter decode a second block alone.
+    const uint64_t rounds = cdiv(m.nb, (uint64_t)grid * C::kWarps);
+    const int warps = (int)cdiv(m.nb, rounds * (uint64_t)grid);
+    const bool spec = rounds > 1;  // some warps decode more than one block
     if (k_ragged(m))
-        return spec ? launch_gemv_k<ELEM, NB, true, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream)
-                    : launch_gemv_k<ELEM, NB, true, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream);
-    return spec ? launch_gemv_k<ELEM, NB, false, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream)
-                : launch_gemv_k<ELEM, NB, false, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, stream);
+        return spec ? launch_gemv_k<ELEM, NB, true, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, warps, stream)
+                    : launch_gemv_k<ELEM, NB, true, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, warps, stream);
+    return spec ? launch_gemv_k<ELEM, NB, false, true>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, warps, stream)
+                : launch_gemv_k<ELEM, NB, false, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, warps, stream);
 }
 
 template <int ELEM, bool KR>
