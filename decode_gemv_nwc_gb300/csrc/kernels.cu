@@ -1381,11 +1381,12 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
     const uint64_t start = (uint64_t)blockIdx.x * per;
     const uint64_t end = start + per < m.nb ? start + per : m.nb;
     const uint64_t cb_first = start / m.rbs;
+    const uint32_t warps = blockDim.x >> 5;
     uint64_t p = start + (uint64_t)warp;
     // (rb, cb) of position p, stepped without division; (rbn, cbn) of the next position
     uint64_t cb = p / m.rbs, rb = p % m.rbs;
     auto step = [&](uint64_t &r, uint64_t &c) {
-        r += kBatchWarps;
+        r += warps;
         while (r >= m.rbs) {
             r -= m.rbs;
             c += 1;
@@ -1460,7 +1461,7 @@ __global__ void __launch_bounds__(kBatchWarps * 32, 1)
 
     while (p < end && !timed_out) {
         const uint64_t b = rb * m.cbs + cb;
-        const uint64_t pn = p + kBatchWarps;
+        const uint64_t pn = p + warps;
         uint64_t rbn = rb, cbn = cb;
         step(rbn, cbn);
         const uint64_t bn = rbn * m.cbs + cbn;
@@ -2333,13 +2334,18 @@ cudaError_t launch_batch(const Mat &m, const uint16_t *x, int64_t ld_x, int nb, 
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     uint32_t *counters = reinterpret_cast<uint32_t *>(w8);
     float *partial = reinterpret_cast<float *>(w8 + (m.cbs > 1 ? up16(4 * m.rbs) : 0));
+    // a CTA's range of `per` positions takes r = ceil(per / kBatchWarps) rounds of its warps;
+    // the fewest warps that keep r rounds leave no warp of the last round decoding alone
+    const uint64_t per = (m.nb + (uint64_t)grid - 1) / (uint64_t)grid;
+    const uint64_t rounds = (per + kBatchWarps - 1) / kBatchWarps;
+    const int warps = rounds == 0 ? kBatchWarps : (int)((per + rounds - 1) / rounds);
     if (k_ragged(m)) {
         if (!smem_ready<gemv_batch_kernel<ELEM, true>>(kBatchSmem)) return cudaErrorInvalidConfiguration;
-        return launch_pdl(gemv_batch_kernel<ELEM, true>, grid, kBatchWarps * 32, kBatchSmem, s, m, x, ld_x, nb, y, ld_y,
+        return launch_pdl(gemv_batch_kernel<ELEM, true>, grid, warps * 32, kBatchSmem, s, m, x, ld_x, nb, y, ld_y,
                           partial, counters, n_pad);
     }
     if (!smem_ready<gemv_batch_kernel<ELEM, false>>(kBatchSmem)) return cudaErrorInvalidConfiguration;
-    return launch_pdl(gemv_batch_kernel<ELEM, false>, grid, kBatchWarps * 32, kBatchSmem, s, m, x, ld_x, nb, y, ld_y,
+    return launch_pdl(gemv_batch_kernel<ELEM, false>, grid, warps * 32, kBatchSmem, s, m, x, ld_x, nb, y, ld_y,
                       partial, counters, n_pad);
 }
 }  // namespace
