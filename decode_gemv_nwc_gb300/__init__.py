@@ -30,6 +30,7 @@ class NwcError(RuntimeError):
 
 
 LIST_MAX = 256  # NWC_GEMV_LIST_MAX: products per nwc_gemv_list call
+ROUTE_GEMV, ROUTE_CLUSTER, ROUTE_LIST = 0, 1, 2  # NWC_ROUTE_*: the kernel nwc_gemv launches
 
 
 class NwcMatrix(ctypes.Structure):
@@ -95,11 +96,12 @@ def lib():
     L.nwc_file_read.argtypes = [cp, i32, p, sz, ctypes.POINTER(sz)]
     L.nwc_file_load.argtypes = [cp, i32, p, sz, p, sz, ctypes.POINTER(NwcMatrix), p]
     L.nwc_gemv_list.argtypes = [ctypes.POINTER(NwcGemvItem), i32, p]
+    L.nwc_gemv_route.argtypes = [ctypes.POINTER(NwcMatrix), ctypes.POINTER(i32)]
     for name in ("nwc_encode", "nwc_encode_fp8", "nwc_quantize_fp8", "nwc_validate", "nwc_bind",
                  "nwc_decode", "nwc_gemv_prepare", "nwc_gemv", "nwc_gemv_noalloc", "nwc_gemv_batch_prepare",
                  "nwc_gemv_batch", "nwc_gather", "nwc_check", "nwc_decode_table", "nwc_gemv_next",
                  "nwc_dequantize_fp8", "nwc_file_save", "nwc_file_count", "nwc_file_entry", "nwc_file_find",
-                 "nwc_file_read", "nwc_file_load", "nwc_gemv_list"):
+                 "nwc_file_read", "nwc_file_load", "nwc_gemv_list", "nwc_gemv_route"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -266,6 +268,13 @@ class Matrix:
                                     ctypes.c_void_p(self.workspace.data_ptr()), self.ws_bytes, ctypes.byref(next.m),
                                     _stream_ptr(stream)), "nwc_gemv_next")
         return y
+
+    def route(self) -> int:
+        """The kernel gemv() launches for this matrix on the current device (nwc_gemv_route):
+        ROUTE_GEMV, ROUTE_CLUSTER or ROUTE_LIST."""
+        r = ctypes.c_int(-1)
+        _ok(lib().nwc_gemv_route(ctypes.byref(self.m), ctypes.byref(r)), "nwc_gemv_route")
+        return r.value
 
     def gemv_batch(self, x, y=None, stream=None):
         """Y (float32[nb, N]) = W x[v] for the nb <= 16 rows of x (BF16 [nb, K] as an int16/bfloat16

@@ -202,12 +202,31 @@ nwc_status nwc_gemv_prepare(const nwc_matrix *m, void *ws, size_t ws_bytes, nwc_
  * fused kernel): x is BF16[K] (16-byte
  * aligned), y is FP32[N], y_n = sum_k w[n,k] x[k] accumulated in FP32 (fp8: y_n = s_n * sum_k q x).
  * Finite inputs give |y_n - exact| <= 2^-10 * sum_k |w x| + 1e-6. ws/ws_bytes: a workspace
- * prepared by nwc_gemv_prepare for this matrix. Whatever the launch configuration (a tall
- * matrix with a device decode table runs the kernel of nwc_gemv_list), the column blocks' sums
- * are added in one fixed order, so results are bitwise repeatable.
+ * prepared by nwc_gemv_prepare for this matrix. Whatever the kernel (nwc_gemv_route), the
+ * column blocks' sums are added in one fixed order, so results are bitwise repeatable and equal
+ * to nwc_gemv_list's.
  */
 nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, size_t ws_bytes,
                     nwc_stream stream);
+
+/* Kernels nwc_gemv launches (nwc_gemv_route). */
+#define NWC_ROUTE_GEMV 0    /* one CTA per SM, blocks dealt round-robin; sums over column
+                               blocks through the workspace (partial sums and a ticket)     */
+#define NWC_ROUTE_CLUSTER 1 /* clusters of 2 or 4 CTAs, each taking whole row blocks; sums
+                               over column blocks in the cluster's distributed shared memory */
+#define NWC_ROUTE_LIST 2    /* the nwc_gemv_list kernel with one item (a tall matrix with a
+                               device decode table)                                          */
+
+/*
+ * nwc_gemv_route -- the kernel nwc_gemv launches for m on the current device: NWC_ROUTE_LIST
+ * when every SM's share of the blocks holds at least 32 whole row blocks and m->table is set;
+ * else NWC_ROUTE_CLUSTER when m has more than one column block and a cluster launch (whole row
+ * blocks per cluster) gives the busiest SM no more blocks than the round-robin launch and at most
+ * 8; else NWC_ROUTE_GEMV. The choice depends only on m's shape, m->table and the device (its SM
+ * count and how many clusters it holds at once). *route receives the value; NWC_ERR_CUDA when
+ * the device cannot be queried.
+ */
+nwc_status nwc_gemv_route(const nwc_matrix *m, int *route);
 
 /*
  * nwc_gemv_next -- nwc_gemv on m, which also brings the block regions, block table and decode

@@ -176,6 +176,9 @@ def test_gpu_entry_points_reject_bad_arguments_before_any_launch():
     assert L.nwc_gather(mp, P(0x60000), 0, P(0x50000), 1100, None) == 0        # nothing to do
     assert L.nwc_gather(mp, None, 3, P(0x50000), 1100, None) == 1
     assert L.nwc_gemv_noalloc(None, P(0x20000), P(0x30000), None) == 1
+    r = ctypes.c_int(-1)
+    assert L.nwc_gemv_route(None, ctypes.byref(r)) == 1
+    assert L.nwc_gemv_route(mp, None) == 1
 
 
 def test_batch_gemv_workspace_and_argument_checks():
