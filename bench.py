@@ -274,6 +274,30 @@ def extra_workloads(dev, stream, steps):
     del omats, wo, host, w, dec_o
     torch.cuda.empty_cache()
 
+    # A small matrix of the stack (the k projection, 1024x2560: five blocks per SM), which runs in
+    # clusters with its final sums in distributed shared memory; rotated copies beyond L2.
+    kn, kk = 1024, 2560
+    w = synth.normal_bf16((kn, kk), 0.02, 3, device=dev)
+    blob = encode_on_host(w)
+    kcopies = int(560e6 // len(blob)) + 1
+    host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+    kmats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(kcopies)]
+    xk = torch.from_numpy(synth.activations_bf16(kk, 1003).view(np.int16)).to(dev)
+    yk = torch.empty(kn, dtype=torch.float32, device=dev)
+    k_ms = time_graph(lambda: [m.gemv(xk, y=yk, stream=stream) for m in kmats], stream, max(3, steps // 10))
+    wk = [w.view(torch.bfloat16).clone() for _ in range(kcopies)]
+    ybk = torch.empty(kn, dtype=torch.bfloat16, device=dev)
+    k_bf16_ms = time_graph(lambda: [torch.mv(wc, xk.view(torch.bfloat16), out=ybk) for wc in wk], stream,
+                           max(3, steps // 10))
+    route = {nwc.ROUTE_GEMV: "round-robin", nwc.ROUTE_CLUSTER: "clusters", nwc.ROUTE_LIST: "list"}[kmats[0].route()]
+    out["k_proj_1024x2560"] = {
+        "workload": f"1024x2560 BF16 batch-1 GEMV, {kcopies} rotated copies", "kernel": route,
+        "us": k_ms * 1e3 / kcopies, "compressed_bytes": len(blob),
+        "frac_of_measured_hbm": (len(blob) + 2 * kk + 4 * kn) / (k_ms * 1e-3 / kcopies) / 1e9 / peak,
+        "bf16_cublas_us": k_bf16_ms * 1e3 / kcopies}
+    del kmats, wk, host, w
+    torch.cuda.empty_cache()
+
     # 36-layer decoder stack, one token = one GEMV per matrix (252), as one CUDA graph
     t0 = time.time()
     mats, xs, ys, wbf = [], {}, [], []
@@ -515,8 +539,9 @@ def run_batch_only(args):
 def run_only(args):
     """One workload of the pages' configurations alone (few launches, for profiling): the
     lm_head GEMV of the 151936x2560 table, the gather of 4096 ids from it, the fp8 gate / down
-    GEMV (12 rotated copies), the odd 4095x4100 BF16 GEMV (24 rotated copies) or the 24 rotated
-    4096x4096 copies as one nwc_gemv_list launch. One JSON line, not the benchmark contract's."""
+    GEMV (12 rotated copies), the odd 4095x4100 BF16 GEMV (24 rotated copies), the 24 rotated
+    4096x4096 copies as one nwc_gemv_list launch, or the 1024x2560 GEMV (the cluster kernel,
+    rotated copies beyond L2). One JSON line, not the benchmark contract's."""
     import torch
     import decode_gemv_nwc_gb300 as nwc
     from decode_gemv_nwc_gb300 import build, synth
@@ -556,6 +581,18 @@ def run_only(args):
         gbs = len(blob) / (ms * 1e-3) / 1e9
         out = {"workload": "24 rotated 4096x4096 copies as one nwc_gemv_list launch", "us_per_matrix": ms * 1e3,
                "compressed_gbs": gbs, "frac_of_hbm": gbs / peak}
+    elif name == "kproj":
+        w = synth.normal_bf16((1024, 2560), 0.02, 3, device=dev)
+        blob = encode_on_host(w)
+        host = torch.from_numpy(np.frombuffer(blob, np.uint8).copy())
+        mats = [nwc.Matrix(blob, device_blob=host.to(dev)) for _ in range(int(560e6 // len(blob)) + 1)]
+        x = torch.from_numpy(synth.activations_bf16(2560, 1003).view(np.int16)).to(dev)
+        y = torch.empty(1024, dtype=torch.float32, device=dev)
+        ms = time_graph(lambda: [mm.gemv(x, y=y, stream=stream) for mm in mats], stream, args.steps,
+                        args.warmup) / len(mats)
+        gbs = len(blob) / (ms * 1e-3) / 1e9
+        out = {"workload": f"1024x2560 BF16 GEMV, {len(mats)} rotated copies", "us": ms * 1e3,
+               "compressed_gbs": gbs, "frac_of_hbm": gbs / peak, "route": mats[0].route()}
     elif name == "odd":
         w = synth.normal_bf16((4095, 4100), 0.02, 1, device=dev)
         blob = encode_on_host(w)
@@ -597,7 +634,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline workload only")
     ap.add_argument("--only-batch", type=int, default=0, metavar="NB",
                     help="time only nwc_gemv_batch with NB vectors on the headline matrix")
-    ap.add_argument("--only", choices=["lm_head", "gather", "fp8_gate", "fp8_down", "odd", "list4096"],
+    ap.add_argument("--only", choices=["lm_head", "gather", "fp8_gate", "fp8_down", "odd", "list4096", "kproj"],
                     help="time only this workload (few launches; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
