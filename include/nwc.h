@@ -254,7 +254,7 @@ nwc_status nwc_gemv_next(const nwc_matrix *m, const uint16_t *x, float *y, void 
  * the GEMV on the stream; results equal nwc_gemv's. All calls share the one array, so calls that
  * overlap on the GPU (different streams, or different host threads without ordering) race.
  * The first call on a device resolves the array's device address with cudaGetSymbolAddress
- * (device current at that moment), so make that first call before any stream capture.
+ * (on the device current at that moment) and keeps it for later calls on that device.
  */
 nwc_status nwc_gemv_noalloc(const nwc_matrix *m, const uint16_t *x, float *y, nwc_stream stream);
 
