@@ -274,8 +274,8 @@ def extra_workloads(dev, stream, steps):
     del omats, wo, host, w, dec_o
     torch.cuda.empty_cache()
 
-    # A small matrix of the stack (the k projection, 1024x2560: five blocks per SM), which runs in
-    # clusters with its final sums in distributed shared memory; rotated copies beyond L2.
+    # A small matrix of the stack (the k projection, 1024x2560: five blocks per SM, where the
+    # launch's start-up and final sums weigh most); rotated copies beyond L2.
     kn, kk = 1024, 2560
     w = synth.normal_bf16((kn, kk), 0.02, 3, device=dev)
     blob = encode_on_host(w)
@@ -289,7 +289,7 @@ def extra_workloads(dev, stream, steps):
     ybk = torch.empty(kn, dtype=torch.bfloat16, device=dev)
     k_bf16_ms = time_graph(lambda: [torch.mv(wc, xk.view(torch.bfloat16), out=ybk) for wc in wk], stream,
                            max(3, steps // 10))
-    route = {nwc.ROUTE_GEMV: "round-robin", nwc.ROUTE_CLUSTER: "clusters", nwc.ROUTE_LIST: "list"}[kmats[0].route()]
+    route = {nwc.ROUTE_GEMV: "round-robin", nwc.ROUTE_LIST: "list"}[kmats[0].route()]
     out["k_proj_1024x2560"] = {
         "workload": f"1024x2560 BF16 batch-1 GEMV, {kcopies} rotated copies", "kernel": route,
         "us": k_ms * 1e3 / kcopies, "compressed_bytes": len(blob),
@@ -540,8 +540,8 @@ def run_only(args):
     """One workload of the pages' configurations alone (few launches, for profiling): the
     lm_head GEMV of the 151936x2560 table, the gather of 4096 ids from it, the fp8 gate / down
     GEMV (12 rotated copies), the odd 4095x4100 BF16 GEMV (24 rotated copies), the 24 rotated
-    4096x4096 copies as one nwc_gemv_list launch, or the 1024x2560 GEMV (the cluster kernel,
-    rotated copies beyond L2). One JSON line, not the benchmark contract's."""
+    4096x4096 copies as one nwc_gemv_list launch, or the 1024x2560 GEMV (rotated copies beyond
+    L2). One JSON line, not the benchmark contract's."""
     import torch
     import decode_gemv_nwc_gb300 as nwc
     from decode_gemv_nwc_gb300 import build, synth

@@ -30,7 +30,7 @@ class NwcError(RuntimeError):
 
 
 LIST_MAX = 256  # NWC_GEMV_LIST_MAX: products per nwc_gemv_list call
-ROUTE_GEMV, ROUTE_CLUSTER, ROUTE_LIST = 0, 1, 2  # NWC_ROUTE_*: the kernel nwc_gemv launches
+ROUTE_GEMV, ROUTE_LIST = 0, 2  # NWC_ROUTE_*: the kernel nwc_gemv launches
 
 
 class NwcMatrix(ctypes.Structure):
@@ -271,7 +271,7 @@ class Matrix:
 
     def route(self) -> int:
         """The kernel gemv() launches for this matrix on the current device (nwc_gemv_route):
-        ROUTE_GEMV, ROUTE_CLUSTER or ROUTE_LIST."""
+        ROUTE_GEMV or ROUTE_LIST."""
         r = ctypes.c_int(-1)
         _ok(lib().nwc_gemv_route(ctypes.byref(self.m), ctypes.byref(r)), "nwc_gemv_route")
         return r.value

@@ -957,206 +957,6 @@ __global__ void __launch_bounds__(GemvCfg<NB>::kWarps * 32, 1)
     if (bad) raise_error(kErrFormat);
 }
 
-// =================================================================== GEMV in clusters
-// y = W x with the sums over column blocks kept on chip. The CTAs run in clusters of cs (2 or
-// 4); cluster q of Q takes the whole row blocks [q R / Q, (q + 1) R / Q) and splits their blocks,
-// in row-block-major order, into cs contiguous shares, one per CTA, whose warps take every
-// warps-th block from the share's first one. A finished block's row sums go into the shared
-// memory of the cluster's first CTA, beside a ticket per row block; the warp that takes a row
-// block's last ticket adds its column blocks in the order finish_rows uses and writes y, so y is
-// bit for bit the same as with the other kernels. No partial sum reaches global memory.
-__device__ __forceinline__ uint32_t cluster_reg(int which) {
-    uint32_t r;
-    if (which == 0) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    else if (which == 1) asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    else if (which == 2) asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    else asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-// The address, in the cluster's shared window, of the same offset in the cluster's first CTA.
-__device__ __forceinline__ uint32_t in_rank0(uint32_t a) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Row block rb (the li-th of the cluster's) done: sum in the lanes transpose_reduce left it in.
-// tickets / slots: rank 0's ticket array and slot array, in the cluster window; slot (li, c, r)
-// at slots + 4 ((li cbs + c) 8 + r).
-template <int ELEM>
-__device__ __forceinline__ void cluster_finish(const Mat &m, float sum, int lane, uint64_t rb, uint64_t cb, uint32_t li,
-                                               float *y, uint32_t tickets, uint32_t slots) {
-    const uint64_t row = rb * kRows + (uint64_t)rowsel(lane);
-    if (m.cbs == 1) {
-        if ((lane & 3) == 0 && row < m.n) y[row] = ELEM == 0 ? sum : sum * m.scales[row];
-        return;
-    }
-    const uint32_t base = slots + 32u * li * (uint32_t)m.cbs;
-    if ((lane & 3) == 0)
-        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(base + 32u * (uint32_t)cb + 4u * (uint32_t)rowsel(lane)), "f"(sum)
-                     : "memory");
-    // the writer lanes' stores precede lane 0's release (warp barrier); the last ticket's
-    // acquire precedes its warp's loads (warp barrier)
-    __syncwarp();
-    uint32_t ticket = 0;
-    if (lane == 0)
-        asm volatile("atom.acq_rel.cluster.shared::cluster.add.u32 %0, [%1], 1;" : "=r"(ticket) : "r"(tickets + 4u * li) : "memory");
-    ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
-    if (ticket != (uint32_t)m.cbs - 1) return;
-    __syncwarp();
-    const uint32_t r2 = (uint32_t)(lane & 7);
-    const uint64_t grow = rb * kRows + r2;
-    float s = 0.0f;
-    if (grow < m.n)
-        for (uint32_t c2 = (uint32_t)lane >> 3; c2 < (uint32_t)m.cbs; c2 += 4) {
-            float v;
-            asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(base + 32u * c2 + 4u * r2) : "memory");
-            s += v;
-        }
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 8);
-    s += __shfl_xor_sync(0xFFFFFFFFu, s, 16);
-    if (lane < kRows && grow < m.n) y[grow] = ELEM == 0 ? s : s * m.scales[grow];
-}
-
-// red_off: the byte offset of the tickets (then the slots, 16-byte aligned) in every CTA's
-// shared memory, after the stages of the launched warps.
-template <int ELEM, bool KR>
-__global__ void __launch_bounds__(kGemvWarps * 32, 1)
-    gemv_cluster_kernel(Mat m, const uint16_t *__restrict__ x, float *__restrict__ y, uint32_t red_off, Prefetch pf) {
-    using S = Smem<kGemvWarps>;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t warps = blockDim.x >> 5;
-    const uint32_t bar = smem_u32(smem + S::kBar + 8 * warp), lut_bar = smem_u32(smem + S::kLutBar);
-    const uint32_t stage = smem_u32(smem + S::kStage + warp * kStageBytes);
-    const uint32_t rank = cluster_reg(0), cs = cluster_reg(1), q = cluster_reg(2), nq = cluster_reg(3);
-    // the cluster's row blocks [ra, rz) and this CTA's share [b0, b1) of their blocks
-    const uint64_t ra = m.rbs * q / nq, rz = m.rbs * (q + 1) / nq;
-    const uint64_t nbq = (rz - ra) * m.cbs;
-    const uint64_t b0 = ra * m.cbs + nbq * rank / cs, b1 = ra * m.cbs + nbq * (rank + 1) / cs;
-    const uint32_t tickets = in_rank0(smem_u32(smem + red_off));
-    const uint32_t slots = tickets + (uint32_t)up16(4 * (rz - ra));
-    if (rank == 0)
-        for (uint32_t i = threadIdx.x; i < (uint32_t)(rz - ra); i += blockDim.x)
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(smem + red_off) + 4u * i), "r"(0u) : "memory");
-
-    uint64_t b = b0 + warp;
-    uint32_t phase = 0;
-    bool bad = false, timed_out = false, inflight = false;
-    uint32_t c0 = 0, c1 = 0, n0 = 0, n1 = 0;
-    if (lane == 0 && b < b1) {
-        c0 = m.tab[b];
-        c1 = m.tab[b + 1];
-    }
-    if (lane == 0 && b + warps < b1) {
-        n0 = m.tab[b + warps];
-        n1 = m.tab[b + warps + 1];
-    }
-    c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
-    c1 = __shfl_sync(0xFFFFFFFFu, c1, 0);
-    auto issue = [&](uint32_t s0, uint32_t s1, bool reuse) {
-        const uint32_t bytes = 16 * (s1 - s0);
-        if (bytes <= (uint32_t)kStageBytes) {
-            if (lane == 0) {
-                if (reuse) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_expect_tx(bar, bytes);
-                tma_load_1d(stage, m.data + 16 * (uint64_t)s0, bytes, bar);
-            }
-            inflight = true;
-        }
-    };
-    if (lane == 0) {
-        mbar_init(bar);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    if (b < b1) issue(c0, c1, false);
-    lut_start(m, smem, lut_bar);
-    // the barriers, the table build and rank 0's zeroed tickets, for every thread of the cluster
-    cluster_sync_all();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t lutb = smem_u32(smem);
-    // the prefetch of the next matrix: one share per warp of the launch
-    const uint64_t w_id = (uint64_t)blockIdx.x * warps + warp, ways = (uint64_t)gridDim.x * warps;
-    bool prefetched = false, lut_ok = false;
-    while (b < b1 && !timed_out) {
-        const uint64_t nxt = b + warps, nn = nxt + warps;
-        uint32_t f0 = 0, f1 = 0;
-        if (lane == 0) {
-            if (nn < b1) {
-                f0 = m.tab[nn];
-                f1 = m.tab[nn + 1];
-            }
-            if (nxt < b1) l2_prefetch(m.data + 16 * (uint64_t)n0, 16 * (n1 - n0));
-        }
-        const uint32_t bytes = 16 * (c1 - c0);
-        const uint32_t rb32 = div_q((uint32_t)b, m.cdiv);
-        const uint64_t rb = rb32, cb = b - (uint64_t)rb32 * m.cbs;
-        const int rows = real_rows(m.n, rb);
-        const uint64_t kc64 = m.k - cb * kCols;
-        const int kc = kc64 < (uint64_t)kCols ? (int)kc64 : kCols;
-        const uint16_t *xb = x + cb * kCols;
-        float acc[1][8];
-#pragma unroll
-        for (int r = 0; r < 8; r++) acc[0][r] = 0.0f;
-        if (bytes <= (uint32_t)kStageBytes) {
-            uint32_t xs[1][8];
-            const int cl = kc - kLaneCols * lane, cols = cl < 0 ? 0 : (cl > kLaneCols ? kLaneCols : cl);
-            load_x16(xb + kLaneCols * lane, cols, xs[0]);
-            if (!mbar_wait(bar, phase & 1u)) {
-                timed_out = true;
-                break;
-            }
-            inflight = false;
-            phase ^= 1u;
-            if (!lut_ok) {
-                if (!lut_ready(m, lut_bar)) {
-                    timed_out = true;
-                    break;
-                }
-                lut_ok = true;
-            }
-            if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
-            prefetched = true;
-            if (KR && kc < kCols) gemv_block<ELEM, 1, KR>(stage, bytes, lane, lutb, xb, 0, xs, acc, bad, kc, rows);
-            else gemv_block<ELEM, 1, false>(stage, bytes, lane, lutb, xb, 0, xs, acc, bad, kCols, rows);
-        } else {
-            if (!lut_ok) {
-                if (!lut_ready(m, lut_bar)) {
-                    timed_out = true;
-                    break;
-                }
-                lut_ok = true;
-            }
-            if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
-            prefetched = true;
-            gemv_block_global<ELEM, 1>(m.data + 16 * (uint64_t)c0, bytes, lane, lutb, xb, 0, acc, bad, kc, rows);
-        }
-        const float sum = transpose_reduce(acc[0], lane);
-        cluster_finish<ELEM>(m, sum, lane, rb, cb, (uint32_t)(rb - ra), y, tickets, slots);
-        __syncwarp();
-        c0 = __shfl_sync(0xFFFFFFFFu, n0, 0);
-        c1 = __shfl_sync(0xFFFFFFFFu, n1, 0);
-        if (nxt < b1) issue(c0, c1, true);
-        n0 = f0;
-        n1 = f1;
-        b = nxt;
-    }
-    if (!prefetched && lane == 0) prefetch_share(pf, w_id, ways);
-    if (timed_out) {
-        raise_error(kErrTimeout);
-        if (inflight) mbar_wait(bar, phase & 1u);
-    }
-    if (m.table) mbar_wait(lut_bar, 0);
-    if (bad) raise_error(kErrFormat);
-    // rank 0's tickets and slots stay until every CTA of the cluster is done with them
-    cluster_sync_all();
-}
-
 // =================================================================== GEMV list
 // y_i = W_i x_i for up to kListMax independent products in one launch. The items' blocks are
 // numbered one after another (item by item, each in its blob's row-block-major order) and CTA c
@@ -2383,109 +2183,6 @@ cudaError_t launch_gemv_nb(const Mat &m, const uint16_t *x, int64_t ld_x, float 
                 : launch_gemv_k<ELEM, NB, false, false>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, grid, warps, stream);
 }
 
-// ---- the cluster GEMV's launch
-constexpr int kSmemOptIn = 232448 - 1024;  // dynamic shared memory per CTA (the opt-in limit less room for static)
-// The cluster launch is taken when its busiest SM gets no more blocks than the plain launch's
-// and at most this many. Measured (back to back, with programmatic dependent launch): at 1 and
-// 5 blocks per SM it is 0.5 us faster than the plain launch (its final sums stay on chip); at 11
-// to 40 blocks per SM it is 0.6-1.2 us slower, and slower in isolation at every size.
-#ifndef NWC_CLUSTER_MAX_LOAD
-#define NWC_CLUSTER_MAX_LOAD 8
-#endif
-constexpr uint64_t kClusterMaxLoad = NWC_CLUSTER_MAX_LOAD;
-
-template <class... A>
-cudaError_t launch_cluster_pdl(void (*kernel)(A...), int grid, int cs, int threads, int smem, cudaStream_t s, A... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)threads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)cs;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-// Clusters of cs CTAs (one per SM at this shared-memory size) that can be resident together on
-// the current device; 0 when the query fails.
-int max_clusters(int cs) {
-    static int count[kMaxDevices][2];
-    static bool known[kMaxDevices][2];
-    static std::mutex mu;
-    const int dev = current_device();
-    if (dev < 0 || (cs != 2 && cs != 4)) return 0;
-    const int i = cs == 2 ? 0 : 1;
-    if (!smem_ready<gemv_cluster_kernel<0, false>>(kSmemOptIn)) return 0;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!known[dev][i]) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)cs);
-        cfg.blockDim = dim3((unsigned)(kGemvWarps * 32));
-        cfg.dynamicSmemBytes = (size_t)kSmemOptIn;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemv_cluster_kernel<0, false>, &cfg) != cudaSuccess) {
-            (void)cudaGetLastError();
-            n = 0;
-        }
-        count[dev][i] = n;
-        known[dev][i] = true;
-    }
-    return count[dev][i];
-}
-
-struct ClusterPlan {
-    int cs, clusters, warps, smem;
-    uint32_t red_off;
-    uint64_t load;  // blocks of the busiest CTA
-};
-// The cluster launch for m, if one fits, gives the busiest SM no more blocks than the plain
-// launch and at most kClusterMaxLoad.
-bool cluster_plan(const Mat &m, int sms, ClusterPlan &best) {
-    if (m.cbs <= 1) return false;
-    using S = Smem<kGemvWarps>;
-    const uint64_t plain = cdiv(m.nb, m.nb < (uint64_t)sms ? m.nb : (uint64_t)sms);
-    bool found = false;
-    for (int cs : {2, 4}) {
-        uint64_t q = (uint64_t)max_clusters(cs);
-        if ((uint64_t)(sms / cs) < q) q = (uint64_t)(sms / cs);
-        if (m.rbs < q) q = m.rbs;
-        if (q == 0) continue;
-        const uint64_t rq = cdiv(m.rbs, q), load = cdiv(rq * m.cbs, (uint64_t)cs);
-        const uint64_t rounds = cdiv(load, (uint64_t)kGemvWarps);
-        const int warps = (int)cdiv(load, rounds);
-        const uint64_t red_off = up16((uint64_t)S::kStage + (uint64_t)warps * kStageBytes + kStageSlack);
-        const uint64_t smem = red_off + up16(4 * rq) + 32 * rq * m.cbs;
-        if (smem > (uint64_t)kSmemOptIn) continue;
-        if (!found || load < best.load) {
-            best = ClusterPlan{cs, (int)q, warps, (int)smem, (uint32_t)red_off, load};
-            found = true;
-        }
-    }
-    return found && best.load <= plain && best.load <= kClusterMaxLoad;
-}
-
-template <int ELEM, bool KR>
-cudaError_t launch_cluster_k(const Mat &m, const uint16_t *x, float *y, const Prefetch &pf, const ClusterPlan &pl,
-                             cudaStream_t stream) {
-    if (!smem_ready<gemv_cluster_kernel<ELEM, KR>>(kSmemOptIn)) return cudaErrorInvalidConfiguration;
-    return launch_cluster_pdl(gemv_cluster_kernel<ELEM, KR>, pl.cs * pl.clusters, pl.cs, pl.warps * 32, pl.smem, stream, m,
-                              x, y, pl.red_off, pf);
-}
-
 template <int ELEM, bool KR>
 cudaError_t launch_list(const ListParams &p, int grid, cudaStream_t s);
 
@@ -2518,11 +2215,9 @@ void set_item(ListParams &p, int i, const Mat &m, const uint16_t *x, float *y, f
 // Which kernel the GEMV of m for nb vectors (with a next matrix to prefetch or not) launches.
 // A tall matrix (every SM's share of the blocks holds at least 32 whole row blocks) runs the
 // list kernel with one item: its whole row blocks are summed by one warp each, without partial
-// sums, with the same y bit for bit (the list kernel needs the device decode table). A small
-// one may run in clusters (cluster_plan).
-int route_of(const Mat &m, int nb, bool next, int sms, ClusterPlan &pl) {
+// sums, with the same y bit for bit (the list kernel needs the device decode table).
+int route_of(const Mat &m, int nb, bool next, int sms) {
     if (nb == 1 && !next && m.table && m.cbs > 1 && m.rbs >= 33 * (uint64_t)sms) return NWC_ROUTE_LIST;
-    if (nb == 1 && cluster_plan(m, sms, pl)) return NWC_ROUTE_CLUSTER;
     return NWC_ROUTE_GEMV;
 }
 
@@ -2532,9 +2227,7 @@ nwc_status launch_gemv(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, 
                        uint32_t *counters, uint64_t n_pad, cudaStream_t stream, const nwc_matrix *next = nullptr) {
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
-    ClusterPlan pl;
-    const int route = route_of(m, nb, next != nullptr, sms, pl);
-    if (route == NWC_ROUTE_LIST) {
+    if (route_of(m, nb, next != nullptr, sms) == NWC_ROUTE_LIST) {
         ListParams &p = list_params();
         p.count = 1;
         p.total = 0;
@@ -2555,11 +2248,7 @@ nwc_status launch_gemv(const Mat &m, const uint16_t *x, int64_t ld_x, float *y, 
         pf.table = next->table;
     }
     cudaError_t rc;
-    if (route == NWC_ROUTE_CLUSTER) {
-        const bool kr = k_ragged(m);
-        if (m.elem == NWC_ELEM_BF16) rc = kr ? launch_cluster_k<0, true>(m, x, y, pf, pl, stream) : launch_cluster_k<0, false>(m, x, y, pf, pl, stream);
-        else rc = kr ? launch_cluster_k<1, true>(m, x, y, pf, pl, stream) : launch_cluster_k<1, false>(m, x, y, pf, pl, stream);
-    } else if (nb == 1)
+    if (nb == 1)
         rc = m.elem == NWC_ELEM_BF16 ? launch_gemv_nb<0, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream)
                                      : launch_gemv_nb<1, 1>(m, x, ld_x, y, ld_y, partial, counters, n_pad, pf, sms, stream);
     else
@@ -2589,8 +2278,7 @@ extern "C" nwc_status nwc_gemv_route(const nwc_matrix *mp, int *route) {
     if (!mp || !route) return NWC_ERR_INVALID_ARG;
     const int sms = sm_count();
     if (sms <= 0) return NWC_ERR_CUDA;
-    ClusterPlan pl;
-    *route = route_of(to_mat(*mp), 1, false, sms, pl);
+    *route = route_of(to_mat(*mp), 1, false, sms);
     return NWC_OK;
 }
 

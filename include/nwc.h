@@ -210,21 +210,16 @@ nwc_status nwc_gemv(const nwc_matrix *m, const uint16_t *x, float *y, void *ws, 
                     nwc_stream stream);
 
 /* Kernels nwc_gemv launches (nwc_gemv_route). */
-#define NWC_ROUTE_GEMV 0    /* one CTA per SM, blocks dealt round-robin; sums over column
-                               blocks through the workspace (partial sums and a ticket)     */
-#define NWC_ROUTE_CLUSTER 1 /* clusters of 2 or 4 CTAs, each taking whole row blocks; sums
-                               over column blocks in the cluster's distributed shared memory */
-#define NWC_ROUTE_LIST 2    /* the nwc_gemv_list kernel with one item (a tall matrix with a
-                               device decode table)                                          */
+#define NWC_ROUTE_GEMV 0 /* one CTA per SM, blocks dealt round-robin; sums over column blocks
+                            through the workspace (partial sums and a ticket)                 */
+#define NWC_ROUTE_LIST 2 /* the nwc_gemv_list kernel with one item (a tall matrix with a
+                            device decode table)                                              */
 
 /*
  * nwc_gemv_route -- the kernel nwc_gemv launches for m on the current device: NWC_ROUTE_LIST
- * when every SM's share of the blocks holds at least 32 whole row blocks and m->table is set;
- * else NWC_ROUTE_CLUSTER when m has more than one column block and a cluster launch (whole row
- * blocks per cluster) gives the busiest SM no more blocks than the round-robin launch and at most
- * 8; else NWC_ROUTE_GEMV. The choice depends only on m's shape, m->table and the device (its SM
- * count and how many clusters it holds at once). *route receives the value; NWC_ERR_CUDA when
- * the device cannot be queried.
+ * when m has more than one column block, m->table is set and every SM's share of the blocks
+ * holds at least 32 whole row blocks (row blocks >= 33 x the SM count); else NWC_ROUTE_GEMV.
+ * *route receives the value; NWC_ERR_CUDA when the device's SM count cannot be read.
  */
 nwc_status nwc_gemv_route(const nwc_matrix *m, int *route);
 

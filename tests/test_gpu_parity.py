@@ -893,10 +893,10 @@ def test_tall_matrix_through_the_list_kernel_equals_the_single_kernel(elem):
     assert np.array_equal(y.view(np.uint64), y_single.view(np.uint64))
 
 
-# small shapes run in clusters on a 152-SM GB300 (the final sums in distributed shared memory);
-# 4096x4096 runs the round-robin kernel and 41000x1030 the list kernel
-ROUTES_152 = {(13, 700): nwc.ROUTE_CLUSTER, (72, 1500): nwc.ROUTE_CLUSTER, (1000, 1030): nwc.ROUTE_CLUSTER,
-              (1024, 2560): nwc.ROUTE_CLUSTER, (4096, 4096): nwc.ROUTE_GEMV, (41000, 1030): nwc.ROUTE_LIST}
+# every shape below runs the round-robin kernel on a 152-SM GB300 except 41000x1030 (the list
+# kernel)
+ROUTES_152 = {(13, 700): nwc.ROUTE_GEMV, (72, 1500): nwc.ROUTE_GEMV, (1000, 1030): nwc.ROUTE_GEMV,
+              (1024, 2560): nwc.ROUTE_GEMV, (4096, 4096): nwc.ROUTE_GEMV, (41000, 1030): nwc.ROUTE_LIST}
 
 
 @pytest.mark.parametrize("elem", [nwc.BF16, nwc.FP8])
@@ -905,7 +905,7 @@ def test_every_route_equals_the_list_kernel_bitwise(shape, elem):
     """nwc_gemv through the kernel nwc_gemv_route names equals nwc_gemv_list with the matrix as
     its only item bit for bit (one fixed order of the column blocks' sums in every kernel), and
     the oracle within tolerance on every row; ragged K (700, 1030) takes the edge layout. Twice
-    in a row, so the on-chip tickets and the workspace both start clean each call."""
+    in a row, so the workspace is back in its prepared state after each call."""
     n, k = shape
     w = synth.normal_bf16((n, k), 0.02, seed=n + k)
     blob = nwc.encode(w, elem=elem)
@@ -922,22 +922,3 @@ def test_every_route_equals_the_list_kernel_bitwise(shape, elem):
     yl = yl.cpu().numpy().astype(np.float64)
     assert np.array_equal(y.view(np.uint64), y2.view(np.uint64))
     assert np.array_equal(y.view(np.uint64), yl.view(np.uint64))
-
-
-def test_cluster_route_with_next_prefetch_and_no_table():
-    """The cluster kernel with a next matrix to prefetch (nwc_gemv_next) and with the decode table
-    built in the kernel (no device table): y bit for bit the plain call's."""
-    w = synth.normal_bf16((1024, 2560), 0.02, seed=5)
-    blob = nwc.encode(w)
-    x = dev_bits(synth.activations_bf16(2560, 9))
-    m, other = nwc.Matrix(blob), nwc.Matrix(nwc.encode(synth.normal_bf16((4096, 4096), 0.02, seed=6)))
-    notable = nwc.Matrix(blob, table=False)
-    y = m.gemv(x)
-    yn = m.gemv(x, next=other)
-    yt = notable.gemv(x)
-    torch.cuda.synchronize()
-    assert_clean()
-    if nwc.sm_count() == 152:
-        assert notable.route() == nwc.ROUTE_CLUSTER
-    assert torch.equal(y.view(torch.int32), yn.view(torch.int32))
-    assert torch.equal(y.view(torch.int32), yt.view(torch.int32))
