@@ -21,8 +21,9 @@
 // is a BF16 with exponent field v + 120 and mantissa m << 4 (zeros keep field 0, subnormal and
 // NaN codes are listed), so fp8 runs through the same BF16 arithmetic.
 //
-// GB300 choices: the GEMV is a persistent grid of one 32-warp CTA per SM (block b on CTA
-// b % grid); each warp streams whole block regions from HBM into its own shared-memory stage
+// GB300 choices: the GEMV is a persistent grid of one CTA per SM (block b on CTA b % grid) with
+// up to 32 warps, as few as keep the number of rounds of blocks so that no warp of the last
+// round decodes alone; each warp streams whole block regions from HBM into its own shared-memory stage
 // with one TMA bulk copy (cp.async.bulk, completion on an mbarrier, bounded waits) and
 // prefetches its next region into L2; the decode table is copied in by TMA from a device copy
 // prepared once per matrix (or built by the CTA when there is none) while the first regions
@@ -30,9 +31,12 @@
 // spreads the two raw bytes (sign replicated into the high byte) and a LOP3 that merges them
 // with the table's exponents into a BF16x2, then two FMAs with BF16 operands and FP32
 // accumulators; the window is refilled every two pairs. Cross-column-block sums: every warp
-// stores its partial sums, takes a ticket and, in the same round trip, loads the other column
-// blocks' partial sums of its row block; the last warp adds them in a fixed order (partials
-// not yet visible read as a sentinel and are loaded again), writes y and resets the slots.
+// stores its partial sums and takes a ticket; the warp with the last ticket adds the column
+// blocks' partial sums of its row block in a fixed order, writes y and resets the slots. When
+// warps have further blocks, each loads the other partials while its ticket is in flight
+// (partials not yet visible read as a sentinel and are loaded again); otherwise the ticket is an
+// acquire-release atomic and only the last warp loads. The list kernel sums the row blocks that
+// lie wholly in one SM's share inside one warp, without partial sums.
 // The kernel is launched with programmatic stream serialization: it may start while the
 // previous kernel on the stream drains and waits for it before touching x, the workspace or y.
 // The small-batch GEMV keeps the decoder and moves the products with three or more vectors to
